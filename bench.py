@@ -1,0 +1,465 @@
+"""Benchmark of the block-scaled 4-bit hot path on GB300.
+
+Headline workload (one step): the decode qmv sweep over a hidden-5120 dense
+stack -- 64 layers x (q, k, v, o 5120x5120; gate, up 17408x5120; down
+5120x17408) -- against NVFP4 weights (group 16, E4M3 scales, fp32 global
+scale), bf16 activations, fp32 accumulation.  `value` is weight-bytes GB/s
+(packed codes + block scales) with weights resident in HBM; the stack (13.4 GB)
+is far larger than L2, so no flush is needed between steps.  The same line
+reports the other formats (MXFP4, affine-4 g64), the activation quantize, the
+NVFP4 prefill qqmm and the MXFP4 MoE gather_qmm as components.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs an independent replica (the path has no
+exchange step), timings are max-reduced, value = all ranks' bytes / time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_scaled_fp4_fp_gb300 import synth  # noqa: E402
+
+METRIC = "FP4 qmv weight GB/s (% of HBM peak); NVFP4 qqmm TFLOPS (% of FP4 peak)"
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / bf16 tensor ratio on GB300
+
+
+# --------------------------------------------------------------------------- utils
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash(name: str) -> str:
+    p = os.path.join(ROOT, "block_scaled_fp4_fp_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (p, os.path.join(ROOT, "block_scaled_fp4_fp_gb300", "csrc", "common.cuh")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_file: str, key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(key)
+    if not d or d.get("source_hash") != kernel_source_hash(kernel_file):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- decode stack
+class DecodeStack:
+    """64-layer weight stack in one format, weights resident on the device."""
+
+    def __init__(self, B, mode: int, layers: int, device):
+        self.B, self.mode, self.layers = B, mode, layers
+        self.mats = []
+        self.bytes = 0
+        for l in range(layers):
+            for p, (name, N, K) in enumerate(synth.LAYER_PROJECTIONS):
+                seed = synth.layer_seed(l, p)
+                self.mats.append(self._make(N, K, seed, device))
+        self.x = {K: synth.bf16_normal((K,), 1.0, seed=7 + K, device=device)
+                  for K in {k for _, _, k in synth.LAYER_PROJECTIONS}}
+        self.y = [torch.empty((m["N"],), dtype=torch.bfloat16, device=device) for m in self.mats]
+
+    def _make(self, N, K, seed, device):
+        B = self.B
+        if self.mode == B.MODE_AFFINE:
+            # synthetic affine-4 g64 weights: uniform codes, per-group bf16 scale/bias in the
+            # range the affine quantizer gives for N(0, 0.02) groups (scale ~ 0.11/15, bias ~ -0.055)
+            g = torch.Generator(device=device)
+            g.manual_seed(seed)
+            q = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), generator=g, device=device, dtype=torch.int64)
+            q = q.to(torch.int32)
+            s = (0.11 / 15 * (1 + 0.1 * torch.rand((N, K // 64), generator=g, device=device))).to(torch.bfloat16)
+            b = (-0.055 * (1 + 0.1 * torch.rand((N, K // 64), generator=g, device=device))).to(torch.bfloat16)
+            nbytes = q.numel() * 4 + s.numel() * 2 + b.numel() * 2
+            self.bytes += nbytes
+            return {"N": N, "K": K, "q": q, "s": s, "b": b, "gs": None, "bytes": nbytes}
+        w = synth.bf16_normal((N, K), 0.02, seed=seed, device=device)
+        gs = B.fp4_amax_global_scale(w) if self.mode == B.MODE_NVFP4 else None
+        q, s = B.fp4_quantize(w, self.mode, global_scale=gs)
+        del w
+        nbytes = q.numel() * 4 + s.numel()
+        self.bytes += nbytes
+        return {"N": N, "K": K, "q": q, "s": s, "b": None, "gs": gs, "bytes": nbytes}
+
+    def step(self, stream=None):
+        B = self.B
+        for m, y in zip(self.mats, self.y):
+            B.qmv(self.x[m["K"]], m["q"], m["s"], m["b"], m["gs"], mode=self.mode, y=y, stream=stream)
+
+    @property
+    def launches(self):
+        return len(self.mats)
+
+
+def time_graph(graph, steps, warmup, stream):
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(stream)  # warm (loads kernels, sets attributes) outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+    torch.cuda.synchronize()
+    return g
+
+
+# ------------------------------------------------------------------ components
+def bench_quantize(B, device, reps=30):
+    """Activation quantize 4096x5120 (0.1 % outliers x50), tiled scales; 4 rotating inputs."""
+    xs = [synth.activations_with_outliers(4096, 5120, seed=i, outlier_seed=100 + i, device=device) for i in range(4)]
+    res = {}
+    for mode, name in ((B.MODE_NVFP4, "nvfp4"), (B.MODE_MXFP4, "mxfp4")):
+        gss = [B.fp4_amax_global_scale(x) if mode == B.MODE_NVFP4 else None for x in xs]
+        outs = [B.fp4_quantize(x, mode, global_scale=g, layout=B.SCALES_TILED) for x, g in zip(xs, gss)]
+        times = []
+        for r in range(reps + 3):
+            i = r % 4
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.fp4_quantize(xs[i], mode, global_scale=gss[i], layout=B.SCALES_TILED, xq=outs[i][0], scales=outs[i][1])
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        nbytes = 4096 * 5120 * 2 + 4096 * 5120 // 2 + outs[0][1].numel()
+        res[name] = {"ms": ms, "GB/s": nbytes / ms / 1e6, "bytes": nbytes}
+    return res
+
+
+def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=10):
+    N, K = 17408, 5120
+    w = synth.bf16_normal((N, K), 0.02, seed=1, device=device)
+    gw = B.fp4_amax_global_scale(w)
+    wq, ws = B.fp4_quantize(w, B.MODE_NVFP4, global_scale=gw, layout=B.SCALES_TILED)
+    del w
+    res = {}
+    for M in Ms:
+        x = synth.bf16_normal((M, K), 1.0, seed=2, device=device)
+        gx = B.fp4_amax_global_scale(x)
+        xq, xs = B.fp4_quantize(x, B.MODE_NVFP4, global_scale=gx, layout=B.SCALES_TILED)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        times = []
+        for r in range(reps + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        flops = 2.0 * M * N * K
+        res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}
+        del x, xq, xs, out
+    return res
+
+
+def bench_gather(B, device, reps=10):
+    tokens, E, topk, N, K = 2048, 32, 4, 5760, 2880
+    lhs, rhs = synth.moe_routing(tokens, E, topk, seed=0)
+    lhs_d, rhs_d = torch.from_numpy(lhs).to(device), torch.from_numpy(rhs).to(device)
+    x = synth.bf16_normal((tokens, K), 1.0, seed=1, device=device)
+    w = synth.bf16_normal((E * N, K), 0.02, seed=2, device=device)
+    q, s = B.fp4_quantize(w, B.MODE_MXFP4)
+    del w
+    q3, s3 = q.view(E, N, K // 8), s.view(E, N, K // 32)
+    out = torch.empty((len(lhs), N), dtype=torch.bfloat16, device=device)
+    times = []
+    for r in range(reps + 3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    flops = 2.0 * len(lhs) * N * K
+    return {"gate_up": {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_layer_sample(mode_name="nvfp4"):
+    """Oracle qmv over layer 0's seven NVFP4 projections (weights generated on
+    the CPU and quantized by the oracle, untimed); returns (seconds, bytes)."""
+    import oracle
+    mats = []
+    for p, (name, N, K) in enumerate(synth.LAYER_PROJECTIONS):
+        w = synth.to_u16(synth.bf16_normal((N, K), 0.02, seed=synth.layer_seed(0, p)))
+        gs = oracle.global_scale(w)
+        q, s = oracle.nvfp4_quantize(w, gs)
+        mats.append((q, s, gs, K))
+    xs = {K: synth.to_u16(synth.bf16_normal((K,), 1.0, seed=7 + K)) for K in (synth.HIDDEN, synth.MLP)}
+    nbytes = sum(q.nbytes + s.nbytes for q, s, _, _ in mats)
+    t0 = time.perf_counter()
+    for q, s, gs, K in mats:
+        oracle.qmv(xs[K], q, s, None, oracle.MODE_NVFP4, 16, gs)
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------------ main
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    times, nbytes = [], 0
+    for i in range(args.warmup + args.steps):
+        t, nbytes = oracle_layer_sample()
+        if i >= args.warmup:
+            times.append(t)
+    sec = statistics.median(times)
+    v = nbytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode qmv, NVFP4 weights (hidden 5120, MLP 17408); oracle on layer 0 (7 projections)",
+                   "l2": "inputs larger than L2 per step"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "layer 0 of 64: q,k,v,o,gate,up,down NVFP4 GEMV in the C oracle (fp64)"},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from block_scaled_fp4_fp_gb300 import binding as B
+    B.fp4_init(local)
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(device)
+
+    modes = [("nvfp4", B.MODE_NVFP4)] + ([] if args.quick else [("mxfp4", B.MODE_MXFP4), ("affine_g64", B.MODE_AFFINE)])
+    results = {}
+    headline = None
+    for name, mode in modes:
+        stack = DecodeStack(B, mode, args.layers, device)
+        graph = capture(stack.step, stream)
+        if name == "nvfp4":
+            with ClockSampler(local) as clk:
+                if ws > 1:
+                    torch.distributed.barrier()
+                ms = time_graph(graph, args.steps, args.warmup, stream)
+            clocks = clk.summary()
+            headline = (stack, graph, ms)
+        else:
+            ms = time_graph(graph, args.steps, args.warmup, stream)
+        results[name] = {"ms_per_step": ms, "GB/s": stack.bytes / ms / 1e6, "bytes_per_step": stack.bytes,
+                         "launches_per_step": stack.launches}
+        if name != "nvfp4":
+            del stack, graph
+            torch.cuda.empty_cache()
+
+    stack, graph, ms = headline
+    # e2e: pinned host activations in, every projection's output back, through the C ABI
+    hx = {k: v.cpu().pin_memory() for k, v in stack.x.items()}
+    hy = torch.empty((sum(m["N"] for m in stack.mats),), dtype=torch.bfloat16).pin_memory()
+    dy = torch.empty_like(hy, device=device)
+    ys = []
+    off = 0
+    for m in stack.mats:
+        ys.append(dy[off:off + m["N"]])
+        off += m["N"]
+    stack.y = ys
+
+    def e2e_step(s):
+        for k in stack.x:
+            stack.x[k].copy_(hx[k], non_blocking=True)
+        stack.step(s)
+        hy.copy_(dy, non_blocking=True)
+
+    g2 = capture(e2e_step, stream)
+    e2e_ms = time_graph(g2, args.steps, args.warmup, stream)
+    h2d = sum(v.numel() * 2 for v in hx.values())
+    d2h = hy.numel() * 2
+
+    # max over ranks
+    t = torch.tensor([ms, e2e_ms], device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms = t.tolist()
+    value = ws * stack.bytes / ms / 1e6
+    comps = {"decode_qmv": results}
+    if not args.quick and rank == 0:
+        comps["quantize_4096x5120"] = bench_quantize(B, device)
+        comps["qqmm_nvfp4_Mx17408x5120"] = bench_qqmm(B, device)
+        comps["gather_qmm_mxfp4_moe"] = bench_gather(B, device)
+        fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        for k, v in comps["qqmm_nvfp4_Mx17408x5120"].items():
+            v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
+        for k, v in comps["gather_qmm_mxfp4_moe"].items():
+            v["frac_of_bf16_peak"] = v["TFLOP/s"] / peaks["bf16_tflops"]
+        for k, v in comps["quantize_4096x5120"].items():
+            v["frac_of_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        sec, nb = oracle_layer_sample()
+        cpu = {"value": nb / sec / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": "layer 0 of 64 (q,k,v,o,gate,up,down), NVFP4 GEMV in the C oracle, fp64, weights "
+                         "quantized by the oracle (untimed)"}
+    if rank == 0:
+        per_launch_bytes = stack.bytes / stack.launches
+        achieved = stack.bytes / ms / 1e6
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp4-e2m1 x bf16, f32 acc", "data": "synthetic",
+            "config": {"workload": "decode qmv over a 64-layer hidden-5120 stack (q,k,v,o 5120x5120; gate,up "
+                                   "17408x5120; down 5120x17408), NVFP4 g16 weights, bf16 x, one token",
+                       "layers": args.layers, "weight_bytes_per_step": stack.bytes,
+                       "tokens_per_s": 1e3 / ms, "l2": "inputs larger than L2 (13.4 GB stack)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": committed_traffic("qmv.cu", "qmv_nvfp4_decode"),
+                         "kernel": "qmv_kernel<NVFP4>", "bytes_per_launch": per_launch_bytes,
+                         "peak_src": peaks["src"] + " hbm_gbs"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * stack.bytes / e2e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": stack.launches * args.steps,
+            "clocks": clocks,
+            "components": comps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=synth.LAYERS)
+    ap.add_argument("--quick", action="store_true", help="headline only (no other formats/components)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+"""Thin Python binding of libfp4gb300 (ctypes).
+
+Functions carry the C ABI's names and only marshal arguments: shapes and
+device pointers of torch tensors, the current CUDA stream, and output
+allocation with torch (PyTorch is the memory allocator here, nothing more).
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU fallback -- if the shared library is missing the first call raises.
+
+Packed 4-bit codes are held in ``torch.int32`` tensors (uint32 bit patterns),
+scales in ``torch.uint8`` (NVFP4/MXFP4) or ``torch.bfloat16`` (affine).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp4gb300.so")
+
+FP4_OK, FP4_ERR_INVALID_ARG, FP4_ERR_UNSUPPORTED, FP4_ERR_ALIGNMENT, FP4_ERR_CUDA, FP4_ERR_TIMEOUT = range(6)
+MODE_AFFINE, MODE_MXFP4, MODE_NVFP4 = 0, 1, 2
+SCALES_LINEAR, SCALES_TILED = 0, 1
+GROUP = {MODE_NVFP4: 16, MODE_MXFP4: 32, MODE_AFFINE: 64}
+
+_lock = threading.Lock()
+_lib = None
+
+# (name, restype, argtypes) of every entry point the header declares
+c = ctypes
+_VP, _I64, _INT, _F = c.c_void_p, c.c_int64, c.c_int, c.c_float
+SIGNATURES = {
+    "fp4_init": (_INT, [_INT]),
+    "fp4_status_string": (c.c_char_p, [_INT]),
+    "fp4_check_device_error": (_INT, [_VP]),
+    "fp4_padded_scale_dims": (None, [_I64, _I64, c.POINTER(_I64), c.POINTER(_I64)]),
+    "fp4_amax_workspace_bytes": (c.c_size_t, [_I64]),
+    "fp4_amax_global_scale": (_INT, [_VP, _I64, _VP, _VP, _VP, c.c_size_t, _VP]),
+    "fp4_quantize": (_INT, [_VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP, _VP, _INT, _VP]),
+    "fp4_dequantize": (_INT, [_VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _INT, _VP, _VP]),
+    "qmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
+    "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
+    "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
+                          _VP, _VP]),
+    "fp4_debug_inject_wait_timeout": (_INT, [_INT]),
+}
+
+
+class Fp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib():
+    """Load libfp4gb300.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fp4_status_string(int(status)).decode()
+
+
+def _check(st: int, where: str):
+    if st != FP4_OK:
+        raise Fp4Error(st, where)
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def padded_scale_dims(rows: int, scale_cols: int):
+    pr, pc = c.c_int64(), c.c_int64()
+    lib().fp4_padded_scale_dims(rows, scale_cols, c.byref(pr), c.byref(pc))
+    return pr.value, pc.value
+
+
+def fp4_init(device: int = 0):
+    _check(lib().fp4_init(device), "fp4_init")
+
+
+def fp4_check_device_error(stream=None) -> int:
+    """Returns the status (FP4_OK or FP4_ERR_TIMEOUT...) without raising."""
+    return lib().fp4_check_device_error(_s(stream))
+
+
+def fp4_amax_global_scale(x: torch.Tensor, gs_out=None, amax_out=None, ws=None, stream=None):
+    n = x.numel()
+    if gs_out is None:
+        gs_out = torch.empty((), dtype=torch.float32, device=x.device)
+    wsb = lib().fp4_amax_workspace_bytes(n)
+    if ws is None:
+        ws = torch.empty(wsb, dtype=torch.uint8, device=x.device)
+    _check(lib().fp4_amax_global_scale(_p(x), n, _p(gs_out), _p(amax_out), _p(ws), ws.numel() * ws.element_size(),
+                                       _s(stream)), "fp4_amax_global_scale")
+    return gs_out
+
+
+def scales_shape(rows: int, cols: int, group: int, layout: int):
+    if layout == SCALES_TILED:
+        return padded_scale_dims(rows, cols // group)
+    return rows, cols // group
+
+
+def fp4_quantize(x: torch.Tensor, mode: int, group_size: int = None, global_scale=None,
+                 layout: int = SCALES_LINEAR, xq=None, scales=None, stream=None):
+    group_size = group_size or GROUP[mode]
+    rows, cols = x.shape
+    if xq is None:
+        xq = torch.empty((rows, cols // 8), dtype=torch.int32, device=x.device)
+    if scales is None:
+        scales = torch.empty(scales_shape(rows, cols, group_size, layout), dtype=torch.uint8, device=x.device)
+    _check(lib().fp4_quantize(_p(x), rows, cols, mode, 4, group_size, _p(global_scale), _p(xq), _p(scales), layout,
+                              _s(stream)), "fp4_quantize")
+    return xq, scales
+
+
+def fp4_dequantize(wq: torch.Tensor, scales: torch.Tensor, biases=None, mode: int = MODE_NVFP4,
+                   group_size: int = None, global_scale=None, layout: int = SCALES_LINEAR, out=None,
+                   stream=None, rows: int = None):
+    group_size = group_size or GROUP[mode]
+    rows = rows if rows is not None else wq.shape[0]
+    cols = wq.shape[-1] * 8
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16, device=wq.device)
+    _check(lib().fp4_dequantize(_p(wq), _p(scales), _p(biases), rows, cols, mode, 4, group_size,
+                                _p(global_scale), layout, _p(out), _s(stream)), "fp4_dequantize")
+    return out
+
+
+def qmv(x: torch.Tensor, w: torch.Tensor, scales: torch.Tensor, biases=None, global_scale_w=None,
+        mode: int = MODE_NVFP4, group_size: int = None, y=None, stream=None):
+    group_size = group_size or GROUP[mode]
+    N, K = w.shape[0], w.shape[1] * 8
+    if y is None:
+        y = torch.empty((N,), dtype=torch.bfloat16, device=w.device)
+    _check(lib().qmv(_p(x), _p(w), _p(scales), _p(biases), _p(global_scale_w), N, K, mode, 4, group_size, _p(y),
+                     _s(stream)), "qmv")
+    return y
+
+
+def qqmm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor, global_scale_x=None,
+         global_scale_w=None, mode: int = MODE_NVFP4, out=None, stream=None, M: int = None):
+    M = M if M is not None else xq.shape[0]
+    N, K = wq.shape[0], wq.shape[1] * 8
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=wq.device)
+    _check(lib().qqmm(_p(xq), _p(sx), _p(wq), _p(sw), _p(global_scale_x), _p(global_scale_w), M, N, K, mode,
+                      _p(out), _s(stream)), "qqmm")
+    return out
+
+
+def gather_qmm(x: torch.Tensor, lhs_idx: torch.Tensor, rhs_idx: torch.Tensor, w: torch.Tensor,
+               scales: torch.Tensor, biases=None, mode: int = MODE_MXFP4, group_size: int = None,
+               sorted_indices: bool = True, out=None, stream=None):
+    group_size = group_size or GROUP[mode]
+    R = lhs_idx.numel()
+    E, N, K = w.shape[0], w.shape[1], w.shape[2] * 8
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.bfloat16, device=w.device)
+    _check(lib().gather_qmm(_p(x), _p(lhs_idx), _p(rhs_idx), R, _p(w), _p(scales), _p(biases), E, N, K, mode, 4,
+                            group_size, 1 if sorted_indices else 0, _p(out), _s(stream)), "gather_qmm")
+    return out
+
+
+def fp4_debug_inject_wait_timeout(enable: bool):
+    _check(lib().fp4_debug_inject_wait_timeout(1 if enable else 0), "fp4_debug_inject_wait_timeout")

@@ -1,0 +1,240 @@
+// api.cu -- the C ABI of libfp4gb300: host-side validation, per-device state
+// and launches.  No entry point throws, allocates or keeps a pointer.
+#include <atomic>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/fp4_gb300.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp4 {
+namespace {
+
+// Device error word, one per device context.  Bounded waits that expire
+// atomically OR kErrTimeout into it; fp4_check_device_error reads and clears it.
+__device__ unsigned g_device_error;
+
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+std::atomic<int> g_inject_timeout{0};
+
+fp4_status init_device(int device, const DevInfo** out) {
+  if (device < 0 || device >= kMaxDevices) return FP4_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevInfo& d = g_dev[device];
+  if (d.device == device) {
+    *out = &d;
+    return FP4_OK;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return FP4_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return FP4_ERR_UNSUPPORTED;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return FP4_ERR_CUDA;
+  if (cur != device && cudaSetDevice(device) != cudaSuccess) return FP4_ERR_CUDA;
+  void* err_addr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&err_addr, g_device_error);
+  if (e == cudaSuccess) e = cudaMemset(err_addr, 0, sizeof(unsigned));
+  if (cur != device) cudaSetDevice(cur);
+  if (e != cudaSuccess) return FP4_ERR_CUDA;
+  d.sm_count = prop.multiProcessorCount;
+  d.smem_optin = prop.sharedMemPerBlockOptin;
+  d.err = static_cast<unsigned*>(err_addr);
+  d.device = device;
+  *out = &d;
+  return FP4_OK;
+}
+
+fp4_status current(const DevInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4_ERR_CUDA;
+  return init_device(dev, out);
+}
+
+fp4_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return FP4_OK;
+  if (e == cudaErrorInvalidValue) return FP4_ERR_INVALID_ARG;
+  return FP4_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// mode/bits/group combinations of the pages: affine 4-bit groups 32/64/128,
+// MXFP4 4-bit group 32, NVFP4 4-bit group 16.
+fp4_status check_format(int mode, int bits, int group) {
+  if (bits != 4) return FP4_ERR_UNSUPPORTED;
+  if (mode == FP4_MODE_NVFP4) return group == 16 ? FP4_OK : FP4_ERR_UNSUPPORTED;
+  if (mode == FP4_MODE_MXFP4) return group == 32 ? FP4_OK : FP4_ERR_UNSUPPORTED;
+  if (mode == FP4_MODE_AFFINE)
+    return (group == 32 || group == 64 || group == 128) ? FP4_OK : FP4_ERR_UNSUPPORTED;
+  return FP4_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace fp4
+
+using namespace fp4;
+
+extern "C" {
+
+fp4_status fp4_init(int device) {
+  const DevInfo* d = nullptr;
+  return init_device(device, &d);
+}
+
+const char* fp4_status_string(fp4_status s) {
+  switch (s) {
+    case FP4_OK: return "ok";
+    case FP4_ERR_INVALID_ARG: return "invalid argument";
+    case FP4_ERR_UNSUPPORTED: return "unsupported mode/bits/group combination or device";
+    case FP4_ERR_ALIGNMENT: return "pointer or row pitch misaligned";
+    case FP4_ERR_CUDA: return "CUDA runtime error";
+    case FP4_ERR_TIMEOUT: return "a bounded device wait expired";
+  }
+  return "unknown status";
+}
+
+fp4_status fp4_check_device_error(cudaStream_t stream) {
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FP4_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, d->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FP4_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FP4_ERR_CUDA;
+    return FP4_ERR_TIMEOUT;
+  }
+  return FP4_OK;
+}
+
+void fp4_padded_scale_dims(int64_t rows, int64_t scale_cols, int64_t* padded_rows, int64_t* padded_cols) {
+  if (padded_rows) *padded_rows = ((rows + 127) / 128) * 128;
+  if (padded_cols) *padded_cols = ((scale_cols + 3) / 4) * 4;
+}
+
+size_t fp4_amax_workspace_bytes(int64_t n) { return amax_workspace_bytes(n); }
+
+fp4_status fp4_amax_global_scale(const fp4_bf16* x, int64_t n, float* gs_out, float* amax_out, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  if (!x || !gs_out || !ws || n <= 0) return FP4_ERR_INVALID_ARG;
+  if (ws_bytes < amax_workspace_bytes(n)) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(gs_out, 4) || !aligned(ws, 4) || (amax_out && !aligned(amax_out, 4)))
+    return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  const int max_partials = (int)(ws_bytes / sizeof(uint32_t));
+  return from_cuda(launch_amax(*d, x, n, gs_out, amax_out, static_cast<uint32_t*>(ws),
+                               max_partials > 1024 ? 1024 : max_partials, stream));
+}
+
+fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits,
+                        int group_size, const float* global_scale, uint32_t* xq, uint8_t* scales,
+                        fp4_scale_layout layout, cudaStream_t stream) {
+  fp4_status st = check_format(mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  if (mode == FP4_MODE_AFFINE) return FP4_ERR_UNSUPPORTED;
+  if (!x || !xq || !scales || rows <= 0 || cols <= 0) return FP4_ERR_INVALID_ARG;
+  if (cols % group_size != 0) return FP4_ERR_INVALID_ARG;
+  if (global_scale && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+  if (layout != FP4_SCALES_LINEAR && layout != FP4_SCALES_TILED_128x4) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xq, 4) || (global_scale && !aligned(global_scale, 4))) return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_quantize(*d, x, rows, cols, mode, group_size, global_scale, xq, scales,
+                                   layout == FP4_SCALES_TILED_128x4, stream));
+}
+
+fp4_status fp4_dequantize(const uint32_t* wq, const void* scales, const fp4_bf16* biases, int64_t rows,
+                          int64_t cols, fp4_mode mode, int bits, int group_size, const float* global_scale,
+                          fp4_scale_layout layout, fp4_bf16* out, cudaStream_t stream) {
+  fp4_status st = check_format(mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  if (!wq || !scales || !out || rows <= 0 || cols <= 0 || cols % group_size != 0) return FP4_ERR_INVALID_ARG;
+  if (mode == FP4_MODE_AFFINE) {
+    if (!biases || layout != FP4_SCALES_LINEAR || global_scale) return FP4_ERR_INVALID_ARG;
+    if (!aligned(scales, 2) || !aligned(biases, 2)) return FP4_ERR_ALIGNMENT;
+  } else {
+    if (biases) return FP4_ERR_INVALID_ARG;
+    if (global_scale && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+    if (layout != FP4_SCALES_LINEAR && layout != FP4_SCALES_TILED_128x4) return FP4_ERR_INVALID_ARG;
+  }
+  if (!aligned(wq, 4) || !aligned(out, 16) || (global_scale && !aligned(global_scale, 4))) return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_dequantize(*d, wq, scales, biases, rows, cols, mode, group_size, global_scale,
+                                     layout == FP4_SCALES_TILED_128x4, out, stream));
+}
+
+fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
+               const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, int bits, int group_size,
+               fp4_bf16* y, cudaStream_t stream) {
+  fp4_status st = check_format(mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  if (!x || !w || !scales || !y || N <= 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || K % group_size != 0 || N > INT32_MAX || K > (1 << 20)) return FP4_ERR_INVALID_ARG;
+  if (mode == FP4_MODE_AFFINE) {
+    if (!biases || global_scale_w) return FP4_ERR_INVALID_ARG;
+    if (!aligned(scales, 2) || !aligned(biases, 2)) return FP4_ERR_ALIGNMENT;
+  } else {
+    if (biases) return FP4_ERR_INVALID_ARG;
+    if (global_scale_w && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+    if (mode == FP4_MODE_NVFP4 && !aligned(scales, 2)) return FP4_ERR_ALIGNMENT;
+  }
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 2)) return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_qmv(*d, x, w, scales, biases, global_scale_w, N, K, mode, group_size, y, stream));
+}
+
+fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
+                const float* global_scale_x, const float* global_scale_w, int64_t M, int64_t N, int64_t K,
+                fp4_mode mode, fp4_bf16* out, cudaStream_t stream) {
+  if (mode != FP4_MODE_NVFP4 && mode != FP4_MODE_MXFP4) return FP4_ERR_UNSUPPORTED;
+  if (!xq || !sx || !wq || !sw || !out || M <= 0 || N <= 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 8 != 0 || M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > (1 << 24))
+    return FP4_ERR_INVALID_ARG;
+  if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(sx, 16) || !aligned(sw, 16) || !aligned(out, 16))
+    return FP4_ERR_ALIGNMENT;
+  if ((global_scale_x && !aligned(global_scale_x, 4)) || (global_scale_w && !aligned(global_scale_w, 4)))
+    return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_qqmm(*d, xq, sx, wq, sw, global_scale_x, global_scale_w, M, N, K, mode, out,
+                               g_inject_timeout.load(), stream));
+}
+
+fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* rhs_idx, int64_t R,
+                      const uint32_t* w, const void* scales, const fp4_bf16* biases, int64_t E, int64_t N,
+                      int64_t K, fp4_mode mode, int bits, int group_size, int sorted, fp4_bf16* out,
+                      cudaStream_t stream) {
+  fp4_status st = check_format(mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  if (mode != FP4_MODE_MXFP4) return FP4_ERR_UNSUPPORTED;
+  if (!sorted) return FP4_ERR_UNSUPPORTED;
+  if (!x || !lhs_idx || !rhs_idx || !w || !scales || !out || biases) return FP4_ERR_INVALID_ARG;
+  if (R <= 0 || E <= 0 || N <= 0 || K <= 0 || K % 64 != 0 || N % 16 != 0) return FP4_ERR_INVALID_ARG;
+  if (R > INT32_MAX / 2 || E > 4096 || N > INT32_MAX / 2 || K > (1 << 20)) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(lhs_idx, 4) || !aligned(rhs_idx, 4))
+    return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_gather_qmm(*d, x, lhs_idx, rhs_idx, R, w, static_cast<const uint8_t*>(scales), E, N,
+                                     K, mode, out, stream));
+}
+
+fp4_status fp4_debug_inject_wait_timeout(int enable) {
+  g_inject_timeout.store(enable ? 1 : 0);
+  return FP4_OK;
+}
+
+}  // extern "C"

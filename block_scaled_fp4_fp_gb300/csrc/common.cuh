@@ -1,0 +1,204 @@
+// common.cuh -- shared device helpers for libfp4gb300 (sm_103a only).
+//
+// Everything here is written for the GB300 tensor-memory/TMA execution model:
+// mbarrier waits are bounded (a wait that gives up records an error word and
+// returns false; no trap, no endless loop), conversions use the hardware
+// e2m1x2 / e4m3x2 converters, and fp32 steps that must match the quantization
+// rule bit for bit use the explicitly rounded intrinsics (__fmul_rn, __fdiv_rn,
+// __frcp_rn) so the compiler cannot contract or approximate them.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030 || !defined(__CUDA_ARCH_FEAT_SM103_ALL))
+#error "libfp4gb300 is built for sm_103a only (-gencode arch=compute_103a,code=sm_103a)"
+#endif
+
+namespace fp4 {
+
+// Error word bits written by bounded waits.
+constexpr unsigned kErrTimeout = 1u;
+
+// Limit of one bounded wait, in SM clock cycles (~0.5 s at 2 GHz).  A thread
+// whose wait expired once stops waiting (later waits try once and return), so
+// a broken pipeline costs one limit per thread, not one per stage.
+constexpr long long kWaitLimitCycles = 1000000000LL;
+
+__device__ __forceinline__ void record_error(unsigned* err, unsigned code) {
+  if (err) atomicOr(err, code);
+}
+
+// ---------------------------------------------------------------- bf16 ----
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round an fp32 value to the nearest-even bf16 (returns the 16 bits).
+__device__ __forceinline__ uint32_t f32_to_bf16_rn(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// --------------------------------------------------------- 4-bit codecs ----
+// Two fp32 values -> one byte of two e2m1 codes: `lo` in bits 0..3, `hi` in
+// bits 4..7 (round to nearest even, saturate to +-6, sign kept).
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\t"
+      "cvt.u32.u8 %0, b;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One byte of two e2m1 codes -> f16x2 (low code in the low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\t"
+      "cvt.u8.u32 b, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(r) : "r"(byte));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// fp32 -> E4M3 byte (round to nearest even, saturate to 448).
+__device__ __forceinline__ uint32_t e4m3_rn(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xFFu;
+}
+
+// E4M3 byte -> fp32 (exact, through the hardware e4m3x2 -> f16x2 converter).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  uint32_t h2;
+  uint16_t b = (uint16_t)(byte & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
+  return f16_lo_to_f32(h2);
+}
+
+// 2^e as fp32 for e in [-127, 127] (2^-127 is a subnormal).
+__device__ __forceinline__ float exp2i_f32(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// E8M0 byte -> fp32 (0xFF, NaN, is outside the contract).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t byte) { return exp2i_f32((int)(byte & 0xFFu) - 127); }
+
+// ---------------------------------------------------------- tiled scales ----
+__device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t c, int64_t padded_cols) {
+  int64_t tile = (r >> 7) * (padded_cols >> 2) + (c >> 2);
+  int64_t rr = r & 127;
+  return (tile << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (c & 3);
+}
+
+// ------------------------------------------------------------ memory ops ----
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// -------------------------------------------------------------- mbarrier ----
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar_addr), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false (records
+// kErrTimeout, sets `failed`) if the phase did not complete within `limit`
+// cycles; once `failed` is set, later calls only test the phase once.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err, bool& failed,
+                                          long long limit = kWaitLimitCycles) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  if (failed) return false;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (clock64() - t0 > limit) {
+      record_error(err, kErrTimeout);
+      failed = true;
+      return false;
+    }
+  }
+}
+
+// --------------------------------------------------------------- TMA -------
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int x,
+                                            int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      :: "r"(smem_u32(smem_dst)), "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
+}
+
+__device__ __forceinline__ uint32_t elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred;
+}
+
+}  // namespace fp4

@@ -1,0 +1,48 @@
+// launch.h -- host-side launchers shared between the C ABI (api.cu) and the
+// kernel translation units.  Arguments reaching these functions have already
+// been validated by api.cu; each returns the cudaError_t of its launch(es).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4 {
+
+struct DevInfo {
+  int device = -1;
+  int sm_count = 0;
+  size_t smem_optin = 0;   // max dynamic shared memory per block (opt-in)
+  unsigned* err = nullptr; // device address of the error word on this device
+};
+
+// quant.cu
+size_t amax_workspace_bytes(int64_t n);
+cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* gs_out,
+                        float* amax_out, uint32_t* partials, int max_partials, cudaStream_t s);
+cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, int64_t cols,
+                            int mode, int group, const float* gs, uint32_t* xq, uint8_t* scales,
+                            int tiled, cudaStream_t s);
+cudaError_t launch_dequantize(const DevInfo& d, const uint32_t* wq, const void* scales,
+                              const uint16_t* biases, int64_t rows, int64_t cols, int mode,
+                              int group, const float* gs, int tiled, uint16_t* out,
+                              cudaStream_t s);
+
+// qmv.cu
+cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, const void* scales,
+                       const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode,
+                       int group, uint16_t* y, cudaStream_t s);
+
+// qqmm.cu
+cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
+                        const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
+                        int64_t N, int64_t K, int mode, uint16_t* out, int inject_timeout,
+                        cudaStream_t s);
+
+// gather_qmm.cu
+cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs,
+                              const int32_t* rhs, int64_t R, const uint32_t* w,
+                              const uint8_t* scales, int64_t E, int64_t N, int64_t K, int mode,
+                              uint16_t* out, cudaStream_t s);
+
+}  // namespace fp4

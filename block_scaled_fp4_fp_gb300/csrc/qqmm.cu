@@ -1,0 +1,321 @@
+// qqmm.cu -- FP4 x FP4 block-scaled GEMM on the 5th-generation tensor cores.
+//
+// Pages: "mlx 0.30.7.3 -> 0.30.7.6" qqmm.cpp (QQMatmul::eval_gpu: x [M, K] and
+// W [N, K] both K-major, W "always transposed", lda = ldb = K), qqmm_impl
+// (block-scaled FP4 GEMM, batch 1, alpha/beta as device scalars),
+// qqmm_utils.cu (alpha = amax_x*amax_w/(448*6)^2, beta = 0) and qqmm_utils.h
+// (scales in 128-row x 4-column tiles, zero padded).
+//
+// Design (GB300-native, not the pages' cuBLASLt call):
+//   * one CTA per 128 x 256 output tile, 192 threads:
+//       warp 0  -- TMA producer: codes of x and W by 2-D tensor maps with the
+//                  128-byte swizzle, scale tiles by 1-D bulk copies, into a
+//                  4-stage shared-memory ring (K = 256 per stage);
+//       warp 1  -- allocates tensor memory; one elected thread copies each
+//                  stage's scale tiles into tensor memory (tcgen05.cp 32x128b,
+//                  replicated to the four lane quadrants -- the 128x4 tile is
+//                  exactly that copy's source layout) and issues
+//                  tcgen05.mma.kind::mxf4nvf4.block_scale (4X with E4M3 scales
+//                  for NVFP4, 2X with E8M0 for MXFP4), fp32 accumulation in
+//                  tensor memory, K = 64 per instruction;
+//       warps 2-5 -- epilogue: tcgen05.ld of the accumulator, times alpha,
+//                  round to bf16, store.
+//   * every mbarrier wait is bounded; an expired wait records an error word
+//     and the protocol continues, so the kernel always terminates.
+#include <algorithm>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp4 {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 256;             // fp4 elements per stage (128 bytes per row)
+constexpr int BK_BYTES = BK / 2;
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t A_BYTES = BM * BK_BYTES;  // 16 KB
+constexpr uint32_t B_BYTES = BN * BK_BYTES;  // 32 KB
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;     // accumulator: columns [0, 256)
+constexpr uint32_t SF_COL = 256;    // scale factors: 48 columns per stage
+
+template <int MODE>
+struct Cfg {
+  static constexpr int GROUP = (MODE == 2) ? 16 : 32;
+  // 128x4 scale tiles per 128 rows per stage (K = 256 covers 256/GROUP scale columns)
+  static constexpr int TILES_PER_STAGE = (BK / GROUP) / 4;         // 4 (NVFP4) or 2 (MXFP4)
+  static constexpr uint32_t SFA_BYTES = TILES_PER_STAGE * 512;     // one 128-row tile
+  static constexpr uint32_t SFB_BYTES = 2 * SFA_BYTES;             // two 128-row tiles
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // instruction descriptor: a/b format E2M1 (1), K-major, N>>3, M>>4, scale format
+  static constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                    ((MODE == 2 ? 0u : 1u) << 23) | ((uint32_t)(BM >> 4) << 24);
+};
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Descriptor of one 512-byte scale tile: 32 rows x 16 bytes, no swizzle,
+// 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t tmem, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(tmem), "l"(sdesc) : "memory");
+}
+
+template <int MODE>
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  if (MODE == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    const uint8_t* __restrict__ sx, const uint8_t* __restrict__ sw, const float* __restrict__ gs_x,
+    const float* __restrict__ gs_w, int M, int N, int K, uint16_t* __restrict__ out,
+    unsigned* __restrict__ err, int inject_timeout) {
+  using C = Cfg<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  // per stage: [A | B | SFA | SFB]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* accum_full = bars + 2 * STAGES;
+  uint64_t* never = bars + 2 * STAGES + 1;  // fault-injection barrier, never arrived at
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_blk = blockIdx.x, m_blk = blockIdx.y;
+  const int m0 = m_blk * BM, n0 = n_blk * BN;
+  const int num_kb = K / BK;
+  const int64_t sf_cols_padded = K / C::GROUP;          // multiple of 4 since K % 256 == 0
+  const int64_t tiles_per_rowtile = sf_cols_padded / 4;
+  const int n_rowtiles = (N + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum_full, 1);
+    mbar_init(never, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;  // this thread gave up a wait (see mbar_wait)
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (elect_one_sync()) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      const bool second_b_tile = (n_blk * 2 + 1) < n_rowtiles;
+      const uint32_t tx = A_BYTES + B_BYTES + C::SFA_BYTES + (second_b_tile ? 2u : 1u) * C::SFA_BYTES;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        const int round = kb / STAGES;
+        if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
+        uint8_t* st = smem + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], tx);
+        tma_load_2d(st, &tmA, &full[s], kb * BK_BYTES, m0);
+        tma_load_2d(st + A_BYTES, &tmB, &full[s], kb * BK_BYTES, n0);
+        const int64_t tcol = (int64_t)kb * C::TILES_PER_STAGE;
+        bulk_load(st + A_BYTES + B_BYTES, sx + ((int64_t)m_blk * tiles_per_rowtile + tcol) * 512,
+                  C::SFA_BYTES, &full[s]);
+        bulk_load(st + A_BYTES + B_BYTES + C::SFA_BYTES,
+                  sw + ((int64_t)(2 * n_blk) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES, &full[s]);
+        if (second_b_tile)
+          bulk_load(st + A_BYTES + B_BYTES + 2 * C::SFA_BYTES,
+                    sw + ((int64_t)(2 * n_blk + 1) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES,
+                    &full[s]);
+      }
+      // drain: every stage's last fill has landed before the CTA may exit
+      for (int kb = std::max(0, num_kb - STAGES); kb < num_kb; ++kb)
+        mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1, err, failed);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer --
+    if (elect_one_sync()) {
+      if (inject_timeout) {
+        bool injected = false;  // separate flag: the injected expiry must not stop later waits
+        mbar_wait(never, 0, err, injected, 2000000LL);
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        mbar_wait(&full[s], (kb / STAGES) & 1, err, failed);
+        tc_fence_after();
+        const uint32_t st = base + s * C::STAGE_BYTES;
+        const uint32_t sfa_smem = st + A_BYTES + B_BYTES;
+        const uint32_t sfb_smem = sfa_smem + C::SFA_BYTES;
+        const uint32_t sfa_t = tmem + SF_COL + s * 48;
+        const uint32_t sfb_t = sfa_t + 16;
+#pragma unroll
+        for (int j = 0; j < C::TILES_PER_STAGE; ++j) {
+          tc_cp_sf(sfa_t + 4 * j, desc_sf(sfa_smem + 512 * j));
+          tc_cp_sf(sfb_t + 8 * j, desc_sf(sfb_smem + 512 * j));
+          tc_cp_sf(sfb_t + 8 * j + 4, desc_sf(sfb_smem + C::SFA_BYTES + 512 * j));
+        }
+        const uint64_t adesc = desc_sw128(st);
+        const uint64_t bdesc = desc_sw128(st + A_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 64; ++k) {
+          // K = 64 fp4 = 32 bytes further along the swizzled 128-byte row
+          const int tile = (MODE == 2) ? k : (k >> 1);
+          const uint32_t sf_id = (MODE == 2) ? 0u : (uint32_t)((k & 1) * 2);
+          const uint32_t idesc = C::IDESC | (sf_id << 29) | (sf_id << 4);
+          tc_mma<MODE>(tmem + ACC_COL, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                       sfa_t + 4 * tile, sfb_t + 8 * tile, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(accum_full);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
+    const float alpha = __fmul_rn(gs_x ? __ldg(gs_x) : 1.0f, gs_w ? __ldg(gs_w) : 1.0f);
+    mbar_wait(accum_full, 0, err, failed);
+    tc_fence_after();
+    const int row = m0 + 32 * q + lane;
+    uint16_t* orow = out + (int64_t)row * N;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + ACC_COL + c, r);
+      tmem_ld_wait();
+      const int col = n0 + c;
+      if (row < M) {
+        uint4 o0, o1;
+        o0.x = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[0]), alpha), __fmul_rn(__uint_as_float(r[1]), alpha));
+        o0.y = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[2]), alpha), __fmul_rn(__uint_as_float(r[3]), alpha));
+        o0.z = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[4]), alpha), __fmul_rn(__uint_as_float(r[5]), alpha));
+        o0.w = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[6]), alpha), __fmul_rn(__uint_as_float(r[7]), alpha));
+        o1.x = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[8]), alpha), __fmul_rn(__uint_as_float(r[9]), alpha));
+        o1.y = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[10]), alpha), __fmul_rn(__uint_as_float(r[11]), alpha));
+        o1.z = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[12]), alpha), __fmul_rn(__uint_as_float(r[13]), alpha));
+        o1.w = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[14]), alpha), __fmul_rn(__uint_as_float(r[15]), alpha));
+        if (col < N) *reinterpret_cast<uint4*>(orow + col) = o0;
+        if (col + 8 < N) *reinterpret_cast<uint4*>(orow + col + 8) = o1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over packed codes viewed as bytes: [rows, K/2], box 128 bytes x box_rows.
+bool make_code_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
+                        const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M, int64_t N,
+                        int64_t K, uint16_t* out, int inject, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_code_map(&ta, xq, M, K, BM) || !make_code_map(&tb, wq, N, K, BN)) return cudaErrorInvalidValue;
+  const size_t smem = Cfg<MODE>::SMEM_BYTES;
+  if (smem > d.smem_optin) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(qqmm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  qqmm_kernel<MODE><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, out,
+                                                  d.err, inject);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
+                        const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
+                        int64_t N, int64_t K, int mode, uint16_t* out, int inject_timeout,
+                        cudaStream_t s) {
+  if (mode == 2) return launch_mode<2>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, out, inject_timeout, s);
+  return launch_mode<1>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, out, inject_timeout, s);
+}
+
+}  // namespace fp4

@@ -1,0 +1,192 @@
+/*
+ * fp4_gb300.h -- C ABI of libfp4gb300: block-scaled 4-bit quantization and
+ * quantized matmul on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (pages cited by title and section):
+ *   [P1] "perf(cuda): enable hardware NVFP4/MXFP4 conversion on Blackwell
+ *        builds" -- fp_quantize: MXFP4 and NVFP4 share one template; e2m1 by
+ *        cvt.rn.satfinite.e2m1x2.f32 on sm_100a-class targets.
+ *   [P2] "epic: NVIDIA Volta (sm_70) inference acceleration program #1536" --
+ *        Baseline and Diagnosis 3: qmv over affine 4-bit group-64 weights, the
+ *        decode-step weight stream; Diagnosis 1 and 5: gather_gemm / grouped
+ *        GEMM for MoE.
+ *   [P3] "mlx 0.30.7.3 -> 0.30.7.6" -- qqmm.cpp (QQMatmul::eval_gpu,
+ *        quantize_input: packed codes [.., K*bits/32] uint32, scales uint8,
+ *        W always transposed [N, K]), qqmm_utils.h (128x4 scale tiles, zero
+ *        padding, 16-byte aligned start), qqmm_utils.cu (alpha =
+ *        amax_x*amax_w/(448*6)^2, beta = 0), quantized.cpp
+ *        (fast::Quantize::eval_gpu: optional NVFP4 global scale).
+ *   [P4] "mlx: opt-in dense GEMM for nvfp4 prefill ... - #287" -- global scale
+ *        representations (multiplier m versus m*2688).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps none of them after the call returns and allocates nothing.
+ *   - bf16 tensors are raw bfloat16 bit patterns (fp4_bf16), row-major and
+ *     contiguous.  Packed 4-bit codes are uint32 words: element k of a row is
+ *     word k/8, nibble k%8, low nibble first (8 codes per word).
+ *   - Work is enqueued on `stream` (stream-ordered, asynchronous).  Arguments
+ *     are validated on the host before anything is launched; an invalid call
+ *     launches nothing and returns a non-OK status.  No C++ exception crosses
+ *     the ABI.  Launch failures return FP4_ERR_CUDA.  A device-side wait that
+ *     gives up (bounded spin) records FP4_ERR_TIMEOUT, which
+ *     fp4_check_device_error() reports.
+ *   - NVFP4: e2m1 codes, groups of 16, E4M3 block scales, optional fp32 global
+ *     scale gs in the multiplier form gs = amax/2688 (2688 = 448*6).
+ *     MXFP4: e2m1 codes, groups of 32, E8M0 block scales.
+ *     Affine: unsigned 4-bit q, groups of 32/64/128, bf16 scale and bias,
+ *     w = q*scale + bias.
+ */
+#ifndef FP4_GB300_H
+#define FP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fp4_bf16; /* raw bfloat16 bits */
+
+typedef enum {
+  FP4_OK = 0,
+  FP4_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size */
+  FP4_ERR_UNSUPPORTED = 2,  /* mode/bits/group combination or device not supported */
+  FP4_ERR_ALIGNMENT = 3,    /* a pointer or a row pitch breaks the alignment rule */
+  FP4_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  FP4_ERR_TIMEOUT = 5       /* a bounded device wait expired (see fp4_check_device_error) */
+} fp4_status;
+
+typedef enum { FP4_MODE_AFFINE = 0, FP4_MODE_MXFP4 = 1, FP4_MODE_NVFP4 = 2 } fp4_mode;
+
+/* Scale layouts.  LINEAR: row-major [rows, cols/group].
+ * TILED_128x4 [P3 qqmm_utils.h]: rows padded to a multiple of 128 and scale
+ * columns to a multiple of 4; byte (r, c) sits at
+ *   ((r/128)*(Cp/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4
+ * (Cp = padded scale columns), every padding byte is zero, total Rp*Cp bytes. */
+typedef enum { FP4_SCALES_LINEAR = 0, FP4_SCALES_TILED_128x4 = 1 } fp4_scale_layout;
+
+/* Checks that `device` is compute capability 10.3 (GB300) and caches its
+ * properties.  Every other entry point initializes the current device lazily,
+ * so calling this is optional; it is the place to learn FP4_ERR_UNSUPPORTED. */
+fp4_status fp4_init(int device);
+
+/* Static string for a status code; never NULL. */
+const char* fp4_status_string(fp4_status status);
+
+/* Synchronizes `stream`, then reports and clears the device error word of the
+ * current device: FP4_ERR_TIMEOUT if any bounded wait of an earlier launch
+ * expired since the last check, FP4_ERR_CUDA if the stream reports an error,
+ * else FP4_OK. */
+fp4_status fp4_check_device_error(cudaStream_t stream);
+
+/* Padded scale-tile dimensions for `rows` x `scale_cols` scales
+ * [P3 qqmm_utils.h get_padded_scale_dims]: rows up to a multiple of 128,
+ * columns up to a multiple of 4. */
+void fp4_padded_scale_dims(int64_t rows, int64_t scale_cols, int64_t* padded_rows,
+                           int64_t* padded_cols);
+
+/* Bytes of device workspace fp4_amax_global_scale needs for n elements. */
+size_t fp4_amax_workspace_bytes(int64_t n);
+
+/* a1: tensor amax and NVFP4 global scale [P3 quantize_input / compute_qqmm_pointers,
+ * P4 global-scale representation].
+ *   x        bf16[n], 16-byte aligned, n >= 1
+ *   gs_out   device fp32 scalar: fl(amax/2688), the multiplier form m
+ *   amax_out device fp32 scalar or NULL: max |x| (MLX's m*2688 form)
+ *   ws       device scratch of ws_bytes >= fp4_amax_workspace_bytes(n) bytes;
+ *            no initial contents needed; not read after the call completes.
+ * NaN inputs give an unspecified result. */
+fp4_status fp4_amax_global_scale(const fp4_bf16* x, int64_t n, float* gs_out, float* amax_out,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* a2-a4: fp_quantize [P1; P3 qqmm.cpp quantize_input, quantized.cpp].
+ *   x            bf16[rows, cols], 16-byte aligned
+ *   mode, bits, group_size: (NVFP4, 4, 16) or (MXFP4, 4, 32); affine quantize is
+ *                not provided (FP4_ERR_UNSUPPORTED)
+ *   global_scale device fp32 scalar gs (NVFP4 only) or NULL (gs = 1)
+ *   xq           uint32[rows, cols/8] packed codes, 4-byte aligned
+ *   scales       uint8 E4M3/E8M0 block scales in `layout`; for TILED_128x4 the
+ *                whole padded buffer (Rp*Cp bytes) is written, padding with 0
+ * Per NVFP4 group: b = max|x|, s8 = E4M3_rn_sat(b/(6*gs)) (0 when b = 0),
+ *   q = e2m1_rn_sat(x * (1/(s8*gs))) (0 codes with their sign when s8*gs = 0).
+ * Per MXFP4 group: se = clamp(floor(log2 b) - 2, -127, 127) (-127 when b = 0),
+ *   byte = se + 127, q = e2m1_rn_sat(x * 2^-se).
+ * Requires cols % group_size == 0 and rows >= 1. */
+fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits,
+                        int group_size, const float* global_scale, uint32_t* xq, uint8_t* scales,
+                        fp4_scale_layout layout, cudaStream_t stream);
+
+/* a5: fp_dequantize / affine_dequantize [P3 quantized.cpp].
+ *   wq      uint32[rows, cols/8]
+ *   scales  NVFP4/MXFP4: uint8 block scales in `layout`; affine: bf16[rows, cols/group]
+ *           (linear layout only)
+ *   biases  affine: bf16[rows, cols/group]; must be NULL otherwise
+ *   global_scale NVFP4 only, device fp32 or NULL
+ *   out     bf16[rows, cols], 16-byte aligned
+ * Each element is the fp32 value code*scale*gs (affine q*scale + bias) rounded
+ * to nearest-even bf16. */
+fp4_status fp4_dequantize(const uint32_t* wq, const void* scales, const fp4_bf16* biases,
+                          int64_t rows, int64_t cols, fp4_mode mode, int bits, int group_size,
+                          const float* global_scale, fp4_scale_layout layout, fp4_bf16* out,
+                          cudaStream_t stream);
+
+/* a6: qmv, the M = 1 decode GEMV [P2 Baseline, Diagnosis 3; P3 qqmm.cpp fp_qmv route].
+ *   y[n] = sum_k x[k] * deq(W)[n, k]   (fp32 accumulation, bf16 output)
+ *   x       bf16[K], 16-byte aligned
+ *   w       uint32[N, K/8] (W stored [N, K]), 16-byte aligned
+ *   scales  linear block scales: uint8[N, K/group] (NVFP4/MXFP4) or bf16 (affine)
+ *   biases  affine: bf16[N, K/group]; NULL otherwise
+ *   global_scale_w NVFP4 only: device fp32 gs of W, multiplied in the epilogue, or NULL
+ *   y       bf16[N]
+ * Requires K % 32 == 0 and K % group_size == 0. */
+fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
+               const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, int bits,
+               int group_size, fp4_bf16* y, cudaStream_t stream);
+
+/* a7-a9: qqmm, the FP4 x FP4 GEMM [P3 qqmm.cpp, qqmm_impl, qqmm_utils.cu].
+ *   out[m, n] = bf16( alpha * sum_k deq(xq)[m, k] * deq(wq)[n, k] ),  beta = 0
+ *   alpha = (*global_scale_x) * (*global_scale_w); a NULL pointer counts as 1.
+ *   With multiplier-form global scales this is amax_x*amax_w/(448*6)^2.  To pass a
+ *   precomputed alpha, give it as global_scale_x and NULL as global_scale_w.
+ *   xq      uint32[M, K/8], 16-byte aligned (NVFP4 or MXFP4 codes)
+ *   sx      uint8 block scales of xq, TILED_128x4 layout
+ *   wq      uint32[N, K/8] (W stored [N, K]), 16-byte aligned
+ *   sw      uint8 block scales of wq, TILED_128x4 layout
+ *   out     bf16[M, N], 16-byte aligned
+ * Requires K % 256 == 0 (hence K % 64 == 0 for the tensor-core K step), N % 8 == 0,
+ * M >= 1.  mode is NVFP4 (E4M3 scales, group 16) or MXFP4 (E8M0, group 32). */
+fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
+                const float* global_scale_x, const float* global_scale_w, int64_t M, int64_t N,
+                int64_t K, fp4_mode mode, fp4_bf16* out, cudaStream_t stream);
+
+/* a10: gather_qmm, the MoE grouped GEMM with 4-bit weights and bf16 activations
+ * [P2 Diagnosis 1 and 5: gather_gemm / grouped GEMM].
+ *   out[r, n] = sum_k x[lhs_idx[r], k] * deq(w[rhs_idx[r]])[n, k]  (fp32 accumulation)
+ *   x        bf16[T, K] activations (T = 1 + max lhs_idx), 16-byte aligned
+ *   lhs_idx  int32[R] activation row of each routed row
+ *   rhs_idx  int32[R] expert of each routed row, in [0, E)
+ *   w        uint32[E, N, K/8], 16-byte aligned
+ *   scales   uint8[E, N, K/group] linear block scales
+ *   biases   must be NULL
+ *   out      bf16[R, N], 16-byte aligned
+ * mode MXFP4 (group 32).  sorted != 0 promises rhs_idx is non-decreasing (rows
+ * grouped by expert), which this version requires.  Requires K % 64 == 0 and
+ * N % 16 == 0. */
+fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* rhs_idx, int64_t R,
+                      const uint32_t* w, const void* scales, const fp4_bf16* biases, int64_t E,
+                      int64_t N, int64_t K, fp4_mode mode, int bits, int group_size, int sorted,
+                      fp4_bf16* out, cudaStream_t stream);
+
+/* Test hook, off by default: when `enable` is nonzero the next qqmm launches
+ * make their MMA-issuing thread wait on a barrier nothing arrives at, with a
+ * 1 ms limit, before doing its normal work.  The wait expires, the kernel
+ * records FP4_ERR_TIMEOUT and still completes; nothing faults or hangs. */
+fp4_status fp4_debug_inject_wait_timeout(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

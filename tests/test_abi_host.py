@@ -1,0 +1,73 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every entry point declared in include/, and argument validation rejects
+bad calls before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    from block_scaled_fp4_fp_gb300 import build, binding
+    build.build()
+    binding.lib()
+    return binding
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                                src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(B):
+    names = declared_functions()
+    assert {"fp4_quantize", "fp4_dequantize", "qmv", "qqmm", "gather_qmm"} <= set(names)
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in B.SIGNATURES, f"binding has no signature for {n}"
+
+
+def test_status_strings_and_padded_dims(B):
+    for s in range(6):
+        assert B.status_string(s)
+    assert B.padded_scale_dims(1, 32) == (128, 32)
+    assert B.padded_scale_dims(300, 5) == (384, 8)
+    assert B.padded_scale_dims(4096, 320) == (4096, 320)
+    assert B.lib().fp4_amax_workspace_bytes(1 << 20) >= 4
+
+
+def test_validation_rejects_before_launch(B):
+    L = B.lib()
+    p = ctypes.c_void_p(256)  # never dereferenced: every call below fails validation first
+    # unsupported bits / group / mode
+    assert L.qmv(p, p, p, None, None, 64, 64, B.MODE_NVFP4, 3, 16, p, None) == B.FP4_ERR_UNSUPPORTED
+    assert L.qmv(p, p, p, None, None, 64, 64, B.MODE_NVFP4, 4, 32, p, None) == B.FP4_ERR_UNSUPPORTED
+    assert L.qmv(p, p, p, p, None, 64, 64, B.MODE_AFFINE, 4, 16, p, None) == B.FP4_ERR_UNSUPPORTED
+    assert L.fp4_quantize(p, 4, 64, B.MODE_AFFINE, 4, 64, None, p, p, 0, None) == B.FP4_ERR_UNSUPPORTED
+    assert L.qqmm(p, p, p, p, None, None, 1, 8, 256, B.MODE_AFFINE, p, None) == B.FP4_ERR_UNSUPPORTED
+    # null pointers, bad sizes, indivisible shapes
+    assert L.fp4_quantize(None, 4, 64, B.MODE_NVFP4, 4, 16, None, p, p, 0, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize(p, 4, 40, B.MODE_NVFP4, 4, 16, None, p, p, 0, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize(p, 0, 64, B.MODE_NVFP4, 4, 16, None, p, p, 0, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize(p, 4, 64, B.MODE_MXFP4, 4, 32, p, p, p, 0, None) == B.FP4_ERR_INVALID_ARG  # gs w/ MXFP4
+    assert L.qqmm(p, p, p, p, None, None, 1, 8, 320, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG  # K % 256
+    assert L.qqmm(p, p, p, p, None, None, 1, 12, 256, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG  # N % 8
+    assert L.qmv(p, p, p, None, None, 64, 48, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_INVALID_ARG  # K % 32
+    assert L.qmv(p, p, p, None, None, 64, 64, B.MODE_AFFINE, 4, 64, p, None) == B.FP4_ERR_INVALID_ARG  # no biases
+    assert L.gather_qmm(p, p, p, 8, p, p, None, 2, 32, 64, B.MODE_MXFP4, 4, 32, 0, p, None) == B.FP4_ERR_UNSUPPORTED
+    # alignment
+    odd = ctypes.c_void_p(258)
+    assert L.qmv(odd, p, p, None, None, 64, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_ALIGNMENT
+    assert L.qqmm(p, odd, p, p, None, None, 1, 8, 256, B.MODE_NVFP4, p, None) == B.FP4_ERR_ALIGNMENT
+    assert L.fp4_amax_global_scale(p, 16, p, None, p, 2, None) == B.FP4_ERR_INVALID_ARG  # ws too small

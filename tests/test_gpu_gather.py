@@ -1,0 +1,49 @@
+"""GPU parity of gather_qmm (MoE grouped W4A16 GEMM, MXFP4 experts)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_fp_gb300 import synth
+from helpers import assert_close_to_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from block_scaled_fp4_fp_gb300 import build, binding
+    build.build()
+    binding.fp4_init(0)
+    return binding
+
+
+def run(B, tokens, E, topk, N, K, seed=0, rows=None):
+    lhs, rhs = synth.moe_routing(tokens, E, topk, seed=seed)
+    x = synth.bf16_normal((tokens, K), 1.0, seed=seed + 1)
+    w = synth.bf16_normal((E * N, K), 0.02, seed=seed + 2)
+    q, s = oracle.mxfp4_quantize(synth.to_u16(w))
+    q3, s3 = q.reshape(E, N, K // 8), s.reshape(E, N, K // 32)
+    out = B.gather_qmm(x.cuda(), torch.from_numpy(lhs).cuda(), torch.from_numpy(rhs).cuda(),
+                       torch.from_numpy(q3.view(np.int32)).cuda(), torch.from_numpy(s3).cuda())
+    ref = oracle.gather_qmm(synth.to_u16(x), lhs, rhs, q3, s3, None, oracle.MODE_MXFP4, 32, rows=rows)
+    if rows is not None:
+        out = out[torch.as_tensor(rows).cuda()]
+    return out, ref
+
+
+@pytest.mark.parametrize("tokens,E,topk,N,K", [(16, 4, 2, 64, 128), (300, 8, 4, 272, 256), (64, 32, 4, 512, 192)])
+def test_gather_small(B, tokens, E, topk, N, K):
+    out, ref = run(B, tokens, E, topk, N, K, seed=tokens)
+    assert_close_to_oracle(out, ref, f"gather {tokens}x{E}x{N}x{K}")
+
+
+def test_gather_moe_full_size_sampled(B):
+    """2048 tokens, 32 experts, top-4, gate/up 5760 x 2880; sampled routed rows
+    (first/last of several expert segments and random ones)."""
+    lhs, rhs = synth.moe_routing(2048, 32, 4, seed=0)
+    starts = np.searchsorted(rhs, np.arange(32))
+    rows = np.unique(np.concatenate([starts[:6], starts[1:7] - 1, [len(rhs) - 1],
+                                     np.random.default_rng(0).integers(0, len(rhs), 8)]))
+    out, ref = run(B, 2048, 32, 4, 5760, 2880, seed=0, rows=rows)
+    assert_close_to_oracle(out, ref, "gather gate/up full size")

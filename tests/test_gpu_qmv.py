@@ -1,0 +1,97 @@
+"""GPU parity of qmv (decode GEMV, W4A16) against the oracle's fp64 GEMV."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_fp_gb300 import synth
+from helpers import assert_close_to_oracle
+
+pytestmark = pytest.mark.gpu
+GROUP = {0: 64, 1: 32, 2: 16}
+
+
+@pytest.fixture(scope="module")
+def B():
+    from block_scaled_fp4_fp_gb300 import build, binding
+    build.build()
+    binding.fp4_init(0)
+    return binding
+
+
+def make_weights(mode, N, K, seed, group=None):
+    """Quantized weights made by the oracle from seeded bf16 N(0, 0.02)."""
+    w = synth.bf16_normal((N, K), 0.02, seed=seed)
+    wb = synth.to_u16(w)
+    g = group or GROUP[mode]
+    gs = None
+    b = None
+    if mode == 0:
+        q, s, b = oracle.affine_quantize(wb, g)
+    elif mode == 2:
+        gs = oracle.global_scale(wb)
+        q, s = oracle.nvfp4_quantize(wb, gs)
+    else:
+        q, s = oracle.mxfp4_quantize(wb)
+    return q, s, b, gs, g
+
+
+def to_dev(mode, q, s, b, gs):
+    qd = torch.from_numpy(q.view(np.int32)).cuda()
+    sd = synth.from_u16(s, "cuda") if mode == 0 else torch.from_numpy(s).cuda()
+    bd = synth.from_u16(b, "cuda") if b is not None else None
+    gsd = torch.tensor(gs, dtype=torch.float32, device="cuda") if gs is not None else None
+    return qd, sd, bd, gsd
+
+
+@pytest.mark.parametrize("mode", [2, 1, 0])
+@pytest.mark.parametrize("N,K", [(256, 512), (300, 1024), (33, 4096), (1, 64), (1000, 96)])
+def test_qmv_small(B, mode, N, K):
+    if K % GROUP[mode]:
+        pytest.skip("K not a multiple of the group")
+    q, s, b, gs, g = make_weights(mode, N, K, seed=N + K)
+    x = synth.bf16_normal((K,), 1.0, seed=7)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, bd, gsd, mode=mode, group_size=g)
+    ref = oracle.qmv(synth.to_u16(x), q, s, b, mode, g, gs)
+    assert_close_to_oracle(y, ref, f"qmv mode {mode} {N}x{K}")
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_qmv_affine_other_groups(B, group):
+    q, s, b, gs, g = make_weights(0, 96, 1024, seed=3, group=group)
+    x = synth.bf16_normal((1024,), 1.0, seed=8)
+    qd, sd, bd, gsd = to_dev(0, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, bd, None, mode=0, group_size=group)
+    assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, b, 0, group), f"affine g{group}")
+
+
+@pytest.mark.parametrize("mode", [2, 1, 0])
+def test_qmv_one_hot_returns_dequantized_column(B, mode):
+    N, K = 64, 256
+    q, s, b, gs, g = make_weights(mode, N, K, seed=1)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    deq = oracle.dequantize_f64(q, s, b, mode, g, gs)
+    for k in [0, 1, 8, 15, 31, 32, 255]:
+        x = torch.zeros(K, dtype=torch.bfloat16)
+        x[k] = 1.0
+        y = B.qmv(x.cuda(), qd, sd, bd, gsd, mode=mode, group_size=g).float().cpu().double().numpy()
+        ref = oracle.bf16_bits_to_f64(oracle.bf16_round_array(deq[:, k]))
+        assert np.array_equal(y, ref), k
+
+
+@pytest.mark.parametrize("mode", [2, 1, 0])
+@pytest.mark.parametrize("proj", [0, 4, 6])
+def test_qmv_decode_layer_shapes_sampled(B, mode, proj):
+    """Full-size decode projections (q 5120x5120, gate 17408x5120, down
+    5120x17408) in the launch configuration the bench uses; the oracle checks a
+    seeded sample of rows."""
+    name, N, K = synth.LAYER_PROJECTIONS[proj]
+    q, s, b, gs, g = make_weights(mode, N, K, seed=synth.layer_seed(0, proj))
+    x = synth.bf16_normal((K,), 1.0, seed=99)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, bd, gsd, mode=mode, group_size=g)
+    rows = np.unique(np.concatenate([np.arange(8), N - 1 - np.arange(8),
+                                     np.random.default_rng(proj).integers(0, N, 240)]))
+    ref = oracle.qmv(synth.to_u16(x), q, s, b, mode, g, gs, rows=rows)
+    assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"{name} mode {mode}")
