@@ -178,15 +178,17 @@ class DecodeStack:
 
 
 def time_graph(graph, steps, warmup, stream):
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        graph.replay()
-    end.record(stream)
+    # replay() launches on the current stream: make it the stream the events see
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps
 
