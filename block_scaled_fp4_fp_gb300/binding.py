@@ -44,6 +44,7 @@ SIGNATURES = {
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
     "fp4_debug_inject_wait_timeout": (_INT, [_INT]),
+    "fp4_amax_global_scale_noalloc": (_INT, [_VP, _I64, _VP, _VP, _VP]),
 }
 
 
@@ -112,6 +113,15 @@ def fp4_amax_global_scale(x: torch.Tensor, gs_out=None, amax_out=None, ws=None, 
         ws = torch.empty(wsb, dtype=torch.uint8, device=x.device)
     _check(lib().fp4_amax_global_scale(_p(x), n, _p(gs_out), _p(amax_out), _p(ws), ws.numel() * ws.element_size(),
                                        _s(stream)), "fp4_amax_global_scale")
+    return gs_out
+
+
+def fp4_amax_global_scale_noalloc(x: torch.Tensor, gs_out=None, amax_out=None, stream=None):
+    """Allocation-free global scale: the library uses its own fixed device scratch."""
+    if gs_out is None:
+        gs_out = torch.empty((), dtype=torch.float32, device=x.device)
+    _check(lib().fp4_amax_global_scale_noalloc(_p(x), x.numel(), _p(gs_out), _p(amax_out), _s(stream)),
+           "fp4_amax_global_scale_noalloc")
     return gs_out
 
 

@@ -180,6 +180,30 @@ fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* 
                       int64_t N, int64_t K, fp4_mode mode, int bits, int group_size, int sorted,
                       fp4_bf16* out, cudaStream_t stream);
 
+/* Maximum element count accepted by fp4_amax_global_scale_noalloc (2^36). */
+#define FP4_AMAX_NOALLOC_MAX_ELEMS ((int64_t)1 << 36)
+
+/* Allocation-free variant of fp4_amax_global_scale.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory where they need a global scale -- code recording into a CUDA stream
+ * capture, engines that hand every kernel a pre-planned memory arena, hosts
+ * that forbid allocation on a latency-critical path.  The per-block partial
+ * maxima that fp4_amax_global_scale keeps in caller scratch live here in a
+ * fixed 4 KiB file-scope device array (1024 partials) that every GPU loading
+ * the library holds until the process exits.  The results are identical to
+ * fp4_amax_global_scale's.
+ *   x, n, gs_out, amax_out: as for fp4_amax_global_scale; n in [1, 2^36],
+ *            larger n returns FP4_ERR_INVALID_ARG.
+ * Nothing is allocated or freed, by this library or through any allocating
+ * library routine.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and checks the compute capability; make that
+ * first call before any stream capture.  All calls share the array and it keeps
+ * the last call's contents (each call writes every slot it reads, so nothing
+ * needs clearing); calls that overlap on the GPU -- unordered streams -- race
+ * on it and give unspecified results. */
+fp4_status fp4_amax_global_scale_noalloc(const fp4_bf16* x, int64_t n, float* gs_out, float* amax_out,
+                                         cudaStream_t stream);
+
 /* Test hook, off by default: when `enable` is nonzero the next qqmm launches
  * make their MMA-issuing thread wait on a barrier nothing arrives at, with a
  * 1 ms limit, before doing its normal work.  The wait expires, the kernel
