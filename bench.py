@@ -205,24 +205,24 @@ def capture(fn, stream):
 
 
 # ------------------------------------------------------------------ components
-def bench_quantize(B, device, reps=30):
+def bench_quantize(B, device, reps=40):
     """Activation quantize 4096x5120 (0.1 % outliers x50), tiled scales; 4 rotating inputs."""
     xs = [synth.activations_with_outliers(4096, 5120, seed=i, outlier_seed=100 + i, device=device) for i in range(4)]
     res = {}
     for mode, name in ((B.MODE_NVFP4, "nvfp4"), (B.MODE_MXFP4, "mxfp4")):
         gss = [B.fp4_amax_global_scale(x) if mode == B.MODE_NVFP4 else None for x in xs]
         outs = [B.fp4_quantize(x, mode, global_scale=g, layout=B.SCALES_TILED) for x, g in zip(xs, gss)]
-        times = []
-        for r in range(reps + 3):
-            i = r % 4
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
+        for i in range(4):  # warm-up
             B.fp4_quantize(xs[i], mode, global_scale=gss[i], layout=B.SCALES_TILED, xq=outs[i][0], scales=outs[i][1])
-            e1.record()
-            torch.cuda.synchronize()
-            if r >= 3:
-                times.append(e0.elapsed_time(e1))
-        ms = statistics.median(times) if times else float("nan")
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for r in range(reps):  # back-to-back launches over 4 rotating inputs (4 x 84 MB > L2)
+            i = r % 4
+            B.fp4_quantize(xs[i], mode, global_scale=gss[i], layout=B.SCALES_TILED, xq=outs[i][0], scales=outs[i][1])
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps if reps else float("nan")
         nbytes = 4096 * 5120 * 2 + 4096 * 5120 // 2 + outs[0][1].numel()
         res[name] = {"ms": ms, "GB/s": nbytes / ms / 1e6, "bytes": nbytes}
     return res
@@ -240,16 +240,16 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=10):
         gx = B.fp4_amax_global_scale(x)
         xq, xs = B.fp4_quantize(x, B.MODE_NVFP4, global_scale=gx, layout=B.SCALES_TILED)
         out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-        times = []
-        for r in range(reps + 3):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
+        for _ in range(3):  # warm-up
             B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
-            e1.record()
-            torch.cuda.synchronize()
-            if r >= 3:
-                times.append(e0.elapsed_time(e1))
-        ms = statistics.median(times) if times else float("nan")
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps if reps else float("nan")
         flops = 2.0 * M * N * K
         res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}
         del x, xq, xs, out
@@ -266,16 +266,16 @@ def bench_gather(B, device, reps=10):
     del w
     q3, s3 = q.view(E, N, K // 8), s.view(E, N, K // 32)
     out = torch.empty((len(lhs), N), dtype=torch.bfloat16, device=device)
-    times = []
-    for r in range(reps + 3):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+    for _ in range(3):  # warm-up
         B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
-        e1.record()
-        torch.cuda.synchronize()
-        if r >= 3:
-            times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times) if times else float("nan")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps if reps else float("nan")
     flops = 2.0 * len(lhs) * N * K
     return {"gate_up": {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}}
 
@@ -322,11 +322,11 @@ def run_case(args):
         for _ in range(3):
             stack.step()
     elif c.startswith("qqmm_m"):
-        bench_qqmm(B, dev, Ms=(int(c[len("qqmm_m"):]),), reps=0)
+        bench_qqmm(B, dev, Ms=(int(c[len("qqmm_m"):]),), reps=1)
     elif c == "quantize":
         bench_quantize(B, dev, reps=2)
     elif c == "gather":
-        bench_gather(B, dev, reps=0)
+        bench_gather(B, dev, reps=1)
     torch.cuda.synchronize()
     st = B.fp4_check_device_error()
     print(json.dumps({"case": c, "status": B.status_string(st)}))

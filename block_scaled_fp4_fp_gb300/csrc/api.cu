@@ -140,9 +140,12 @@ fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode 
   if (mode == FP4_MODE_AFFINE) return FP4_ERR_UNSUPPORTED;
   if (!x || !xq || !scales || rows <= 0 || cols <= 0) return FP4_ERR_INVALID_ARG;
   if (cols % group_size != 0) return FP4_ERR_INVALID_ARG;
+  if (rows > INT32_MAX / 2 || cols > INT32_MAX / 16) return FP4_ERR_INVALID_ARG;
   if (global_scale && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
   if (layout != FP4_SCALES_LINEAR && layout != FP4_SCALES_TILED_128x4) return FP4_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(xq, 4) || (global_scale && !aligned(global_scale, 4))) return FP4_ERR_ALIGNMENT;
+  if (!aligned(x, 16) || !aligned(xq, mode == FP4_MODE_NVFP4 ? 8 : 16) ||
+      (global_scale && !aligned(global_scale, 4)))
+    return FP4_ERR_ALIGNMENT;
   const DevInfo* d = nullptr;
   st = current(&d);
   if (st != FP4_OK) return st;
@@ -178,7 +181,8 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
   fp4_status st = check_format(mode, bits, group_size);
   if (st != FP4_OK) return st;
   if (!x || !w || !scales || !y || N <= 0 || K <= 0) return FP4_ERR_INVALID_ARG;
-  if (K % 32 != 0 || K % group_size != 0 || N > INT32_MAX || K > (1 << 20)) return FP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || K % group_size != 0 || N > INT32_MAX / 2) return FP4_ERR_INVALID_ARG;
+  if (K > 65536) return FP4_ERR_UNSUPPORTED;  // x is staged whole in shared memory
   if (mode == FP4_MODE_AFFINE) {
     if (!biases || global_scale_w) return FP4_ERR_INVALID_ARG;
     if (!aligned(scales, 2) || !aligned(biases, 2)) return FP4_ERR_ALIGNMENT;

@@ -7,7 +7,7 @@
 // (scales in 128-row x 4-column tiles, zero padded).
 //
 // Design (GB300-native, not the pages' cuBLASLt call):
-//   * one CTA per 128 x 256 output tile, 192 threads:
+//   * persistent: one CTA per SM loops over 128 x 256 output tiles, 320 threads:
 //       warp 0  -- TMA producer: codes of x and W by 2-D tensor maps with the
 //                  128-byte swizzle, scale tiles by 1-D bulk copies, into a
 //                  4-stage shared-memory ring (K = 256 per stage);
@@ -18,8 +18,11 @@
 //                  tcgen05.mma.kind::mxf4nvf4.block_scale (4X with E4M3 scales
 //                  for NVFP4, 2X with E8M0 for MXFP4), fp32 accumulation in
 //                  tensor memory, K = 64 per instruction;
-//       warps 2-5 -- epilogue: tcgen05.ld of the accumulator, times alpha,
-//                  round to bf16, store.
+//       warps 2-9 -- epilogue: tcgen05.ld of the accumulator (lane quadrant
+//                  warp%4, one 128-column half each), times alpha, round to
+//                  bf16 into registers, release the accumulator, then store --
+//                  so the next tile's MMAs overlap the stores, and the producer
+//                  runs ahead into the next tile while the accumulator drains.
 //   * every mbarrier wait is bounded; an expired wait records an error word
 //     and the protocol continues, so the kernel always terminates.
 #include <algorithm>
@@ -38,7 +41,8 @@ constexpr int BN = 256;
 constexpr int BK = 256;             // fp4 elements per stage (128 bytes per row)
 constexpr int BK_BYTES = BK / 2;
 constexpr int STAGES = 4;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, 8 epilogue warps
 constexpr uint32_t A_BYTES = BM * BK_BYTES;  // 16 KB
 constexpr uint32_t B_BYTES = BN * BK_BYTES;  // 32 KB
 constexpr uint32_t TMEM_COLS = 512;
@@ -129,17 +133,17 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
-  uint64_t* accum_full = bars + 2 * STAGES;
-  uint64_t* never = bars + 2 * STAGES + 1;  // fault-injection barrier, never arrived at
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = bars + 2 * STAGES + 1;
+  uint64_t* never = bars + 2 * STAGES + 2;  // fault-injection barrier, never arrived at
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_blk = blockIdx.x, m_blk = blockIdx.y;
-  const int m0 = m_blk * BM, n0 = n_blk * BN;
   const int num_kb = K / BK;
-  const int64_t sf_cols_padded = K / C::GROUP;          // multiple of 4 since K % 256 == 0
-  const int64_t tiles_per_rowtile = sf_cols_padded / 4;
+  const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int64_t tiles_per_rowtile = (K / C::GROUP) / 4;  // 128x4 scale tiles along K
   const int n_rowtiles = (N + 127) / 128;
 
   if (threadIdx.x == 0) {
@@ -147,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum_full, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiWarps);
     mbar_init(never, 1);
     fence_barrier_init();
   }
@@ -167,29 +172,33 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
     if (elect_one_sync()) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      const bool second_b_tile = (n_blk * 2 + 1) < n_rowtiles;
-      const uint32_t tx = A_BYTES + B_BYTES + C::SFA_BYTES + (second_b_tile ? 2u : 1u) * C::SFA_BYTES;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % STAGES;
-        const int round = kb / STAGES;
-        if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
-        uint8_t* st = smem + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], tx);
-        tma_load_2d(st, &tmA, &full[s], kb * BK_BYTES, m0);
-        tma_load_2d(st + A_BYTES, &tmB, &full[s], kb * BK_BYTES, n0);
-        const int64_t tcol = (int64_t)kb * C::TILES_PER_STAGE;
-        bulk_load(st + A_BYTES + B_BYTES, sx + ((int64_t)m_blk * tiles_per_rowtile + tcol) * 512,
-                  C::SFA_BYTES, &full[s]);
-        bulk_load(st + A_BYTES + B_BYTES + C::SFA_BYTES,
-                  sw + ((int64_t)(2 * n_blk) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES, &full[s]);
-        if (second_b_tile)
-          bulk_load(st + A_BYTES + B_BYTES + 2 * C::SFA_BYTES,
-                    sw + ((int64_t)(2 * n_blk + 1) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES,
-                    &full[s]);
+      int g = 0;  // k-blocks issued by this CTA so far (ring position)
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int m_blk = tile % num_m, n_blk = tile / num_m;
+        const bool second_b_tile = (n_blk * 2 + 1) < n_rowtiles;
+        const uint32_t tx = A_BYTES + B_BYTES + C::SFA_BYTES + (second_b_tile ? 2u : 1u) * C::SFA_BYTES;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int s = g % STAGES;
+          const int round = g / STAGES;
+          if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
+          uint8_t* st = smem + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_2d(st, &tmA, &full[s], kb * BK_BYTES, m_blk * BM);
+          tma_load_2d(st + A_BYTES, &tmB, &full[s], kb * BK_BYTES, n_blk * BN);
+          const int64_t tcol = (int64_t)kb * C::TILES_PER_STAGE;
+          bulk_load(st + A_BYTES + B_BYTES, sx + ((int64_t)m_blk * tiles_per_rowtile + tcol) * 512,
+                    C::SFA_BYTES, &full[s]);
+          bulk_load(st + A_BYTES + B_BYTES + C::SFA_BYTES,
+                    sw + ((int64_t)(2 * n_blk) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES, &full[s]);
+          if (second_b_tile)
+            bulk_load(st + A_BYTES + B_BYTES + 2 * C::SFA_BYTES,
+                      sw + ((int64_t)(2 * n_blk + 1) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES,
+                      &full[s]);
+        }
       }
       // drain: every stage's last fill has landed before the CTA may exit
-      for (int kb = std::max(0, num_kb - STAGES); kb < num_kb; ++kb)
-        mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1, err, failed);
+      for (int k = (g > STAGES ? g - STAGES : 0); k < g; ++k)
+        mbar_wait(&full[k % STAGES], (k / STAGES) & 1, err, failed);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer --
@@ -198,62 +207,81 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
         bool injected = false;  // separate flag: the injected expiry must not stop later waits
         mbar_wait(never, 0, err, injected, 2000000LL);
       }
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % STAGES;
-        mbar_wait(&full[s], (kb / STAGES) & 1, err, failed);
+      int g = 0, it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+        // the epilogue must have read the previous tile's accumulator
+        if (it > 0) mbar_wait(acc_empty, (it - 1) & 1, err, failed);
         tc_fence_after();
-        const uint32_t st = base + s * C::STAGE_BYTES;
-        const uint32_t sfa_smem = st + A_BYTES + B_BYTES;
-        const uint32_t sfb_smem = sfa_smem + C::SFA_BYTES;
-        const uint32_t sfa_t = tmem + SF_COL + s * 48;
-        const uint32_t sfb_t = sfa_t + 16;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int s = g % STAGES;
+          mbar_wait(&full[s], (g / STAGES) & 1, err, failed);
+          tc_fence_after();
+          const uint32_t st = base + s * C::STAGE_BYTES;
+          const uint32_t sfa_smem = st + A_BYTES + B_BYTES;
+          const uint32_t sfb_smem = sfa_smem + C::SFA_BYTES;
+          const uint32_t sfa_t = tmem + SF_COL + s * 48;
+          const uint32_t sfb_t = sfa_t + 16;
 #pragma unroll
-        for (int j = 0; j < C::TILES_PER_STAGE; ++j) {
-          tc_cp_sf(sfa_t + 4 * j, desc_sf(sfa_smem + 512 * j));
-          tc_cp_sf(sfb_t + 8 * j, desc_sf(sfb_smem + 512 * j));
-          tc_cp_sf(sfb_t + 8 * j + 4, desc_sf(sfb_smem + C::SFA_BYTES + 512 * j));
-        }
-        const uint64_t adesc = desc_sw128(st);
-        const uint64_t bdesc = desc_sw128(st + A_BYTES);
+          for (int j = 0; j < C::TILES_PER_STAGE; ++j) {
+            tc_cp_sf(sfa_t + 4 * j, desc_sf(sfa_smem + 512 * j));
+            tc_cp_sf(sfb_t + 8 * j, desc_sf(sfb_smem + 512 * j));
+            tc_cp_sf(sfb_t + 8 * j + 4, desc_sf(sfb_smem + C::SFA_BYTES + 512 * j));
+          }
+          const uint64_t adesc = desc_sw128(st);
+          const uint64_t bdesc = desc_sw128(st + A_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / 64; ++k) {
-          // K = 64 fp4 = 32 bytes further along the swizzled 128-byte row
-          const int tile = (MODE == 2) ? k : (k >> 1);
-          const uint32_t sf_id = (MODE == 2) ? 0u : (uint32_t)((k & 1) * 2);
-          const uint32_t idesc = C::IDESC | (sf_id << 29) | (sf_id << 4);
-          tc_mma<MODE>(tmem + ACC_COL, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
-                       sfa_t + 4 * tile, sfb_t + 8 * tile, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BK / 64; ++k) {
+            // K = 64 fp4 = 32 bytes further along the swizzled 128-byte row
+            const int tl = (MODE == 2) ? k : (k >> 1);
+            const uint32_t sf_id = (MODE == 2) ? 0u : (uint32_t)((k & 1) * 2);
+            const uint32_t idesc = C::IDESC | (sf_id << 29) | (sf_id << 4);
+            tc_mma<MODE>(tmem + ACC_COL, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                         sfa_t + 4 * tl, sfb_t + 8 * tl, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
         }
-        tc_commit(&empty[s]);
+        tc_commit(acc_full);
       }
-      tc_commit(accum_full);
     }
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
+    // 8 warps: lane quadrant q = warp % 4 (tensor-memory access rule), column half h.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     const float alpha = __fmul_rn(gs_x ? __ldg(gs_x) : 1.0f, gs_w ? __ldg(gs_w) : 1.0f);
-    mbar_wait(accum_full, 0, err, failed);
-    tc_fence_after();
-    const int row = m0 + 32 * q + lane;
-    uint16_t* orow = out + (int64_t)row * N;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      uint32_t r[16];
-      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + ACC_COL + c, r);
-      tmem_ld_wait();
-      const int col = n0 + c;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const int m_blk = tile % num_m, n_blk = tile / num_m;
+      mbar_wait(acc_full, it & 1, err, failed);
+      tc_fence_after();
+      // drain this warp's 32 rows x 128 columns into registers as packed bf16
+      uint32_t o[64];
+#pragma unroll
+      for (int c4 = 0; c4 < 2; ++c4) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + ACC_COL + h * 128 + (c4 * 4 + j) * 16, r[j]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o[(c4 * 4 + j) * 8 + e] = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[j][2 * e]), alpha),
+                                                     __fmul_rn(__uint_as_float(r[j][2 * e + 1]), alpha));
+      }
+      // the accumulator may now be overwritten by the next tile's MMAs
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      const int row = m_blk * BM + 32 * q + lane;
       if (row < M) {
-        uint4 o0, o1;
-        o0.x = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[0]), alpha), __fmul_rn(__uint_as_float(r[1]), alpha));
-        o0.y = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[2]), alpha), __fmul_rn(__uint_as_float(r[3]), alpha));
-        o0.z = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[4]), alpha), __fmul_rn(__uint_as_float(r[5]), alpha));
-        o0.w = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[6]), alpha), __fmul_rn(__uint_as_float(r[7]), alpha));
-        o1.x = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[8]), alpha), __fmul_rn(__uint_as_float(r[9]), alpha));
-        o1.y = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[10]), alpha), __fmul_rn(__uint_as_float(r[11]), alpha));
-        o1.z = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[12]), alpha), __fmul_rn(__uint_as_float(r[13]), alpha));
-        o1.w = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[14]), alpha), __fmul_rn(__uint_as_float(r[15]), alpha));
-        if (col < N) *reinterpret_cast<uint4*>(orow + col) = o0;
-        if (col + 8 < N) *reinterpret_cast<uint4*>(orow + col + 8) = o1;
+        uint16_t* orow = out + (int64_t)row * N + n_blk * BN + h * 128;
+        const int cols_left = N - (n_blk * BN + h * 128);
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+          if (8 * v < cols_left)
+            *reinterpret_cast<uint4*>(orow + 8 * v) = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
       }
     }
   }
@@ -302,7 +330,8 @@ cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
   if (smem > d.smem_optin) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(qqmm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  dim3 grid((unsigned)std::min<int64_t>(tiles, d.sm_count));
   qqmm_kernel<MODE><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, out,
                                                   d.err, inject);
   return cudaGetLastError();

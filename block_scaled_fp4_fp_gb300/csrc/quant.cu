@@ -16,6 +16,7 @@ namespace fp4 {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kQThreads = 64;
 constexpr float kNvfp4MaxProduct = 2688.0f;  // 448 * 6
 
 // ------------------------------------------------------------------ amax --
@@ -79,45 +80,29 @@ __global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __
 }
 
 // -------------------------------------------------------------- quantize --
-// One thread per 16-byte chunk (8 bf16); a group is 2 (NVFP4) or 4 (MXFP4)
-// neighbouring lanes, so the block amax is an in-thread max plus one or two
-// xor-shuffles, and the codes leave as one coalesced uint32 per thread.
+// One thread per block-scale group (16 or 32 bf16 = 2 or 4 16-byte loads), so
+// the scale arithmetic (one correctly rounded division and reciprocal for
+// NVFP4) runs once per group.  2-D grid: blockIdx.x/threadIdx.x pick the group
+// within a row, blockIdx.y strides over rows (two rows per thread in flight);
+// no index needs a division.  Codes leave as 8/16 contiguous bytes per thread.
+// Blocks with blockIdx.x >= main_bx zero the padding of a tiled scale buffer.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, const float* __restrict__ gs_ptr,
-    uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, int tiled, int64_t padded_rows,
-    int64_t padded_cols, int64_t main_blocks) {
-  constexpr int G = (MODE == 2) ? 16 : 32;
-  const int64_t scols = cols / G;
-  if ((int64_t)blockIdx.x >= main_blocks) {
-    // zero the padding bytes of the tiled scale buffer
-    const int64_t total = padded_rows * padded_cols;
-    for (int64_t off = ((int64_t)blockIdx.x - main_blocks) * blockDim.x + threadIdx.x; off < total;
-         off += (int64_t)(gridDim.x - main_blocks) * blockDim.x) {
-      const int64_t tile = off >> 9, within = off & 511;
-      const int64_t r = (tile / (padded_cols >> 2)) * 128 + (within >> 4) + ((within & 15) >> 2) * 32;
-      const int64_t c = (tile % (padded_cols >> 2)) * 4 + (within & 3);
-      if (r >= rows || c >= scols) scales[off] = 0;
-    }
-    return;
+__device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 4], float gs,
+                                               uint32_t* __restrict__ xq_words,
+                                               uint8_t* __restrict__ scale_byte) {
+  constexpr int NV = (MODE == 2) ? 2 : 4;
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    m2 = __vmaxu2(m2, v[i].x & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, v[i].y & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, v[i].z & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, v[i].w & 0x7FFF7FFFu);
   }
-  const int64_t nchunks = rows * cols / 8;
-  const int64_t ch = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool valid = ch < nchunks;
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (valid) v = ld_stream_v4(x + ch * 8);
-  uint32_t mb = max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu));
-  mb = max(mb, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
-  mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-  if (MODE == 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-  if (!valid) return;
-
-  float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
   float mul;
   uint32_t sbyte;
   if (MODE == 2) {
-    const float gs = gs_ptr ? __ldg(gs_ptr) : 1.0f;
     const float b = __uint_as_float(mb << 16);
     const float p = __fmul_rn(6.0f, gs);
     const float s = (b == 0.0f) ? 0.0f : __fdiv_rn(b, p);
@@ -134,16 +119,72 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(
     sbyte = (uint32_t)(se + 127);
     mul = exp2i_f32(-se);
   }
-  uint32_t word = 0;
+  uint32_t out[NV];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    word |= e2m1x2_rn(__fmul_rn(f[2 * j], mul), __fmul_rn(f[2 * j + 1], mul)) << (8 * j);
-  xq[ch] = word;
-  if ((ch & (G / 8 - 1)) == 0) {
-    const int64_t e0 = ch * 8;
-    const int64_t r = e0 / cols, c = (e0 % cols) / G;
-    const int64_t off = tiled ? tiled_scale_offset(r, c, padded_cols) : r * scols + c;
-    scales[off] = (uint8_t)sbyte;
+  for (int i = 0; i < NV; ++i) {
+    const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
+    out[i] = word;
+  }
+  if (MODE == 2) {
+    *reinterpret_cast<uint2*>(xq_words) = make_uint2(out[0], out[1]);
+  } else {
+    *reinterpret_cast<uint4*>(xq_words) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  *scale_byte = (uint8_t)sbyte;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kQThreads) quantize_kernel(
+    const uint16_t* __restrict__ x, int rows, int cols, const float* __restrict__ gs_ptr,
+    uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, int tiled, int padded_rows,
+    int padded_cols, int main_bx) {
+  constexpr int G = (MODE == 2) ? 16 : 32;
+  constexpr int NV = G / 8;
+  constexpr int RT = (MODE == 2) ? 4 : 2;  // rows in flight per thread (64 or 128 bytes... 128 bytes)
+  const int scols = cols / G;
+  if ((int)blockIdx.x >= main_bx) {
+    // zero the padding bytes of the tiled scale buffer
+    const int64_t total = (int64_t)padded_rows * padded_cols;
+    const int64_t nthreads = (int64_t)(gridDim.x - main_bx) * gridDim.y * blockDim.x;
+    const int64_t first = ((int64_t)blockIdx.y * (gridDim.x - main_bx) + (blockIdx.x - main_bx)) * blockDim.x +
+                          threadIdx.x;
+    const int tiles_per_row = padded_cols >> 2;
+    for (int64_t off = first; off < total; off += nthreads) {
+      const int64_t tile = off >> 9;
+      const int within = (int)(off & 511);
+      const int r = (int)(tile / tiles_per_row) * 128 + (within >> 4) + ((within & 15) >> 2) * 32;
+      const int c = (int)(tile % tiles_per_row) * 4 + (within & 3);
+      if (r >= rows || c >= scols) scales[off] = 0;
+    }
+    return;
+  }
+  const int gi = blockIdx.x * blockDim.x + threadIdx.x;  // group within the row
+  if (gi >= scols) return;
+  const float gs = (MODE == 2 && gs_ptr) ? __ldg(gs_ptr) : 1.0f;
+  const int wpr = cols >> 3;  // code words per row
+  const int gy = gridDim.y;
+  for (int r = blockIdx.y; r < rows; r += RT * gy) {
+    uint4 a[RT][NV];
+#pragma unroll
+    for (int k = 0; k < RT; ++k) {
+      const int rk = r + k * gy;
+      if (rk < rows) {
+        const uint4* pa = reinterpret_cast<const uint4*>(x + (int64_t)rk * cols + gi * G);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) a[k][i] = ld_stream_v4(pa + i);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < RT; ++k) {
+      const int rk = r + k * gy;
+      if (rk < rows)
+        quantize_group<MODE>(a[k], gs, xq + (int64_t)rk * wpr + gi * NV,
+                             scales + (tiled ? tiled_scale_offset(rk, gi, padded_cols) : (int64_t)rk * scols + gi));
+    }
   }
 }
 
@@ -211,21 +252,27 @@ cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* g
 cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, int64_t cols,
                             int mode, int group, const float* gs, uint32_t* xq, uint8_t* scales,
                             int tiled, cudaStream_t s) {
-  (void)d;
-  const int64_t nchunks = rows * cols / 8;
-  const int64_t main_blocks = (nchunks + kThreads - 1) / kThreads;
   const int64_t scols = cols / group;
+  const int64_t main_bx = (scols + kQThreads - 1) / kQThreads;
   const int64_t prow = ((rows + 127) / 128) * 128, pcol = ((scols + 3) / 4) * 4;
-  int64_t pad_blocks = 0;
-  if (tiled && (prow != rows || pcol != scols))
-    pad_blocks = std::min<int64_t>((prow * pcol + kThreads - 1) / kThreads, 1024);
-  const unsigned grid = (unsigned)(main_blocks + pad_blocks);
+  // enough (x, y) blocks for ~16 resident 64-thread blocks per SM; each thread
+  // keeps 2-4 rows of loads in flight and strides over the rest
+  const int64_t rt = (mode == 2) ? 4 : 2;
+  int64_t gy = std::max<int64_t>(1, ((int64_t)d.sm_count * 16) / main_bx);
+  gy = std::min<int64_t>(gy, std::min<int64_t>((rows + rt - 1) / rt, 65535));
+  gy = std::max<int64_t>(gy, 1);
+  int64_t pad_bx = 0;
+  if (tiled && (prow != rows || pcol != scols)) {
+    const int64_t pad = prow * pcol;
+    pad_bx = std::min<int64_t>(std::max<int64_t>((pad + kQThreads * gy - 1) / (kQThreads * gy), 1), 64);
+  }
+  dim3 grid((unsigned)(main_bx + pad_bx), (unsigned)gy);
   if (mode == 2)
-    quantize_kernel<2><<<grid, kThreads, 0, s>>>(x, rows, cols, gs, xq, scales, tiled, prow, pcol,
-                                                 main_blocks);
+    quantize_kernel<2><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, gs, xq, scales, tiled, (int)prow,
+                                                  (int)pcol, (int)main_bx);
   else
-    quantize_kernel<1><<<grid, kThreads, 0, s>>>(x, rows, cols, nullptr, xq, scales, tiled, prow,
-                                                 pcol, main_blocks);
+    quantize_kernel<1><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, nullptr, xq, scales, tiled,
+                                                  (int)prow, (int)pcol, (int)main_bx);
   return cudaGetLastError();
 }
 

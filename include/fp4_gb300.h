@@ -107,7 +107,7 @@ fp4_status fp4_amax_global_scale(const fp4_bf16* x, int64_t n, float* gs_out, fl
  *   mode, bits, group_size: (NVFP4, 4, 16) or (MXFP4, 4, 32); affine quantize is
  *                not provided (FP4_ERR_UNSUPPORTED)
  *   global_scale device fp32 scalar gs (NVFP4 only) or NULL (gs = 1)
- *   xq           uint32[rows, cols/8] packed codes, 4-byte aligned
+ *   xq           uint32[rows, cols/8] packed codes, 8-byte (NVFP4) / 16-byte (MXFP4) aligned
  *   scales       uint8 E4M3/E8M0 block scales in `layout`; for TILED_128x4 the
  *                whole padded buffer (Rp*Cp bytes) is written, padding with 0
  * Per NVFP4 group: b = max|x|, s8 = E4M3_rn_sat(b/(6*gs)) (0 when b = 0),
