@@ -8,34 +8,46 @@
 // The tensor core decodes the weights: W streams by TMA as the block-scaled
 // FP4 A operand of tcgen05.mma.kind::mxf4nvf4 (E4M3 scales per 16, applied by
 // the hardware), so no instruction touches a weight.  The bf16 activation x is
-// written as kTerms NVFP4 terms in radix 4, block by block (16 elements):
-//     x = 2^e0 * S_b * (sum_t d_t 4^-t + r),   d_t in {-2, ..., 2},
-// with 2^e0 a per-vector power of two (max|x| / 2^e0 in [256, 512)) and S_b a
-// power of two per block chosen so |x| / (2^e0 S_b) <= 2: then
-// d_0 = rint(v), v <- 4 (v - d_0), ... keeps every digit in [-2, 2] (exact
-// e2m1 codes) and each term's block scale S_b 4^-t is an exact E4M3 value.
-// Eight terms carry 16 bits per block -- |r| <= 2^-15 of the block scale,
-// about 2^-13 of a typical element -- and become rows 0..7 of the B operand.  The MMA
-// yields D[row, t] = sum_k W[row, k] (d_t S_b 4^-t)[k] in fp32 tensor memory;
-// the epilogue forms y = gs_w 2^e0 sum_t D[row, t].
+// written as kTerms = 9 FP4 terms in radix 4 over one power-of-two scale per
+// CTA slice of K:
+//     x = 2^e0 * (sum_t d_t 2^(7 - 2t) + r),   d_t in {-2, ..., 2},
+// with max|x| / 2^e0 in [128, 256).  Rounding r_t 2^(2t-7) to the nearest
+// integer and subtracting keeps every digit in [-2, 2] (exact e2m1 codes);
+// the term weights 2^7 ... 2^-9 are exact E4M3 values, and |r| <= 2^-10, at
+// most 2^-17 of max|x|.  The terms are rows 0..8 of the B operand (N = 16;
+// rows 9..15 carry zero scales), so the term-scale tile is one constant tile.
+// The MMA yields D[row, t] = sum_k W[row, k] d_t[k] 2^(7-2t) in fp32 tensor
+// memory; the epilogue forms y = gs_w 2^e0 sum_t D[row, t].
 //
-// One CTA per SM owns <= 128 consecutive rows (row ranges balanced to +-1).
-//   warp 0: TMA producer -- 8-row atoms of W (128-byte swizzle) per K = 256
-//           stage, into a 6-stage ring, issued before griddepcontrol.wait
-//           (programmatic dependent launch: no earlier kernel writes W);
-//   warp 1: tensor memory allocation; one thread copies each stage's scale
-//           tiles to tensor memory (tcgen05.cp) and issues 4 MMAs (M 128,
-//           N 16, K 64) into four independent accumulators;
-//   warps 2-17: four groups of four warps; group g prepares stages
-//           kb % 4 == g -- permute the weights' linear E4M3 scales into the
-//           128x4 tile order tcgen05.cp reads, copy the < 8 rows that do not
-//           fill a TMA atom, and build the x terms (codes + scales); after the
-//           last stage group 0 reads D and writes y.
-// The B operand's rows 8-15 are the next stage's term atom (128-byte-swizzle
-// stride 1024); their block scales are zero, so they add nothing.
+// Work split.  A cluster of `split` CTAs owns R <= 128 consecutive rows; CTA
+// rank i of the cluster takes the i-th slice of the K stages (K = 256 each),
+// so a light problem runs fewer, fuller stages per CTA.  Each CTA sums its
+// slice into fp32 partials; ranks 1.. store theirs into rank 0's shared
+// memory (distributed shared memory), and rank 0 adds them in rank order --
+// the same order on every run -- and writes y.
+//   warp 0: TMA producer -- per stage one box of R rows x 128 bytes of W
+//           (128-byte swizzle, so rows land as the 8-row atoms the MMA reads)
+//           and one box of R rows x 16 bytes of W's linear E4M3 scales, into
+//           a ring sized in bytes (a slot holds ceil(R/8) KB of codes; up to
+//           32 slots).  Issued before griddepcontrol.wait (programmatic
+//           dependent launch: W is not written by the kernel this one
+//           overlaps);
+//   warp 1: tensor memory allocation; one thread copies each stage's four
+//           weight-scale tiles to tensor memory (tcgen05.cp) and issues 4 MMAs
+//           (M 128, N 16, K 64) into four independent accumulators, then one
+//           commit that frees the stage's operands.  A-operand rows >= R read
+//           whatever follows the slot; their scales are zero;
+//   warps 2-17: four groups of four warps; group g prepares local stages
+//           i % 4 == g into a ring of kMeta operand slots: the x terms, then,
+//           once the stage's weights have landed, the weights' scales
+//           permuted into the 128x4 tile order tcgen05.cp reads.  A group that
+//           finds operand slot m free again (stage i - kMeta done) passes the
+//           weight slot of that stage back to the TMA producer.  After the
+//           last stage group 0 reads D and forms the partials.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -44,34 +56,46 @@ namespace fp4 {
 
 namespace {
 
-constexpr int kTerms = 8;           // x expansion terms (B rows 0..7, one 1 KB atom)
-constexpr int kStages = 6;          // W / scale-tile / term ring
-constexpr int kRawDepth = 12;       // ring of the prep warps' own copies (scales, partial-atom rows)
-constexpr int kAhead = 8;           // their lookahead (a multiple of kGroups), independent of MMA progress
-constexpr uint32_t kRawBytes = 128 * 16 + 8 * 128;  // 128 rows x 16 scale bytes + up to 8 rows x 128 B
+constexpr int kTerms = 9;           // x expansion terms (B rows 0..8)
+constexpr int kMeta = 6;            // ring of per-stage MMA operands built by the prep warps
+constexpr int kMaxSlots = 32;       // weight ring slots at most
 constexpr int kBK = 256;            // codes per stage (128 bytes per row)
 constexpr int kRows = 128;          // rows per CTA at most (one M = 128 tile)
-constexpr int kGroups = 4;          // prep groups; group g prepares stages kb % kGroups == g
+constexpr int kMaxSplit = 8;        // CTAs per cluster at most (portable cluster size)
+constexpr int kGroups = 4;          // prep groups; group g prepares local stages i % kGroups == g
 constexpr int kGroupThreads = 128;  // one group = 4 warps, two elements per thread per stage
 constexpr int kPrep = kGroups * kGroupThreads;
 constexpr int kThreads = 64 + kPrep;  // TMA warp, MMA warp, prep warps (group 0 also runs the epilogue)
-constexpr uint32_t kWBytes = kRows * 128;  // 16 KB
-constexpr uint32_t kSFBytes = 4 * 512;     // four 128x4 scale tiles (one per MMA k-step)
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = 64;            // D: four accumulators of 16 columns, [0, 64)
+constexpr uint32_t kSFABytes = 4 * 512;  // four 128x4 weight-scale tiles (one per MMA k-step)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSfbCol = 64;         // D: four accumulators of 16 columns in [0, 64); term scales
+constexpr uint32_t kSfaCol = 80;         // weight scales of operand slot m: kSfaCol + 16 m + 4 j
+static_assert(kSfaCol + kMeta * 16 <= kTmemCols, "scale columns exceed the allocation");
+static_assert(kMeta >= kGroups, "a group's stages must not share an operand slot");
 // kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, N = 16, E4M3 scales, M = 128
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
-// shared memory offsets (from a 1024-aligned base)
-constexpr uint32_t kOffW = 0;
-constexpr uint32_t kOffB = kOffW + kStages * kWBytes;            // (kStages + 1) term atoms of 1 KB
-constexpr uint32_t kOffSFA = kOffB + (kStages + 1) * 1024;
-constexpr uint32_t kOffSFB = kOffSFA + kStages * kSFBytes;
-constexpr uint32_t kOffRaw = kOffSFB + kStages * kSFBytes;       // kRawDepth x kRawBytes
-constexpr uint32_t kOffX = kOffRaw + kRawDepth * kRawBytes;        // x (bf16), K <= kMaxK
-constexpr int kMaxK = 16384 + 1024;                               // 17408
-constexpr uint32_t kOffBar = kOffX + kMaxK * 2;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+// Shared memory (from a 1024-aligned base): [weight ring | term atoms | term-8
+// atoms | weight-scale tiles | term-scale tile | x slice | partials | barriers].
+// The weight ring is split at launch into code slots and, after them, scale slots.
+constexpr int kMaxKSlice = 17408;  // elements of x per CTA
+constexpr uint32_t kSmemBytes = 227u * 1024u;
+constexpr uint32_t kBarBytes = 1024;
+constexpr uint32_t kRedBytes = kMaxSplit * kRows * 4;
+constexpr uint32_t kFixedBytes = 2 * kMeta * 1024 + kMeta * kSFABytes + 512 + kMaxKSlice * 2 + kRedBytes +
+                                 kBarBytes + 1024;
+constexpr uint32_t kRingBytes = (kSmemBytes - kFixedBytes) / 1024u * 1024u;
+constexpr uint32_t kOffB = kRingBytes;                    // terms 0..7 of slot m: one 1 KB atom
+constexpr uint32_t kOffB8 = kOffB + kMeta * 1024;         // term 8 (+ 7 unused rows) of slot m
+constexpr uint32_t kOffSFA = kOffB8 + kMeta * 1024;
+constexpr uint32_t kOffSFB = kOffSFA + kMeta * kSFABytes;
+constexpr uint32_t kOffX = kOffSFB + 512;                 // x slice (bf16)
+constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;      // [split][128] fp32 partials (rank 0)
+constexpr uint32_t kOffBar = kOffRed + kRedBytes;
+static_assert(kOffBar + kBarBytes + 1024 <= kSmemBytes, "shared memory layout overflows");
+// an MMA reads 16 KB of A from a slot's start: that stays inside the allocation
+static_assert(kRingBytes + 16384 <= kOffBar, "A-operand reads past the allocation");
+static_assert((2 * kMaxSlots + 2 * kMeta + 2) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -82,38 +106,63 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// E4M3 byte of 2^e, -9 <= e <= 8
+__host__ __device__ constexpr uint32_t e4m3_pow2(int e) {
+  return (e >= -6) ? (uint32_t)((e + 7) << 3) : (1u << (e + 9));
+}
 
 __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                              const __grid_constant__ CUtensorMap tmS,
                                                               const uint16_t* __restrict__ x,
-                                                              const uint32_t* __restrict__ w,
-                                                              const uint8_t* __restrict__ scales,
                                                               const float* __restrict__ gs_w, int N, int K,
-                                                              uint16_t* __restrict__ y, unsigned* __restrict__ err) {
+                                                              int R, int split, int nslots, uint32_t wslot,
+                                                              uint32_t sslot, uint16_t* __restrict__ y,
+                                                              unsigned* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + kOffBar);  // weight slot landed (TMA bytes)
+  uint64_t* wempty = wfull + kMaxSlots;                           // weight slot consumed (relayed)
+  uint64_t* mfull = wempty + kMaxSlots;                           // stage operands built (prep group)
+  uint64_t* mempty = mfull + kMeta;                               // stage operands consumed (MMA commit)
+  uint64_t* done = mempty + kMeta;
   uint64_t* xbar = done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kPrep / 32 floats
+  float* part = reinterpret_cast<float*>(smem + kOffRed);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + kOffX);
+  const uint32_t offS = (uint32_t)nslots * wslot;  // linear-scale slots follow the code slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = (int)(((int64_t)N * blockIdx.x) / gridDim.x);
-  const int r1 = (int)(((int64_t)N * (blockIdx.x + 1)) / gridDim.x);
-  const int rows = r1 - r0;                  // <= 128
-  const int atoms = rows >> 3, rem = rows & 7;
+  const int rank = (int)(blockIdx.x % (unsigned)split);  // rank within the cluster (clusters are consecutive)
+  const int blk = (int)(blockIdx.x / (unsigned)split);
+  const int nblk = (int)(gridDim.x / (unsigned)split);
+  const int r0 = (int)(((int64_t)N * blk) / nblk);
+  const int r1 = (int)(((int64_t)N * (blk + 1)) / nblk);
+  const int rows = r1 - r0;  // <= R <= 128
   const int nkb = K / kBK;
-  const int words = K >> 3;
+  const int kb0 = (int)(((int64_t)nkb * rank) / split);
+  const int nst = (int)(((int64_t)nkb * (rank + 1)) / split) - kb0;  // this CTA's stages (>= 1)
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (split > 1) cluster_arrive_relaxed();  // matched by the wait before the partials move
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + kGroupThreads);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < nslots; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 1);
+    }
+    for (int s = 0; s < kMeta; ++s) {
+      mbar_init(&mfull[s], kGroupThreads);
+      mbar_init(&mempty[s], 1);
     }
     mbar_init(done, 1);
     mbar_init(xbar, 1);
@@ -124,58 +173,74 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
                  :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // rows 8..15 of every stage's term scale tiles stay zero (those B rows add nothing)
-  for (uint32_t i = threadIdx.x; i < kStages * kSFBytes / 4; i += kThreads)
-    reinterpret_cast<uint32_t*>(smem + kOffSFB)[i] = 0u;
+  // The constant term-scale tile: B row t < 9 (tile row t, slot 0) holds the
+  // E4M3 weight 2^(7-2t) for each of the k-step's four 16-element blocks;
+  // rows 9..31 are zero, so B rows 9..15 add nothing.
+  if (threadIdx.x < 128) {
+    const int row = threadIdx.x >> 2, word = threadIdx.x & 3;
+    const uint32_t v = (row < kTerms && word == 0) ? e4m3_pow2(7 - 2 * row) * 0x01010101u : 0u;
+    reinterpret_cast<uint32_t*>(smem + kOffSFB)[threadIdx.x] = v;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  float partial = 0.f;  // group 0: this CTA's partial y of row 32 (warp & 3) + lane
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (weights)
     if (elect_one_sync()) {
       prefetch_tmap(&tmW);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages, round = kb / kStages;
-        if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)atoms * 1024u);
-        uint8_t* st = smem + kOffW + s * kWBytes;
-        for (int a = 0; a < atoms; ++a) tma_load_2d(st + a * 1024, &tmW, &full[s], kb * 128, r0 + 8 * a);
+      prefetch_tmap(&tmS);
+      const uint32_t tx = (uint32_t)R * (128u + 16u);  // out-of-range rows are zero-filled and counted
+      int s = 0, round = 0;
+      for (int i = 0; i < nst; ++i) {
+        if (round > 0) mbar_wait(&wempty[s], (round - 1) & 1, err, failed);
+        mbar_arrive_expect_tx(&wfull[s], tx);
+        tma_load_2d(smem + s * wslot, &tmW, &wfull[s], (kb0 + i) * 128, r0);
+        tma_load_2d(smem + offS + s * sslot, &tmS, &wfull[s], (kb0 + i) * 16, r0);
+        if (++s == nslots) { s = 0; ++round; }
       }
-      for (int k = std::max(0, nkb - kStages); k < nkb; ++k)
-        mbar_wait(&full[k % kStages], (k / kStages) & 1, err, failed);
+      // no copy may still be writing shared memory when the CTA exits
+      for (int i = max(0, nst - nslots); i < nst; ++i)
+        mbar_wait(&wfull[i % nslots], (i / nslots) & 1, err, failed);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (elect_one_sync()) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        mbar_wait(&full[s], (kb / kStages) & 1, err, failed);
+      asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+                   :: "r"(tmem + kSfbCol), "l"(desc_sf(base + kOffSFB)) : "memory");
+      const uint32_t sfb_t = tmem + kSfbCol;
+      int m = 0, mround = 0, s = 0;
+      for (int i = 0; i < nst; ++i) {
+        mbar_wait(&mfull[m], mround & 1, err, failed);  // the group also saw the weights land
         tc_fence_after();
-        const uint32_t sfa_t = tmem + kSfCol + s * 32, sfb_t = sfa_t + 16;
-        const uint32_t sfa_s = base + kOffSFA + s * kSFBytes, sfb_s = base + kOffSFB + s * kSFBytes;
+        const uint32_t sfa_t = tmem + kSfaCol + 16 * m;
+        const uint32_t sfa_s = base + kOffSFA + m * kSFABytes;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(sfa_t + 4 * j), "l"(desc_sf(sfa_s + 512 * j)) : "memory");
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(sfb_t + 4 * j), "l"(desc_sf(sfb_s + 512 * j)) : "memory");
-        }
-        const uint64_t adesc = desc_sw128(base + kOffW + s * kWBytes, 1024);
-        const uint64_t bdesc = desc_sw128(base + kOffB + s * 1024, 1024);  // rows 8-15: next term atom
+        for (int j = 0; j < 4; ++j)  // scale tiles start on 4-column boundaries of tensor memory
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
+                       :: "r"(sfa_t + 4 * j), "l"(desc_sf(sfa_s + 512 * j)) : "memory");
+        const uint64_t adesc = desc_sw128(base + s * wslot, 1024);
+        // B rows 0..7: the slot's term atom; rows 8..15: its term-8 atom, kMeta KB further
+        const uint64_t bdesc = desc_sw128(base + kOffB + m * 1024, kMeta * 1024);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           // k-step j accumulates into its own 16-column tile, so the four MMAs of a
           // stage do not wait on each other; the epilogue adds the four tiles
-          const uint32_t acc = (kb > 0) ? 1u : 0u;
+          const uint32_t acc = (i > 0) ? 1u : 0u;
           asm volatile(
               "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
               "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
               :: "r"(tmem + 16 * j), "l"(adesc + (uint64_t)(2 * j)), "l"(bdesc + (uint64_t)(2 * j)), "r"(kIdesc),
-                 "r"(sfa_t + 4 * j), "r"(sfb_t + 4 * j), "r"(acc) : "memory");
+                 "r"(sfa_t + 4 * j), "r"(sfb_t), "r"(acc) : "memory");
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                     :: "r"(smem_u32(&empty[s])) : "memory");
+                     :: "r"(smem_u32(&mempty[m])) : "memory");
+        if (++m == kMeta) { m = 0; ++mround; }
+        if (++s == nslots) s = 0;
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    :: "r"(smem_u32(done)) : "memory");
@@ -186,14 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     const int grp = pa / kGroupThreads;        // prep group
     const int pt = pa % kGroupThreads;         // thread within the group
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // x (bf16, K*2 bytes) -> shared memory in one bulk copy, then max|x| from shared memory
+    // this CTA's slice of x (bf16, nst * 512 bytes) -> shared memory in one bulk copy
+    const uint32_t xbytes = (uint32_t)nst * (kBK * 2);
     if (pa == 0) {
-      mbar_arrive_expect_tx(xbar, (uint32_t)K * 2u);
-      bulk_load(xs, x, (uint32_t)K * 2u, xbar);
+      mbar_arrive_expect_tx(xbar, xbytes);
+      bulk_load(xs, x + (int64_t)kb0 * kBK, xbytes, xbar);
     }
     mbar_wait(xbar, 0, err, failed);
     uint32_t m2 = 0;
-    for (int v = pa; v < words; v += kPrep) {
+    for (int v = pa; v < nst * (kBK / 8); v += kPrep) {
       const uint4 q = reinterpret_cast<const uint4*>(xs)[v];
       m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
       m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
@@ -208,135 +274,90 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < kPrep / 32; ++i) amax = fmaxf(amax, red[i]);
-    // e0: max|x| / 2^e0 in [256, 512), so every block scale S_b = 2^k fits k <= 8
+    // e0: max|x| / 2^e0 in [128, 256) (bf16 magnitudes sort as integers; a NaN
+    // or infinity in the slice shows as a value above the largest finite one)
+    const bool finite = amax <= 3.3895313892515355e38f;
     int e0 = 0;
-    if (amax > 0.f) {
+    if (amax > 0.f && finite) {
       int ex;
       frexpf(amax, &ex);  // amax = m * 2^ex, 0.5 <= m < 1
-      e0 = max(ex - 9, -126);
+      e0 = max(ex - 8, -126);
     }
     const float pre = ldexpf(1.0f, -e0);
 
-    const int b16 = pt >> 3;  // this thread's 16-element block within the stage (0..15)
-    // The prep warps' global traffic -- row pt's 16 linear scale bytes and, for
-    // threads < 8*rem, one 16-byte piece of the rows that do not fill a TMA atom --
-    // runs kAhead stages ahead through a private cp.async ring.  Every thread later
-    // reads back only what it copied itself, so the ring needs no barrier and never
-    // waits for the MMA.
-    auto issue = [&](int kb) {
-      const uint32_t slot = base + kOffRaw + (kb % kRawDepth) * kRawBytes;
-      if (pt < rows) {
-        const uint8_t* src = scales + (int64_t)(r0 + pt) * (K >> 4) + kb * 16;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(slot + pt * 16), "l"(src) : "memory");
+    // stage bookkeeping without divisions: operand slot m (round mr), weight slot s (round wr)
+    int m = grp, mr = 0, s = grp, wr = 0;
+    const int lo = pt & 15, hi4 = ((pt >> 4) & 7) << 4;
+    for (int i = grp; i < nst; i += kGroups) {
+      if (i >= kMeta) {
+        mbar_wait(&mempty[m], (mr - 1) & 1, err, failed);  // operand slot m is free: stage i - kMeta is done
+        if (pt == 0) {
+          int sj = s - kMeta;  // weight slot of stage i - kMeta (nslots >= kMeta)
+          if (sj < 0) sj += nslots;
+          mbar_arrive(&wempty[sj]);
+        }
       }
-      if (pt < rem * 8) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(w) + (int64_t)(r0 + 8 * atoms + (pt >> 3)) * (K >> 1) +
-                             kb * 128 + (pt & 7) * 16;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(slot + 2048 + pt * 16), "l"(src) : "memory");
+      // (a) x terms for elements 2pt, 2pt+1 of this stage (radix-4 digits, see the header)
+      const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + i * kBK + 2 * pt);
+      float r0v = bf16_lo(xv) * pre, r1v = bf16_hi(xv) * pre;
+      uint8_t* batom = smem + kOffB + m * 1024;
+#pragma unroll
+      for (int t = 0; t < kTerms; ++t) {
+        // d = rint(r / 2^(7-2t)): one fused multiply-add onto 1.5 * 2^23 rounds the
+        // exact product to an integer; subtracting the constant back is exact
+        const float inv = __int_as_float((127 - (7 - 2 * t)) << 23);  // 2^-(7-2t)
+        const float w = __int_as_float((127 + (7 - 2 * t)) << 23);    // 2^(7-2t)
+        const float d0 = __fsub_rn(__fmaf_rn(r0v, inv, 12582912.0f), 12582912.0f);
+        const float d1 = __fsub_rn(__fmaf_rn(r1v, inv, 12582912.0f), 12582912.0f);
+        r0v = __fmaf_rn(-w, d0, r0v);  // exact: |result| <= w / 2
+        r1v = __fmaf_rn(-w, d1, r1v);
+        const uint8_t code = (uint8_t)e2m1x2_rn(d0, d1);  // exact: digits in [-2, 2]
+        // byte pt of term row t (row 0 of the term-8 atom for t = 8), 128-byte swizzle
+        if (t < 8) batom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
+        else batom[kMeta * 1024 + hi4 + lo] = code;
       }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    // this group's stages are grp, grp + kGroups, ...; its copies run kAhead/kGroups of them ahead
-    constexpr int kAheadG = kAhead / kGroups;
-    int issued = grp;
-    for (int p = 0; p < kAheadG; ++p) {
-      if (issued < nkb) issue(issued);
-      else asm volatile("cp.async.commit_group;" ::: "memory");
-      issued += kGroups;
-    }
-    for (int kb = grp; kb < nkb; kb += kGroups) {
-      const int s = kb % kStages, round = kb / kStages;
-      if (issued < nkb) issue(issued);
-      else asm volatile("cp.async.commit_group;" ::: "memory");  // keep the group count uniform
-      issued += kGroups;
-      asm volatile("cp.async.wait_group %0;" :: "n"(kAheadG) : "memory");  // this thread's copies for kb
-      const uint8_t* rawp = smem + kOffRaw + (kb % kRawDepth) * kRawBytes;
-      if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);  // stage slot s is free
-      // (a) weight scales of row pt: 16 E4M3 bytes -> word j of tile j, 16B-row (pt%32), slot pt/32
-      uint8_t* sfa = smem + kOffSFA + s * kSFBytes;
+      // (b) weight scales of row pt, once the stage has landed: 16 E4M3 bytes ->
+      // word j of tile j, 16-byte row (pt % 32), slot pt / 32; rows >= rows get 0
+      mbar_wait(&wfull[s], wr & 1, err, failed);
       uint4 sv = make_uint4(0, 0, 0, 0);
-      if (pt < rows) sv = *reinterpret_cast<const uint4*>(rawp + pt * 16);
+      if (pt < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + pt * 16);
+      uint8_t* sfa = smem + kOffSFA + m * kSFABytes;
       const uint32_t so = (uint32_t)((pt & 31) * 16 + (pt >> 5) * 4);
       *reinterpret_cast<uint32_t*>(sfa + 0 * 512 + so) = sv.x;
       *reinterpret_cast<uint32_t*>(sfa + 1 * 512 + so) = sv.y;
       *reinterpret_cast<uint32_t*>(sfa + 2 * 512 + so) = sv.z;
       *reinterpret_cast<uint32_t*>(sfa + 3 * 512 + so) = sv.w;
-      // (a') the partial atom's piece this thread copied, into the swizzled W tile
-      if (pt < rem * 8) {
-        const int rr = pt >> 3, c = pt & 7;
-        *reinterpret_cast<uint4*>(smem + kOffW + s * kWBytes + atoms * 1024 + rr * 128 + ((c ^ rr) << 4)) =
-            *reinterpret_cast<const uint4*>(rawp + 2048 + pt * 16);
-      }
-      // (b) x terms for elements 2pt, 2pt+1 of this stage (radix-4 digits, see the header)
-      const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + kb * kBK + 2 * pt);
-      const float R0 = bf16_lo(xv) * pre, R1 = bf16_hi(xv) * pre;
-      float mb = fmaxf(fabsf(R0), fabsf(R1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-      // S_b = 2^kexp with mb < 2^(kexp+1), 5 <= kexp <= 8: the floor keeps the last
-      // term's scale 2^(kexp-14) >= 2^-9, the smallest E4M3 value; a block that small
-      // (< 1/8 of max|x|) then carries a few bits less of its own, which is below
-      // 2^-18 of max|x|
-      int kexp = 5;
-      if (mb > 0.f) {
-        int ex;
-        frexpf(mb, &ex);  // mb < 2^ex
-        kexp = min(max(ex - 1, 5), 8);
-      }
-      const float invS = ldexpf(1.0f, -kexp);
-      float v0 = R0 * invS, v1 = R1 * invS;
-      uint8_t* batom = smem + kOffB + s * 1024;
-      uint8_t* sfb = smem + kOffSFB + s * kSFBytes;
-#pragma unroll
-      for (int t = 0; t < kTerms; ++t) {
-        // round to the nearest integer (ties to even): |v| <= 2, so adding 1.5 * 2^23 leaves
-        // exactly the rounded value's bits in the low mantissa; subtracting it back is exact
-        const float d0 = __fsub_rn(__fadd_rn(v0, 12582912.0f), 12582912.0f);
-        const float d1 = __fsub_rn(__fadd_rn(v1, 12582912.0f), 12582912.0f);
-        const uint32_t code = e2m1x2_rn(d0, d1);  // exact: digits in [-2, 2]
-        v0 = (v0 - d0) * 4.0f;
-        v1 = (v1 - d1) * 4.0f;
-        // byte pt of term row t, 128-byte swizzle within the 1 KB atom
-        batom[t * 128 + ((((pt >> 4) ^ t) & 7) << 4) + (pt & 15)] = (uint8_t)code;
-        if ((pt & 7) == 0) {
-          const int e = kexp - 2 * t;  // term scale 2^e, -9 <= e <= 8, as an E4M3 byte
-          const uint32_t sb = (e >= -6) ? (uint32_t)((e + 7) << 3) : (1u << (e + 9));
-          sfb[(b16 >> 2) * 512 + t * 16 + (b16 & 3)] = (uint8_t)sb;
-        }
-      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&full[s]);
+      mbar_arrive(&mfull[m]);
+      m += kGroups;
+      if (m >= kMeta) { m -= kMeta; ++mr; }
+      s += kGroups;
+      if (s >= nslots) { s -= nslots; ++wr; }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    // ---- epilogue (group 0, warps 2..5 = lane quadrants 2, 3, 0, 1): y = gs_w 2^e0 sum_t D[row, t]
+    // ---- epilogue (group 0, warps 2..5 = lane quadrants 2, 3, 0, 1): partial = 2^e0 sum_t D[row, t]
     if (grp == 0) {
-    mbar_wait(done, 0, err, failed);
-    tc_fence_after();
-    const int q = warp & 3;
-    float dsum[kTerms];
+      mbar_wait(done, 0, err, failed);
+      tc_fence_after();
+      const int q = warp & 3;
+      float dsum[kTerms];
 #pragma unroll
-    for (int t = 0; t < kTerms; ++t) dsum[t] = 0.f;
+      for (int t = 0; t < kTerms; ++t) dsum[t] = 0.f;
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      uint32_t d[16];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-          : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]), "=r"(d[7]),
-            "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]), "=r"(d[14]), "=r"(d[15])
-          : "r"(tmem + ((uint32_t)(32 * q) << 16) + 16 * a));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      for (int a = 0; a < 4; ++a) {
+        uint32_t d[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+            : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]), "=r"(d[7]),
+              "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]), "=r"(d[14]), "=r"(d[15])
+            : "r"(tmem + ((uint32_t)(32 * q) << 16) + 16 * a));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int t = 0; t < kTerms; ++t) dsum[t] += __uint_as_float(d[t]);
-    }
-    const int row = 32 * q + lane;
-    if (row < rows) {
+        for (int t = 0; t < kTerms; ++t) dsum[t] += __uint_as_float(d[t]);
+      }
       float acc = 0.f;
 #pragma unroll
       for (int t = kTerms - 1; t >= 0; --t) acc += dsum[t];
-      const float g = gs_w ? __ldg(gs_w) : 1.0f;
-      y[r0 + row] = (uint16_t)f32_to_bf16_rn(ldexpf(acc, e0) * g);
-    }
+      partial = finite ? ldexpf(acc, e0) : __int_as_float(0x7FC00000);
     }
   }
   tc_fence_before();
@@ -344,6 +365,25 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  const bool epi = warp >= 2 && warp < 6;  // group 0
+  const int row = 32 * (warp & 3) + lane;
+  if (split > 1) {
+    cluster_wait();  // every CTA of the cluster has started: rank 0's shared memory is live
+    if (epi && rank > 0 && row < rows) {
+      const uint32_t local = smem_u32(part + rank * kRows + row);
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(local));
+      asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(partial) : "memory");
+    }
+    cluster_arrive_release();
+    cluster_wait();
+  }
+  if (epi && rank == 0 && row < rows) {
+    float acc = partial;
+    for (int c = 1; c < split; ++c) acc += part[c * kRows + row];
+    const float g = gs_w ? __ldg(gs_w) : 1.0f;
+    y[r0 + row] = (uint16_t)f32_to_bf16_rn(acc * g);
   }
 }
 
@@ -360,41 +400,137 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// How many clusters of `split` CTAs of this kernel can be resident at once on
+// the device (cached per device and split; 0 if the query fails).
+int max_clusters(const DevInfo& d, int split) {
+  static std::mutex mu;
+  static int cache[64][kMaxSplit + 1];
+  static bool have[64][kMaxSplit + 1];
+  if (d.device < 0 || d.device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (have[d.device][split]) return cache[d.device][split];
+  int n = 0;
+  if (cudaFuncSetAttribute(qmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(split * std::max(1, d.sm_count / split)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, qmv_tc_kernel, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();  // the failed query leaves no sticky error behind
+    }
+  }
+  cache[d.device][split] = n;
+  have[d.device][split] = true;
+  return n;
+}
+
+struct TcPlan {
+  int split = 0;       // CTAs per cluster (K slices); 0 = no plan
+  int nblk = 0;        // row blocks (clusters)
+  int R = 0;           // rows per CTA at most (blocks own R or R - 1 rows)
+  int nslots = 0;      // weight ring slots
+  uint32_t wslot = 0;  // bytes of codes per slot (ceil(R/8) swizzle atoms)
+  uint32_t sslot = 0;  // bytes of linear scales per slot
+};
+
+// Choose the K split: per CTA the time is about (stages) x max(fixed issue cost
+// of a stage, the stage's bytes at an even share of HBM bandwidth); the split
+// with the smallest estimate wins (ties go to the smaller split).
+TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
+  TcPlan best;
+  if (K % kBK != 0 || N < 1 || d.sm_count < 1) return best;
+  const int64_t nkb = K / kBK;
+  const double stage_us = 0.2, sm_gbs = 43.0;
+  double best_cost = 0.0;
+  for (int split = 1; split <= kMaxSplit; ++split) {
+    if (nkb < split) break;
+    const int64_t nst = (nkb + split - 1) / split;
+    if (nst * kBK > kMaxKSlice) continue;
+    int64_t nblk = split == 1 ? d.sm_count : std::min<int64_t>(max_clusters(d, split), d.sm_count / split);
+    nblk = std::min<int64_t>(nblk, N);
+    if (nblk < 1) continue;
+    const int64_t R = (N + nblk - 1) / nblk;
+    if (R > kRows) continue;
+    const double cost = (double)nst * std::max(stage_us, (double)R * 144.0 / (sm_gbs * 1e3));
+    if (best.split == 0 || cost < best_cost) {
+      best_cost = cost;
+      best.split = split;
+      best.nblk = (int)nblk;
+      best.R = (int)R;
+    }
+  }
+  if (best.split == 0) return best;
+  best.wslot = (uint32_t)((best.R + 7) / 8) * 1024u;
+  best.sslot = ((uint32_t)best.R * 16u + 127u) / 128u * 128u;
+  best.nslots = (int)std::min<uint32_t>(kMaxSlots, kRingBytes / (best.wslot + best.sslot));
+  if (best.nslots < kMeta) best.split = 0;  // the slot relay needs nslots >= kMeta
+  return best;
+}
+
 }  // namespace
 
 // Whether the tensor-core GEMV handles this NVFP4 problem (else the mma.sync kernel does).
 bool qmv_tc_supported(const DevInfo& d, int64_t N, int64_t K) {
-  return K % kBK == 0 && K <= kMaxK && N >= 1 && (N + kRows - 1) / kRows <= d.sm_count &&
-         kSmemBytes <= d.smem_optin;
+  if (kSmemBytes > d.smem_optin || N > (int64_t)kRows * d.sm_count) return false;
+  return plan_qmv_tc(d, N, K).split > 0;
 }
 
 cudaError_t launch_qmv_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
-  CUtensorMap tm;
-  cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
-  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  cuuint32_t box[2] = {128, 8};
+  const TcPlan p = plan_qmv_tc(d, N, K);
+  if (p.split == 0) return cudaErrorInvalidValue;
   cuuint32_t estr[2] = {1, 1};
-  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(w), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  // W codes: [N, K/2] bytes, boxes of R rows x 128 bytes, 128-byte swizzle
+  CUtensorMap tmW;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {128, (cuuint32_t)p.R};
+    if (fn(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(w), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // W scales: [N, K/16] bytes (K/16 a multiple of 16), boxes of R rows x 16 bytes
+  CUtensorMap tmS;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 16)};
+    cuuint32_t box[2] = {16, (cuuint32_t)p.R};
+    if (fn(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(scales), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(qmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(N, std::max<int64_t>(d.sm_count, (N + kRows - 1) / kRows));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)(p.nblk * p.split));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)p.split;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel, tm, x, w, scales, gs_w, (int)N, (int)K, y, d.err);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel, tmW, tmS, x, gs_w, (int)N, (int)K, p.R, p.split, p.nslots,
+                            p.wslot, p.sslot, y, d.err);
 }
 
 }  // namespace fp4

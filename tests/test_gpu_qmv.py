@@ -68,6 +68,35 @@ def test_qmv_nvfp4_tensor_core_ragged_rows(B, N, K):
     assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs), f"nvfp4 {N}x{K}")
 
 
+@pytest.mark.parametrize("N,K", [(64, 65536), (1024, 5120), (5000, 34816)])
+def test_qmv_nvfp4_split_k_clusters(B, N, K):
+    """Shapes whose K is sliced across the CTAs of a cluster (partials summed
+    through distributed shared memory), including K beyond one CTA's x slice."""
+    q, s, b, gs, g = make_weights(2, N, K, seed=N + 1)
+    x = synth.activations_with_outliers(1, K, seed=11).view(-1)
+    qd, sd, bd, gsd = to_dev(2, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=2)
+    rows = np.unique(np.concatenate([np.arange(min(N, 8)), N - 1 - np.arange(min(N, 8)),
+                                     np.random.default_rng(N).integers(0, N, 120)]))
+    ref = oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs, rows=rows)
+    assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"nvfp4 {N}x{K}")
+
+
+@pytest.mark.parametrize("mode", [2, 1, 0])
+def test_qmv_nonfinite_activation_gives_nonfinite_rows(B, mode):
+    """An infinity in x makes every row of the exact product non-finite (inf, or
+    NaN where the weight is zero); the kernels return non-finite rows too."""
+    N, K = 160, 512
+    q, s, b, gs, g = make_weights(mode, N, K, seed=12)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    x = synth.bf16_normal((K,), 1.0, seed=13)
+    x[300] = float("inf")
+    ref = oracle.qmv(synth.to_u16(x), q, s, b, mode, g, gs)
+    assert not np.isfinite(ref).any()
+    y = B.qmv(x.cuda(), qd, sd, bd, gsd, mode=mode, group_size=g).float().cpu()
+    assert not torch.isfinite(y).any()
+
+
 def test_qmv_nvfp4_tiny_and_huge_activations(B):
     """x scaled far from 1 (the residual expansion's per-vector exponent)."""
     N, K = 256, 1024
