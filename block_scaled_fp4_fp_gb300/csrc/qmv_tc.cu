@@ -23,8 +23,9 @@
 // rank i of the cluster takes the i-th slice of the K stages (K = 256 each),
 // so a light problem runs fewer, fuller stages per CTA.  Each CTA sums its
 // slice into fp32 partials; ranks 1.. store theirs into rank 0's shared
-// memory (distributed shared memory), and rank 0 adds them in rank order --
-// the same order on every run -- and writes y.
+// memory with asynchronous remote stores (distributed shared memory) that a
+// barrier there counts by bytes, and rank 0 adds them in rank order -- the
+// same order on every run -- and writes y.
 //   warp 0: TMA producer -- per stage one box of R rows x 128 bytes of W
 //           (128-byte swizzle, so rows land as the 8-row atoms the MMA reads)
 //           and one box of R rows x 16 bytes of W's linear E4M3 scales, into
@@ -95,7 +96,7 @@ constexpr uint32_t kOffBar = kOffRed + kRedBytes;
 static_assert(kOffBar + kBarBytes + 1024 <= kSmemBytes, "shared memory layout overflows");
 // an MMA reads 16 KB of A from a slot's start: that stays inside the allocation
 static_assert(kRingBytes + 16384 <= kOffBar, "A-operand reads past the allocation");
-static_assert((2 * kMaxSlots + 2 * kMeta + 2) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
+static_assert((2 * kMaxSlots + 2 * kMeta + 3) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -109,8 +110,11 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(const void* p, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
@@ -136,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   uint64_t* mempty = mfull + kMeta;                               // stage operands consumed (MMA commit)
   uint64_t* done = mempty + kMeta;
   uint64_t* xbar = done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 1);
+  uint64_t* pbar = xbar + 1;  // rank 0: the other ranks' partials have landed (byte count)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pbar + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kPrep / 32 floats
   float* part = reinterpret_cast<float*>(smem + kOffRed);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + kOffX);
@@ -154,7 +159,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   const int nst = (int)(((int64_t)nkb * (rank + 1)) / split) - kb0;  // this CTA's stages (>= 1)
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (split > 1) cluster_arrive_relaxed();  // matched by the wait before the partials move
   if (threadIdx.x == 0) {
     for (int s = 0; s < nslots; ++s) {
       mbar_init(&wfull[s], 1);
@@ -166,8 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     }
     mbar_init(done, 1);
     mbar_init(xbar, 1);
-    fence_barrier_init();
+    mbar_init(pbar, 1);
+    fence_barrier_init();  // release of the barrier inits to the cluster
   }
+  // Ranks > 0 wait on this arrival before storing into rank 0's shared memory:
+  // rank 0 has started and its barriers are initialized.
+  __syncwarp();
+  if (split > 1) cluster_arrive_relaxed();
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
@@ -250,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     const int pa = threadIdx.x - 64;           // 0..kPrep-1
     const int grp = pa / kGroupThreads;        // prep group
     const int pt = pa % kGroupThreads;         // thread within the group
+    if (split > 1 && rank > 0) cluster_wait();  // (see the arrival after the barrier inits)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // this CTA's slice of x (bf16, nst * 512 bytes) -> shared memory in one bulk copy
     const uint32_t xbytes = (uint32_t)nst * (kBK * 2);
@@ -358,6 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
 #pragma unroll
       for (int t = kTerms - 1; t >= 0; --t) acc += dsum[t];
       partial = finite ? ldexpf(acc, e0) : __int_as_float(0x7FC00000);
+      const int row = 32 * q + lane;
+      if (rank > 0) {
+        // asynchronous store into rank 0's partials; its barrier counts the bytes
+        if (row < rows)
+          asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                       :: "r"(map_rank(part + rank * kRows + row, 0)), "r"(__float_as_uint(partial)),
+                          "r"(map_rank(pbar, 0)) : "memory");
+      } else {
+        if (split > 1) {
+          if (pa == 0) mbar_arrive_expect_tx(pbar, (uint32_t)(split - 1) * (uint32_t)rows * 4u);
+          mbar_wait(pbar, 0, err, failed);  // every other rank's partials have landed
+        }
+        if (row < rows) {
+          float acc_y = partial;
+          for (int c = 1; c < split; ++c) acc_y += part[c * kRows + row];
+          const float g = gs_w ? __ldg(gs_w) : 1.0f;
+          y[r0 + row] = (uint16_t)f32_to_bf16_rn(acc_y * g);
+        }
+      }
     }
   }
   tc_fence_before();
@@ -365,25 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
-  }
-  const bool epi = warp >= 2 && warp < 6;  // group 0
-  const int row = 32 * (warp & 3) + lane;
-  if (split > 1) {
-    cluster_wait();  // every CTA of the cluster has started: rank 0's shared memory is live
-    if (epi && rank > 0 && row < rows) {
-      const uint32_t local = smem_u32(part + rank * kRows + row);
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(local));
-      asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(partial) : "memory");
-    }
-    cluster_arrive_release();
-    cluster_wait();
-  }
-  if (epi && rank == 0 && row < rows) {
-    float acc = partial;
-    for (int c = 1; c < split; ++c) acc += part[c * kRows + row];
-    const float g = gs_w ? __ldg(gs_w) : 1.0f;
-    y[r0 + row] = (uint16_t)f32_to_bf16_rn(acc * g);
   }
 }
 
