@@ -63,10 +63,13 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()  # start timing once sampling runs, so the samples cover the timed region
+            while not self.lines and time.time() - t0 < 3.0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
@@ -281,9 +284,9 @@ def bench_gather(B, device, reps=10):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_layer_sample(mode_name="nvfp4"):
-    """Oracle qmv over layer 0's seven NVFP4 projections (weights generated on
-    the CPU and quantized by the oracle, untimed); returns (seconds, bytes)."""
+def oracle_layer_setup():
+    """Layer 0's seven NVFP4 projections for the oracle: weights generated on the
+    CPU and quantized by the oracle (untimed), and the two activation vectors."""
     import oracle
     mats = []
     for p, (name, N, K) in enumerate(synth.LAYER_PROJECTIONS):
@@ -292,6 +295,12 @@ def oracle_layer_sample(mode_name="nvfp4"):
         q, s = oracle.nvfp4_quantize(w, gs)
         mats.append((q, s, gs, K))
     xs = {K: synth.to_u16(synth.bf16_normal((K,), 1.0, seed=7 + K)) for K in (synth.HIDDEN, synth.MLP)}
+    return mats, xs
+
+
+def oracle_layer_time(mats, xs):
+    """Oracle qmv over the seven projections; returns (seconds, weight bytes)."""
+    import oracle
     nbytes = sum(q.nbytes + s.nbytes for q, s, _, _ in mats)
     t0 = time.perf_counter()
     for q, s, gs, K in mats:
@@ -341,9 +350,10 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
+    mats, xs = oracle_layer_setup()
     times, nbytes = [], 0
     for i in range(args.warmup + args.steps):
-        t, nbytes = oracle_layer_sample()
+        t, nbytes = oracle_layer_time(mats, xs)
         if i >= args.warmup:
             times.append(t)
     sec = statistics.median(times)
@@ -442,7 +452,7 @@ def run_ours(args):
     if rank == 0 and ws == 1 and not args.no_cpu:
         import oracle
         oracle.build()
-        sec, nb = oracle_layer_sample()
+        sec, nb = oracle_layer_time(*oracle_layer_setup())
         cpu = {"value": nb / sec / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": "layer 0 of 64 (q,k,v,o,gate,up,down), NVFP4 GEMV in the C oracle, fp64, weights "
                          "quantized by the oracle (untimed)"}
@@ -460,8 +470,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": committed_traffic("qmv.cu", "qmv_nvfp4_decode"),
-                         "kernel": "qmv_kernel<NVFP4>", "bytes_per_launch": per_launch_bytes,
+                         "traffic": committed_traffic("qmv_tc.cu", "qmv_tc_nvfp4_decode_layer"),
+                         "kernel": "qmv_tc_kernel (tcgen05 NVFP4 GEMV)", "bytes_per_launch": per_launch_bytes,
                          "peak_src": peaks["src"] + " hbm_gbs"},
             "cpu_baseline": cpu,
             "e2e": {"value": ws * stack.bytes / e2e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -478,7 +488,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=synth.LAYERS)

@@ -141,7 +141,14 @@ fp4_status fp4_dequantize(const uint32_t* wq, const void* scales, const fp4_bf16
  *   biases  affine: bf16[N, K/group]; NULL otherwise
  *   global_scale_w NVFP4 only: device fp32 gs of W, multiplied in the epilogue, or NULL
  *   y       bf16[N]
- * Requires K % 32 == 0 and K % group_size == 0. */
+ * Requires K % 32 == 0 and K % group_size == 0.
+ * Launch order: qmv uses programmatic dependent launch and may read w and its
+ * scales before the kernel launched just before it on the stream has finished;
+ * x, global_scale_w and y are touched only after that kernel completes.  No
+ * kernel of this library writes weights and releases its dependents early, so
+ * any sequence of calls through this header is ordered; a caller's own kernel
+ * that writes w and triggers its dependents early must not directly precede qmv.
+ * A NaN or infinity in x gives non-finite rows (NVFP4 tensor-core path: NaN). */
 fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
                const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, int bits,
                int group_size, fp4_bf16* y, cudaStream_t stream);
