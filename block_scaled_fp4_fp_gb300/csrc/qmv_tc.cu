@@ -26,11 +26,12 @@
 // memory with asynchronous remote stores (distributed shared memory) that a
 // barrier there counts by bytes, and rank 0 adds them in rank order -- the
 // same order on every run -- and writes y.
-//   warp 0: TMA producer -- per stage one box of R rows x 128 bytes of W
-//           (128-byte swizzle, so rows land as the 8-row atoms the MMA reads)
-//           and one box of R rows x 16 bytes of W's linear E4M3 scales, into
-//           a ring sized in bytes (a slot holds ceil(R/8) KB of codes; up to
-//           32 slots).  Issued before griddepcontrol.wait (programmatic
+//   warp 0: barrier setup (one barrier per lane), then the TMA producer: per
+//           stage one box of R rows x 128 bytes of W (128-byte swizzle, so
+//           rows land as the 8-row atoms the MMA reads) and one box of R rows
+//           x 16 bytes of W's linear E4M3 scales, into a ring sized in bytes
+//           (a slot holds ceil(R/8) KB of codes; about 128 KB, at least kMeta
+//           slots, in flight).  Issued before griddepcontrol.wait (programmatic
 //           dependent launch: W is not written by the kernel this one
 //           overlaps);
 //   warp 1: tensor memory allocation; one thread copies each stage's four
@@ -60,6 +61,7 @@ namespace {
 constexpr int kTerms = 9;           // x expansion terms (B rows 0..8)
 constexpr int kMeta = 6;            // ring of per-stage MMA operands built by the prep warps
 constexpr int kMaxSlots = 32;       // weight ring slots at most
+constexpr uint32_t kInflightBytes = 128u * 1024u;  // weight bytes a CTA keeps in flight at most
 constexpr int kBK = 256;            // codes per stage (128 bytes per row)
 constexpr int kRows = 128;          // rows per CTA at most (one M = 128 tile)
 constexpr int kMaxSplit = 8;        // CTAs per cluster at most (portable cluster size)
@@ -73,6 +75,7 @@ constexpr uint32_t kSfbCol = 64;         // D: four accumulators of 16 columns i
 constexpr uint32_t kSfaCol = 80;         // weight scales of operand slot m: kSfaCol + 16 m + 4 j
 static_assert(kSfaCol + kMeta * 16 <= kTmemCols, "scale columns exceed the allocation");
 static_assert(kMeta >= kGroups, "a group's stages must not share an operand slot");
+static_assert(kMaxSlots <= 32 && kMeta <= 32, "one barrier pair per lane of warp 0");
 // kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, N = 16, E4M3 scales, M = 128
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
@@ -159,18 +162,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   const int nst = (int)(((int64_t)nkb * (rank + 1)) / split) - kb0;  // this CTA's stages (>= 1)
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < nslots; ++s) {
-      mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], 1);
+  if (warp == 0) {  // one barrier (pair) per lane
+    if (lane < nslots) {
+      mbar_init(&wfull[lane], 1);
+      mbar_init(&wempty[lane], 1);
     }
-    for (int s = 0; s < kMeta; ++s) {
-      mbar_init(&mfull[s], kGroupThreads);
-      mbar_init(&mempty[s], 1);
+    if (lane < kMeta) {
+      mbar_init(&mfull[lane], kGroupThreads);
+      mbar_init(&mempty[lane], 1);
     }
-    mbar_init(done, 1);
-    mbar_init(xbar, 1);
-    mbar_init(pbar, 1);
+    if (lane == 0) {
+      mbar_init(done, 1);
+      mbar_init(xbar, 1);
+      mbar_init(pbar, 1);
+    }
     fence_barrier_init();  // release of the barrier inits to the cluster
   }
   // Ranks > 0 wait on this arrival before storing into rank 0's shared memory:
@@ -481,7 +486,10 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
   if (best.split == 0) return best;
   best.wslot = (uint32_t)((best.R + 7) / 8) * 1024u;
   best.sslot = ((uint32_t)best.R * 16u + 127u) / 128u * 128u;
-  best.nslots = (int)std::min<uint32_t>(kMaxSlots, kRingBytes / (best.wslot + best.sslot));
+  // deeper than about 128 KB only lengthens the queues in front of the first stages
+  const uint32_t slot = best.wslot + best.sslot;
+  best.nslots = (int)std::min<uint32_t>(kMaxSlots, kRingBytes / slot);
+  best.nslots = std::max<int>(std::min<int>(best.nslots, kMeta), std::min<int>(best.nslots, kInflightBytes / slot));
   if (best.nslots < kMeta) best.split = 0;  // the slot relay needs nslots >= kMeta
   return best;
 }
