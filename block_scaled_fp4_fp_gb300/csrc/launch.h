@@ -33,9 +33,9 @@ cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, c
                        const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode,
                        int group, uint16_t* y, cudaStream_t s);
 
-// qmv_tc.cu (NVFP4 on tcgen05; launch_qmv dispatches to it when supported)
-bool qmv_tc_supported(const DevInfo& d, int64_t N, int64_t K);
-cudaError_t launch_qmv_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
+// qmv_tc.cu (NVFP4 = mode 2 and MXFP4 = mode 1 on tcgen05; launch_qmv dispatches to it when supported)
+bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K);
+cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s);
 
 // qqmm.cu

@@ -59,25 +59,45 @@ namespace fp4 {
 namespace {
 
 constexpr int kTerms = 9;           // x expansion terms (B rows 0..8)
-constexpr int kMeta = 6;            // ring of per-stage MMA operands built by the prep warps
+constexpr int kMetaMax = 6;         // ring of per-stage MMA operands built by the prep warps, at most
 constexpr int kMaxSlots = 32;       // weight ring slots at most
 constexpr uint32_t kInflightBytes = 128u * 1024u;  // weight bytes a CTA keeps in flight at most
-constexpr int kBK = 256;            // codes per stage (128 bytes per row)
+constexpr int kChunk = 256;         // codes per TMA box (128 bytes per row)
 constexpr int kRows = 128;          // rows per CTA at most (one M = 128 tile)
 constexpr int kMaxSplit = 8;        // CTAs per cluster at most (portable cluster size)
 constexpr int kGroups = 4;          // prep groups; group g prepares local stages i % kGroups == g
 constexpr int kGroupThreads = 128;  // one group = 4 warps, two elements per thread per stage
 constexpr int kPrep = kGroups * kGroupThreads;
 constexpr int kThreads = 64 + kPrep;  // TMA warp, MMA warp, prep warps (group 0 also runs the epilogue)
-constexpr uint32_t kSFABytes = 4 * 512;  // four 128x4 weight-scale tiles (one per MMA k-step)
+constexpr uint32_t kSFABytes = 4 * 512;  // four 128x4 weight-scale tiles per stage (16 scale bytes per row)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kSfbCol = 64;         // D: four accumulators of 16 columns in [0, 64); term scales
 constexpr uint32_t kSfaCol = 80;         // weight scales of operand slot m: kSfaCol + 16 m + 4 j
-static_assert(kSfaCol + kMeta * 16 <= kTmemCols, "scale columns exceed the allocation");
-static_assert(kMeta >= kGroups, "a group's stages must not share an operand slot");
-static_assert(kMaxSlots <= 32 && kMeta <= 32, "one barrier pair per lane of warp 0");
-// kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, N = 16, E4M3 scales, M = 128
+static_assert(kSfaCol + kMetaMax * 16 <= kTmemCols, "scale columns exceed the allocation");
+static_assert(kMaxSlots <= 32 && kMetaMax <= 32, "one barrier pair per lane of warp 0");
+// kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, N = 16, M = 128; bit 23 selects E8M0 scales
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+
+// Per format: NVFP4 (E4M3 scales per 16 elements) takes one 256-element chunk
+// per stage, MXFP4 (E8M0 per 32) two, so a stage always carries 16 scale bytes
+// per row -- four 128x4 tiles -- and the scale path is the same for both.
+template <int MODE> struct Fmt;
+template <> struct Fmt<2> {
+  static constexpr int kCh = 1;
+  static constexpr int kMeta = 6;  // operand ring depth
+  static constexpr uint32_t kIdesc = fp4::kIdesc;
+  // E4M3 byte of the term weight 2^(7-2t) (exact: 2^7 ... 2^-9)
+  __host__ __device__ static constexpr uint32_t term_scale(int t) {
+    return (7 - 2 * t >= -6) ? (uint32_t)((7 - 2 * t + 7) << 3) : (1u << (7 - 2 * t + 9));
+  }
+};
+template <> struct Fmt<1> {
+  static constexpr int kCh = 2;
+  static constexpr int kMeta = 4;  // stages are twice as large: a shallower ring keeps kMeta weight slots
+  static constexpr uint32_t kIdesc = fp4::kIdesc | (1u << 23);
+  // E8M0 byte of 2^(7-2t)
+  __host__ __device__ static constexpr uint32_t term_scale(int t) { return (uint32_t)(127 + 7 - 2 * t); }
+};
 
 // Shared memory (from a 1024-aligned base): [weight ring | term atoms | term-8
 // atoms | weight-scale tiles | term-scale tile | x slice | partials | barriers].
@@ -86,20 +106,24 @@ constexpr int kMaxKSlice = 17408;  // elements of x per CTA
 constexpr uint32_t kSmemBytes = 227u * 1024u;
 constexpr uint32_t kBarBytes = 1024;
 constexpr uint32_t kRedBytes = kMaxSplit * kRows * 4;
-constexpr uint32_t kFixedBytes = 2 * kMeta * 1024 + kMeta * kSFABytes + 512 + kMaxKSlice * 2 + kRedBytes +
-                                 kBarBytes + 1024;
-constexpr uint32_t kRingBytes = (kSmemBytes - kFixedBytes) / 1024u * 1024u;
-constexpr uint32_t kOffB = kRingBytes;                    // terms 0..7 of slot m: one 1 KB atom
-constexpr uint32_t kOffB8 = kOffB + kMeta * 1024;         // term 8 (+ 7 unused rows) of slot m
-constexpr uint32_t kOffSFA = kOffB8 + kMeta * 1024;
-constexpr uint32_t kOffSFB = kOffSFA + kMeta * kSFABytes;
-constexpr uint32_t kOffX = kOffSFB + 512;                 // x slice (bf16)
-constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;      // [split][128] fp32 partials (rank 0)
-constexpr uint32_t kOffBar = kOffRed + kRedBytes;
-static_assert(kOffBar + kBarBytes + 1024 <= kSmemBytes, "shared memory layout overflows");
-// an MMA reads 16 KB of A from a slot's start: that stays inside the allocation
-static_assert(kRingBytes + 16384 <= kOffBar, "A-operand reads past the allocation");
-static_assert((2 * kMaxSlots + 2 * kMeta + 3) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
+template <int CH, int kMeta> struct Lay {
+  static_assert(kMeta >= kGroups && kMeta <= kMetaMax, "a group's stages must not share an operand slot");
+  static constexpr uint32_t kAtoms = kMeta * CH;  // term atoms in the operand ring (CH per slot)
+  static constexpr uint32_t kFixed = 2 * kAtoms * 1024 + kMeta * kSFABytes + 512 + kMaxKSlice * 2 + kRedBytes +
+                                     kBarBytes + 1024;
+  static constexpr uint32_t kRing = (kSmemBytes - kFixed) / 1024u * 1024u;
+  static constexpr uint32_t kOffB = kRing;                   // terms 0..7: atom CH m + h of slot m
+  static constexpr uint32_t kOffB8 = kOffB + kAtoms * 1024;  // term 8 (+ 7 unused rows), same index
+  static constexpr uint32_t kOffSFA = kOffB8 + kAtoms * 1024;
+  static constexpr uint32_t kOffSFB = kOffSFA + kMeta * kSFABytes;
+  static constexpr uint32_t kOffX = kOffSFB + 512;             // x slice (bf16)
+  static constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;  // [split][128] fp32 partials (rank 0)
+  static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
+  static_assert(kOffBar + kBarBytes + 1024 <= kSmemBytes, "shared memory layout overflows");
+  // an MMA reads 16 KB of A from a code chunk's start: that stays inside the allocation
+  static_assert(kRing + 16384 <= kOffBar, "A-operand reads past the allocation");
+};
+static_assert((2 * kMaxSlots + 2 * kMetaMax + 3) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -121,11 +145,7 @@ __device__ __forceinline__ uint32_t map_rank(const void* p, int rank) {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-// E4M3 byte of 2^e, -9 <= e <= 8
-__host__ __device__ constexpr uint32_t e4m3_pow2(int e) {
-  return (e >= -6) ? (uint32_t)((e + 7) << 3) : (1u << (e + 9));
-}
-
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmS,
                                                               const uint16_t* __restrict__ x,
@@ -133,22 +153,28 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
                                                               int R, int split, int nslots, uint32_t wslot,
                                                               uint32_t sslot, uint16_t* __restrict__ y,
                                                               unsigned* __restrict__ err) {
+  using F = Fmt<MODE>;
+  using L = Lay<F::kCh, F::kMeta>;
+  constexpr int kCh = F::kCh;
+  constexpr int kMeta = F::kMeta;
+  constexpr int kBK = kChunk * kCh;  // codes per stage
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + kOffBar);  // weight slot landed (TMA bytes)
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // weight slot landed (TMA bytes)
   uint64_t* wempty = wfull + kMaxSlots;                           // weight slot consumed (relayed)
   uint64_t* mfull = wempty + kMaxSlots;                           // stage operands built (prep group)
-  uint64_t* mempty = mfull + kMeta;                               // stage operands consumed (MMA commit)
-  uint64_t* done = mempty + kMeta;
+  uint64_t* mempty = mfull + kMetaMax;                            // stage operands consumed (MMA commit)
+  uint64_t* done = mempty + kMetaMax;
   uint64_t* xbar = done + 1;
   uint64_t* pbar = xbar + 1;  // rank 0: the other ranks' partials have landed (byte count)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pbar + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kPrep / 32 floats
-  float* part = reinterpret_cast<float*>(smem + kOffRed);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + kOffX);
+  float* part = reinterpret_cast<float*>(smem + L::kOffRed);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L::kOffX);
   const uint32_t offS = (uint32_t)nslots * wslot;  // linear-scale slots follow the code slots
+  const uint32_t wchunk = wslot / kCh;              // one 256-element chunk of a code slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)(blockIdx.x % (unsigned)split);  // rank within the cluster (clusters are consecutive)
@@ -192,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   // rows 9..31 are zero, so B rows 9..15 add nothing.
   if (threadIdx.x < 128) {
     const int row = threadIdx.x >> 2, word = threadIdx.x & 3;
-    const uint32_t v = (row < kTerms && word == 0) ? e4m3_pow2(7 - 2 * row) * 0x01010101u : 0u;
-    reinterpret_cast<uint32_t*>(smem + kOffSFB)[threadIdx.x] = v;
+    const uint32_t v = (row < kTerms && word == 0) ? F::term_scale(row) * 0x01010101u : 0u;
+    reinterpret_cast<uint32_t*>(smem + L::kOffSFB)[threadIdx.x] = v;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
@@ -208,12 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     if (elect_one_sync()) {
       prefetch_tmap(&tmW);
       prefetch_tmap(&tmS);
-      const uint32_t tx = (uint32_t)R * (128u + 16u);  // out-of-range rows are zero-filled and counted
+      // out-of-range rows are zero-filled and counted
+      const uint32_t tx = (uint32_t)R * (128u * kCh + 16u);
       int s = 0, round = 0;
       for (int i = 0; i < nst; ++i) {
         if (round > 0) mbar_wait(&wempty[s], (round - 1) & 1, err, failed);
         mbar_arrive_expect_tx(&wfull[s], tx);
-        tma_load_2d(smem + s * wslot, &tmW, &wfull[s], (kb0 + i) * 128, r0);
+#pragma unroll
+        for (int h = 0; h < kCh; ++h)
+          tma_load_2d(smem + s * wslot + h * wchunk, &tmW, &wfull[s], ((kb0 + i) * kCh + h) * 128, r0);
         tma_load_2d(smem + offS + s * sslot, &tmS, &wfull[s], (kb0 + i) * 16, r0);
         if (++s == nslots) { s = 0; ++round; }
       }
@@ -225,31 +254,45 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     // ------------------------------------------------------- MMA issuer
     if (elect_one_sync()) {
       asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
-                   :: "r"(tmem + kSfbCol), "l"(desc_sf(base + kOffSFB)) : "memory");
+                   :: "r"(tmem + kSfbCol), "l"(desc_sf(base + L::kOffSFB)) : "memory");
       const uint32_t sfb_t = tmem + kSfbCol;
       int m = 0, mround = 0, s = 0;
       for (int i = 0; i < nst; ++i) {
         mbar_wait(&mfull[m], mround & 1, err, failed);  // the group also saw the weights land
         tc_fence_after();
         const uint32_t sfa_t = tmem + kSfaCol + 16 * m;
-        const uint32_t sfa_s = base + kOffSFA + m * kSFABytes;
+        const uint32_t sfa_s = base + L::kOffSFA + m * kSFABytes;
 #pragma unroll
         for (int j = 0; j < 4; ++j)  // scale tiles start on 4-column boundaries of tensor memory
           asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
                        :: "r"(sfa_t + 4 * j), "l"(desc_sf(sfa_s + 512 * j)) : "memory");
-        const uint64_t adesc = desc_sw128(base + s * wslot, 1024);
-        // B rows 0..7: the slot's term atom; rows 8..15: its term-8 atom, kMeta KB further
-        const uint64_t bdesc = desc_sw128(base + kOffB + m * 1024, kMeta * 1024);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // k-step j accumulates into its own 16-column tile, so the four MMAs of a
-          // stage do not wait on each other; the epilogue adds the four tiles
-          const uint32_t acc = (i > 0) ? 1u : 0u;
-          asm volatile(
-              "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-              :: "r"(tmem + 16 * j), "l"(adesc + (uint64_t)(2 * j)), "l"(bdesc + (uint64_t)(2 * j)), "r"(kIdesc),
-                 "r"(sfa_t + 4 * j), "r"(sfb_t), "r"(acc) : "memory");
+        for (int j = 0; j < 4 * kCh; ++j) {
+          // k-step j (K = 64): chunk h = j / 4, 32 bytes further per k-step along the swizzled rows
+          const int h = j >> 2, jj = j & 3;
+          const uint64_t adesc = desc_sw128(base + s * wslot + h * wchunk, 1024) + (uint64_t)(2 * jj);
+          // B rows 0..7: the chunk's term atom; rows 8..15: its term-8 atom, L::kAtoms KB further
+          const uint64_t bdesc = desc_sw128(base + L::kOffB + (m * kCh + h) * 1024, L::kAtoms * 1024) + (uint64_t)(2 * jj);
+          // the 16 scale bytes of a row cover the stage: NVFP4 k-step j uses tile j; MXFP4
+          // k-step j uses half (j & 1) of tile j / 2 (scale-factor id 0 or 2)
+          const uint32_t tile = (kCh == 1) ? (uint32_t)j : (uint32_t)(j >> 1);
+          const uint32_t sf_id = (kCh == 1) ? 0u : (uint32_t)((j & 1) * 2);
+          const uint32_t idesc = F::kIdesc | (sf_id << 29) | (sf_id << 4);
+          // k-step j accumulates into tile j % 4 of D, so consecutive MMAs of a stage do
+          // not wait on each other; the epilogue adds the four tiles
+          const uint32_t acc = (i > 0 || j >= 4) ? 1u : 0u;
+          if (kCh == 1)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                :: "r"(tmem + 16 * (j & 3)), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_t + 4 * tile), "r"(sfb_t),
+                   "r"(acc) : "memory");
+          else
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+                :: "r"(tmem + 16 * (j & 3)), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_t + 4 * tile), "r"(sfb_t),
+                   "r"(acc) : "memory");
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(smem_u32(&mempty[m])) : "memory");
@@ -312,31 +355,34 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
           mbar_arrive(&wempty[sj]);
         }
       }
-      // (a) x terms for elements 2pt, 2pt+1 of this stage (radix-4 digits, see the header)
-      const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + i * kBK + 2 * pt);
-      float r0v = bf16_lo(xv) * pre, r1v = bf16_hi(xv) * pre;
-      uint8_t* batom = smem + kOffB + m * 1024;
+      // (a) x terms for elements 256 h + 2pt, + 1 of this stage (radix-4 digits, see the header)
 #pragma unroll
-      for (int t = 0; t < kTerms; ++t) {
-        // d = rint(r / 2^(7-2t)): one fused multiply-add onto 1.5 * 2^23 rounds the
-        // exact product to an integer; subtracting the constant back is exact
-        const float inv = __int_as_float((127 - (7 - 2 * t)) << 23);  // 2^-(7-2t)
-        const float w = __int_as_float((127 + (7 - 2 * t)) << 23);    // 2^(7-2t)
-        const float d0 = __fsub_rn(__fmaf_rn(r0v, inv, 12582912.0f), 12582912.0f);
-        const float d1 = __fsub_rn(__fmaf_rn(r1v, inv, 12582912.0f), 12582912.0f);
-        r0v = __fmaf_rn(-w, d0, r0v);  // exact: |result| <= w / 2
-        r1v = __fmaf_rn(-w, d1, r1v);
-        const uint8_t code = (uint8_t)e2m1x2_rn(d0, d1);  // exact: digits in [-2, 2]
-        // byte pt of term row t (row 0 of the term-8 atom for t = 8), 128-byte swizzle
-        if (t < 8) batom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
-        else batom[kMeta * 1024 + hi4 + lo] = code;
+      for (int h = 0; h < kCh; ++h) {
+        const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + i * kBK + h * kChunk + 2 * pt);
+        float r0v = bf16_lo(xv) * pre, r1v = bf16_hi(xv) * pre;
+        uint8_t* batom = smem + L::kOffB + (m * kCh + h) * 1024;
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t) {
+          // d = rint(r / 2^(7-2t)): one fused multiply-add onto 1.5 * 2^23 rounds the
+          // exact product to an integer; subtracting the constant back is exact
+          const float inv = __int_as_float((127 - (7 - 2 * t)) << 23);  // 2^-(7-2t)
+          const float w = __int_as_float((127 + (7 - 2 * t)) << 23);    // 2^(7-2t)
+          const float d0 = __fsub_rn(__fmaf_rn(r0v, inv, 12582912.0f), 12582912.0f);
+          const float d1 = __fsub_rn(__fmaf_rn(r1v, inv, 12582912.0f), 12582912.0f);
+          r0v = __fmaf_rn(-w, d0, r0v);  // exact: |result| <= w / 2
+          r1v = __fmaf_rn(-w, d1, r1v);
+          const uint8_t code = (uint8_t)e2m1x2_rn(d0, d1);  // exact: digits in [-2, 2]
+          // byte pt of term row t (row 0 of the term-8 atom for t = 8), 128-byte swizzle
+          if (t < 8) batom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
+          else batom[L::kAtoms * 1024 + hi4 + lo] = code;
+        }
       }
       // (b) weight scales of row pt, once the stage has landed: 16 E4M3 bytes ->
       // word j of tile j, 16-byte row (pt % 32), slot pt / 32; rows >= rows get 0
       mbar_wait(&wfull[s], wr & 1, err, failed);
       uint4 sv = make_uint4(0, 0, 0, 0);
       if (pt < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + pt * 16);
-      uint8_t* sfa = smem + kOffSFA + m * kSFABytes;
+      uint8_t* sfa = smem + L::kOffSFA + m * kSFABytes;
       const uint32_t so = (uint32_t)((pt & 31) * 16 + (pt >> 5) * 4);
       *reinterpret_cast<uint32_t*>(sfa + 0 * 512 + so) = sv.x;
       *reinterpret_cast<uint32_t*>(sfa + 1 * 512 + so) = sv.y;
@@ -416,7 +462,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // How many clusters of `split` CTAs of this kernel can be resident at once on
-// the device (cached per device and split; 0 if the query fails).
+// the device (cached per device, format and split; 0 if the query fails).
+template <int MODE>
 int max_clusters(const DevInfo& d, int split) {
   static std::mutex mu;
   static int cache[64][kMaxSplit + 1];
@@ -425,7 +472,7 @@ int max_clusters(const DevInfo& d, int split) {
   std::lock_guard<std::mutex> lock(mu);
   if (have[d.device][split]) return cache[d.device][split];
   int n = 0;
-  if (cudaFuncSetAttribute(qmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
+  if (cudaFuncSetAttribute(qmv_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
       cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(split * std::max(1, d.sm_count / split)));
@@ -438,7 +485,7 @@ int max_clusters(const DevInfo& d, int split) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, qmv_tc_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, qmv_tc_kernel<MODE>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();  // the failed query leaves no sticky error behind
     }
@@ -453,29 +500,33 @@ struct TcPlan {
   int nblk = 0;        // row blocks (clusters)
   int R = 0;           // rows per CTA at most (blocks own R or R - 1 rows)
   int nslots = 0;      // weight ring slots
-  uint32_t wslot = 0;  // bytes of codes per slot (ceil(R/8) swizzle atoms)
+  uint32_t wslot = 0;  // bytes of codes per slot (kCh chunks of ceil(R/8) swizzle atoms)
   uint32_t sslot = 0;  // bytes of linear scales per slot
 };
 
 // Choose the K split: per CTA the time is about (stages) x max(fixed issue cost
 // of a stage, the stage's bytes at an even share of HBM bandwidth); the split
 // with the smallest estimate wins (ties go to the smaller split).
+template <int MODE>
 TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
+  constexpr int kCh = Fmt<MODE>::kCh;
+  constexpr int kMeta = Fmt<MODE>::kMeta;
+  constexpr int kBK = kChunk * kCh;
   TcPlan best;
   if (K % kBK != 0 || N < 1 || d.sm_count < 1) return best;
   const int64_t nkb = K / kBK;
-  const double stage_us = 0.2, sm_gbs = 43.0;
+  const double stage_us = 0.2 * kCh, sm_gbs = 43.0;
   double best_cost = 0.0;
   for (int split = 1; split <= kMaxSplit; ++split) {
     if (nkb < split) break;
     const int64_t nst = (nkb + split - 1) / split;
     if (nst * kBK > kMaxKSlice) continue;
-    int64_t nblk = split == 1 ? d.sm_count : std::min<int64_t>(max_clusters(d, split), d.sm_count / split);
+    int64_t nblk = split == 1 ? d.sm_count : std::min<int64_t>(max_clusters<MODE>(d, split), d.sm_count / split);
     nblk = std::min<int64_t>(nblk, N);
     if (nblk < 1) continue;
     const int64_t R = (N + nblk - 1) / nblk;
     if (R > kRows) continue;
-    const double cost = (double)nst * std::max(stage_us, (double)R * 144.0 / (sm_gbs * 1e3));
+    const double cost = (double)nst * std::max(stage_us, (double)R * (128.0 * kCh + 16.0) / (sm_gbs * 1e3));
     if (best.split == 0 || cost < best_cost) {
       best_cost = cost;
       best.split = split;
@@ -484,30 +535,24 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
     }
   }
   if (best.split == 0) return best;
-  best.wslot = (uint32_t)((best.R + 7) / 8) * 1024u;
+  best.wslot = (uint32_t)kCh * (uint32_t)((best.R + 7) / 8) * 1024u;
   best.sslot = ((uint32_t)best.R * 16u + 127u) / 128u * 128u;
   // deeper than about 128 KB only lengthens the queues in front of the first stages
   const uint32_t slot = best.wslot + best.sslot;
-  best.nslots = (int)std::min<uint32_t>(kMaxSlots, kRingBytes / slot);
+  best.nslots = (int)std::min<uint32_t>(kMaxSlots, Lay<kCh, kMeta>::kRing / slot);
   best.nslots = std::max<int>(std::min<int>(best.nslots, kMeta), std::min<int>(best.nslots, kInflightBytes / slot));
   if (best.nslots < kMeta) best.split = 0;  // the slot relay needs nslots >= kMeta
   return best;
 }
 
-}  // namespace
-
-// Whether the tensor-core GEMV handles this NVFP4 problem (else the mma.sync kernel does).
-bool qmv_tc_supported(const DevInfo& d, int64_t N, int64_t K) {
-  if (kSmemBytes > d.smem_optin || N > (int64_t)kRows * d.sm_count) return false;
-  return plan_qmv_tc(d, N, K).split > 0;
-}
-
-cudaError_t launch_qmv_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
+template <int MODE>
+cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
+                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
-  const TcPlan p = plan_qmv_tc(d, N, K);
+  const TcPlan p = plan_qmv_tc<MODE>(d, N, K);
   if (p.split == 0) return cudaErrorInvalidValue;
+  const int group = MODE == 2 ? 16 : 32;
   cuuint32_t estr[2] = {1, 1};
   // W codes: [N, K/2] bytes, boxes of R rows x 128 bytes, 128-byte swizzle
   CUtensorMap tmW;
@@ -520,18 +565,19 @@ cudaError_t launch_qmv_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // W scales: [N, K/16] bytes (K/16 a multiple of 16), boxes of R rows x 16 bytes
+  // W scales: [N, K/group] bytes (a multiple of 16 per row), boxes of R rows x 16 bytes
   CUtensorMap tmS;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)(K / 16), (cuuint64_t)N};
-    cuuint64_t strides[1] = {(cuuint64_t)(K / 16)};
+    cuuint64_t dims[2] = {(cuuint64_t)(K / group), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / group)};
     cuuint32_t box[2] = {16, (cuuint32_t)p.R};
     if (fn(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(scales), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(qmv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(qmv_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.nblk * p.split));
@@ -547,8 +593,26 @@ cudaError_t launch_qmv_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel, tmW, tmS, x, gs_w, (int)N, (int)K, p.R, p.split, p.nslots,
-                            p.wslot, p.sslot, y, d.err);
+  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel<MODE>, tmW, tmS, x, gs_w, (int)N, (int)K, p.R, p.split,
+                            p.nslots, p.wslot, p.sslot, y, d.err);
+}
+
+}  // namespace
+
+// Whether the tensor-core GEMV handles this NVFP4 (mode 2) or MXFP4 (mode 1)
+// problem (else the mma.sync kernel does).
+bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K) {
+  if (kSmemBytes > d.smem_optin || N > (int64_t)kRows * d.sm_count) return false;
+  if (mode == 2) return plan_qmv_tc<2>(d, N, K).split > 0;
+  if (mode == 1) return plan_qmv_tc<1>(d, N, K).split > 0;
+  return false;
+}
+
+cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
+                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
+  if (mode == 2) return launch_mode_tc<2>(d, x, w, scales, gs_w, N, K, y, s);
+  if (mode == 1) return launch_mode_tc<1>(d, x, w, scales, gs_w, N, K, y, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fp4

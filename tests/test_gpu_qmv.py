@@ -57,29 +57,32 @@ def test_qmv_small(B, mode, N, K):
     assert_close_to_oracle(y, ref, f"qmv mode {mode} {N}x{K}")
 
 
-@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (9, 256), (129, 768), (1000, 2048), (20000, 512)])
-def test_qmv_nvfp4_tensor_core_ragged_rows(B, N, K):
+@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (9, 256), (129, 768), (1000, 2048), (20000, 512),
+                                 (333, 1536)])
+def test_qmv_fp4_tensor_core_ragged_rows(B, mode, N, K):
     """Row counts that leave partial 8-row atoms per CTA, and N above 128 rows
-    per SM (which takes the mma.sync kernel)."""
-    q, s, b, gs, g = make_weights(2, N, K, seed=N)
+    per SM or K off the stage size (which take the mma.sync kernel)."""
+    q, s, b, gs, g = make_weights(mode, N, K, seed=N)
     x = synth.activations_with_outliers(1, K, seed=3).view(-1)
-    qd, sd, bd, gsd = to_dev(2, q, s, b, gs)
-    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=2)
-    assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs), f"nvfp4 {N}x{K}")
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
+    assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, mode, g, gs), f"mode {mode} {N}x{K}")
 
 
+@pytest.mark.parametrize("mode", [2, 1])
 @pytest.mark.parametrize("N,K", [(64, 65536), (1024, 5120), (5000, 34816)])
-def test_qmv_nvfp4_split_k_clusters(B, N, K):
+def test_qmv_fp4_split_k_clusters(B, mode, N, K):
     """Shapes whose K is sliced across the CTAs of a cluster (partials summed
     through distributed shared memory), including K beyond one CTA's x slice."""
-    q, s, b, gs, g = make_weights(2, N, K, seed=N + 1)
+    q, s, b, gs, g = make_weights(mode, N, K, seed=N + 1)
     x = synth.activations_with_outliers(1, K, seed=11).view(-1)
-    qd, sd, bd, gsd = to_dev(2, q, s, b, gs)
-    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=2)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
     rows = np.unique(np.concatenate([np.arange(min(N, 8)), N - 1 - np.arange(min(N, 8)),
                                      np.random.default_rng(N).integers(0, N, 120)]))
-    ref = oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs, rows=rows)
-    assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"nvfp4 {N}x{K}")
+    ref = oracle.qmv(synth.to_u16(x), q, s, None, mode, g, gs, rows=rows)
+    assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"mode {mode} {N}x{K}")
 
 
 @pytest.mark.parametrize("mode", [2, 1, 0])
@@ -97,15 +100,16 @@ def test_qmv_nonfinite_activation_gives_nonfinite_rows(B, mode):
     assert not torch.isfinite(y).any()
 
 
-def test_qmv_nvfp4_tiny_and_huge_activations(B):
-    """x scaled far from 1 (the residual expansion's per-vector exponent)."""
+@pytest.mark.parametrize("mode", [2, 1])
+def test_qmv_fp4_tiny_and_huge_activations(B, mode):
+    """x scaled far from 1 (the residual expansion's per-slice exponent)."""
     N, K = 256, 1024
-    q, s, b, gs, g = make_weights(2, N, K, seed=4)
-    qd, sd, bd, gsd = to_dev(2, q, s, b, gs)
+    q, s, b, gs, g = make_weights(mode, N, K, seed=4)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
     for scale in (2.0 ** -60, 2.0 ** -20, 1.0, 2.0 ** 30, 2.0 ** 100):
         x = (synth.bf16_normal((K,), 1.0, seed=5).float() * scale).to(torch.bfloat16)
-        y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=2)
-        assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs), f"scale {scale}")
+        y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
+        assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, mode, g, gs), f"scale {scale}")
 
 
 @pytest.mark.parametrize("group", [32, 128])
@@ -119,11 +123,11 @@ def test_qmv_affine_other_groups(B, group):
 
 @pytest.mark.parametrize("mode", [2, 1, 0])
 def test_qmv_one_hot_returns_dequantized_column(B, mode):
-    N, K = 64, 256
+    N, K = 64, 512  # K = 512 runs both FP4 formats on the tensor-core path
     q, s, b, gs, g = make_weights(mode, N, K, seed=1)
     qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
     deq = oracle.dequantize_f64(q, s, b, mode, g, gs)
-    for k in [0, 1, 8, 15, 31, 32, 255]:
+    for k in [0, 1, 8, 15, 31, 32, 255, 300, 511]:
         x = torch.zeros(K, dtype=torch.bfloat16)
         x[k] = 1.0
         y = B.qmv(x.cuda(), qd, sd, bd, gsd, mode=mode, group_size=g).float().cpu().double().numpy()
