@@ -69,22 +69,22 @@ constexpr int kGroups = 4;          // prep groups; group g prepares local stage
 constexpr int kGroupThreads = 128;  // one group = 4 warps, two elements per thread per stage
 constexpr int kPrep = kGroups * kGroupThreads;
 constexpr int kThreads = 64 + kPrep;  // TMA warp, MMA warp, prep warps (group 0 also runs the epilogue)
-constexpr uint32_t kSFABytes = 4 * 512;  // four 128x4 weight-scale tiles per stage (16 scale bytes per row)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kSfbCol = 64;         // D: four accumulators of 16 columns in [0, 64); term scales
 constexpr uint32_t kSfaCol = 80;         // weight scales of operand slot m: kSfaCol + 16 m + 4 j
-static_assert(kSfaCol + kMetaMax * 16 <= kTmemCols, "scale columns exceed the allocation");
 static_assert(kMaxSlots <= 32 && kMetaMax <= 32, "one barrier pair per lane of warp 0");
 // kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, N = 16, M = 128; bit 23 selects E8M0 scales
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
-// Per format: NVFP4 (E4M3 scales per 16 elements) takes one 256-element chunk
-// per stage, MXFP4 (E8M0 per 32) two, so a stage always carries 16 scale bytes
-// per row -- four 128x4 tiles -- and the scale path is the same for both.
+// Per format: a stage is kCh chunks of 256 elements; a row carries kSB scale
+// bytes per stage, which tcgen05.cp moves as kSB / 4 tiles of 128x4 scales.
+// NVFP4 (E4M3 per 16): k-step j (K = 64) reads tile j; MXFP4 (E8M0 per 32):
+// half j & 1 of tile j / 2, through the scale-factor id.
 template <int MODE> struct Fmt;
 template <> struct Fmt<2> {
   static constexpr int kCh = 1;
-  static constexpr int kMeta = 6;  // operand ring depth
+  static constexpr int kMeta = 6;   // operand ring depth
+  static constexpr int kGroup = 16;
   static constexpr uint32_t kIdesc = fp4::kIdesc;
   // E4M3 byte of the term weight 2^(7-2t) (exact: 2^7 ... 2^-9)
   __host__ __device__ static constexpr uint32_t term_scale(int t) {
@@ -93,10 +93,22 @@ template <> struct Fmt<2> {
 };
 template <> struct Fmt<1> {
   static constexpr int kCh = 2;
-  static constexpr int kMeta = 4;  // stages are twice as large: a shallower ring keeps kMeta weight slots
+  static constexpr int kMeta = 4;   // stages are twice as large: a shallower ring keeps kMeta weight slots
+  static constexpr int kGroup = 32;
   static constexpr uint32_t kIdesc = fp4::kIdesc | (1u << 23);
   // E8M0 byte of 2^(7-2t)
   __host__ __device__ static constexpr uint32_t term_scale(int t) { return (uint32_t)(127 + 7 - 2 * t); }
+};
+template <int MODE> struct Geo {
+  static constexpr int kCh = Fmt<MODE>::kCh;
+  static constexpr int kMeta = Fmt<MODE>::kMeta;
+  static constexpr int kBK = 256 * kCh;                          // codes per stage
+  static constexpr int kSB = kBK / Fmt<MODE>::kGroup;             // scale bytes per row per stage
+  static constexpr int kTiles = kSB / 4;                         // 128x4 scale tiles per stage
+  static constexpr int kSpk = 64 / Fmt<MODE>::kGroup;             // scales per row per k-step
+  static constexpr uint32_t kSFABytes = (uint32_t)kTiles * 512;  // weight-scale tiles of one operand slot
+  static_assert(kSB % 16 == 0, "scale boxes are whole 16-byte rows");
+  static_assert(kSfaCol + kMeta * kTiles * 4 <= kTmemCols, "scale columns exceed the allocation");
 };
 
 // Shared memory (from a 1024-aligned base): [weight ring | term atoms | term-8
@@ -106,16 +118,17 @@ constexpr int kMaxKSlice = 17408;  // elements of x per CTA
 constexpr uint32_t kSmemBytes = 227u * 1024u;
 constexpr uint32_t kBarBytes = 1024;
 constexpr uint32_t kRedBytes = kMaxSplit * kRows * 4;
-template <int CH, int kMeta> struct Lay {
-  static_assert(kMeta >= kGroups && kMeta <= kMetaMax, "a group's stages must not share an operand slot");
-  static constexpr uint32_t kAtoms = kMeta * CH;  // term atoms in the operand ring (CH per slot)
-  static constexpr uint32_t kFixed = 2 * kAtoms * 1024 + kMeta * kSFABytes + 512 + kMaxKSlice * 2 + kRedBytes +
-                                     kBarBytes + 1024;
+template <int MODE> struct Lay {
+  using G = Geo<MODE>;
+  static_assert(G::kMeta >= kGroups && G::kMeta <= kMetaMax, "a group's stages must not share an operand slot");
+  static constexpr uint32_t kAtoms = G::kMeta * G::kCh;  // term atoms in the operand ring (kCh per slot)
+  static constexpr uint32_t kFixed = 2 * kAtoms * 1024 + G::kMeta * G::kSFABytes + 512 + kMaxKSlice * 2 +
+                                     kRedBytes + kBarBytes + 1024;
   static constexpr uint32_t kRing = (kSmemBytes - kFixed) / 1024u * 1024u;
-  static constexpr uint32_t kOffB = kRing;                   // terms 0..7: atom CH m + h of slot m
+  static constexpr uint32_t kOffB = kRing;                   // terms 0..7: atom kCh m + h of slot m
   static constexpr uint32_t kOffB8 = kOffB + kAtoms * 1024;  // term 8 (+ 7 unused rows), same index
   static constexpr uint32_t kOffSFA = kOffB8 + kAtoms * 1024;
-  static constexpr uint32_t kOffSFB = kOffSFA + kMeta * kSFABytes;
+  static constexpr uint32_t kOffSFB = kOffSFA + G::kMeta * G::kSFABytes;
   static constexpr uint32_t kOffX = kOffSFB + 512;             // x slice (bf16)
   static constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;  // [split][128] fp32 partials (rank 0)
   static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
@@ -154,10 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
                                                               uint32_t sslot, uint16_t* __restrict__ y,
                                                               unsigned* __restrict__ err) {
   using F = Fmt<MODE>;
-  using L = Lay<F::kCh, F::kMeta>;
-  constexpr int kCh = F::kCh;
-  constexpr int kMeta = F::kMeta;
-  constexpr int kBK = kChunk * kCh;  // codes per stage
+  using G = Geo<MODE>;
+  using L = Lay<MODE>;
+  constexpr int kCh = G::kCh;
+  constexpr int kMeta = G::kMeta;
+  constexpr int kBK = G::kBK;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -235,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       prefetch_tmap(&tmW);
       prefetch_tmap(&tmS);
       // out-of-range rows are zero-filled and counted
-      const uint32_t tx = (uint32_t)R * (128u * kCh + 16u);
+      const uint32_t tx = (uint32_t)R * (128u * kCh + G::kSB);
       int s = 0, round = 0;
       for (int i = 0; i < nst; ++i) {
         if (round > 0) mbar_wait(&wempty[s], (round - 1) & 1, err, failed);
@@ -243,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
 #pragma unroll
         for (int h = 0; h < kCh; ++h)
           tma_load_2d(smem + s * wslot + h * wchunk, &tmW, &wfull[s], ((kb0 + i) * kCh + h) * 128, r0);
-        tma_load_2d(smem + offS + s * sslot, &tmS, &wfull[s], (kb0 + i) * 16, r0);
+        tma_load_2d(smem + offS + s * sslot, &tmS, &wfull[s], (kb0 + i) * G::kSB, r0);
         if (++s == nslots) { s = 0; ++round; }
       }
       // no copy may still be writing shared memory when the CTA exits
@@ -260,10 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       for (int i = 0; i < nst; ++i) {
         mbar_wait(&mfull[m], mround & 1, err, failed);  // the group also saw the weights land
         tc_fence_after();
-        const uint32_t sfa_t = tmem + kSfaCol + 16 * m;
-        const uint32_t sfa_s = base + L::kOffSFA + m * kSFABytes;
+        const uint32_t sfa_t = tmem + kSfaCol + 4 * G::kTiles * m;
+        const uint32_t sfa_s = base + L::kOffSFA + m * G::kSFABytes;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)  // scale tiles start on 4-column boundaries of tensor memory
+        for (int j = 0; j < G::kTiles; ++j)  // scale tiles start on 4-column boundaries of tensor memory
           asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
                        :: "r"(sfa_t + 4 * j), "l"(desc_sf(sfa_s + 512 * j)) : "memory");
 #pragma unroll
@@ -273,15 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
           const uint64_t adesc = desc_sw128(base + s * wslot + h * wchunk, 1024) + (uint64_t)(2 * jj);
           // B rows 0..7: the chunk's term atom; rows 8..15: its term-8 atom, L::kAtoms KB further
           const uint64_t bdesc = desc_sw128(base + L::kOffB + (m * kCh + h) * 1024, L::kAtoms * 1024) + (uint64_t)(2 * jj);
-          // the 16 scale bytes of a row cover the stage: NVFP4 k-step j uses tile j; MXFP4
-          // k-step j uses half (j & 1) of tile j / 2 (scale-factor id 0 or 2)
-          const uint32_t tile = (kCh == 1) ? (uint32_t)j : (uint32_t)(j >> 1);
-          const uint32_t sf_id = (kCh == 1) ? 0u : (uint32_t)((j & 1) * 2);
+          // scale columns j kSpk .. of the stage: tile (j kSpk) / 4, scale-factor id (j kSpk) % 4
+          const uint32_t tile = (uint32_t)((j * G::kSpk) >> 2);
+          const uint32_t sf_id = (uint32_t)((j * G::kSpk) & 3);
           const uint32_t idesc = F::kIdesc | (sf_id << 29) | (sf_id << 4);
           // k-step j accumulates into tile j % 4 of D, so consecutive MMAs of a stage do
           // not wait on each other; the epilogue adds the four tiles
           const uint32_t acc = (i > 0 || j >= 4) ? 1u : 0u;
-          if (kCh == 1)
+          if (MODE == 2)
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
@@ -377,17 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
           else batom[L::kAtoms * 1024 + hi4 + lo] = code;
         }
       }
-      // (b) weight scales of row pt, once the stage has landed: 16 E4M3 bytes ->
-      // word j of tile j, 16-byte row (pt % 32), slot pt / 32; rows >= rows get 0
+      // (b) weight scales of row pt, once the stage has landed: kSB bytes -> word w of
+      // tile w, 16-byte row (pt % 32), slot pt / 32; rows >= rows get 0
       mbar_wait(&wfull[s], wr & 1, err, failed);
-      uint4 sv = make_uint4(0, 0, 0, 0);
-      if (pt < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + pt * 16);
-      uint8_t* sfa = smem + L::kOffSFA + m * kSFABytes;
+      uint8_t* sfa = smem + L::kOffSFA + m * G::kSFABytes;
       const uint32_t so = (uint32_t)((pt & 31) * 16 + (pt >> 5) * 4);
-      *reinterpret_cast<uint32_t*>(sfa + 0 * 512 + so) = sv.x;
-      *reinterpret_cast<uint32_t*>(sfa + 1 * 512 + so) = sv.y;
-      *reinterpret_cast<uint32_t*>(sfa + 2 * 512 + so) = sv.z;
-      *reinterpret_cast<uint32_t*>(sfa + 3 * 512 + so) = sv.w;
+#pragma unroll
+      for (int v = 0; v < G::kSB / 16; ++v) {
+        uint4 sv = make_uint4(0, 0, 0, 0);
+        if (pt < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + pt * G::kSB + 16 * v);
+        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 0) * 512 + so) = sv.x;
+        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 1) * 512 + so) = sv.y;
+        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 2) * 512 + so) = sv.z;
+        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 3) * 512 + so) = sv.w;
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&mfull[m]);
       m += kGroups;
@@ -509,9 +525,10 @@ struct TcPlan {
 // with the smallest estimate wins (ties go to the smaller split).
 template <int MODE>
 TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
-  constexpr int kCh = Fmt<MODE>::kCh;
-  constexpr int kMeta = Fmt<MODE>::kMeta;
-  constexpr int kBK = kChunk * kCh;
+  using G = Geo<MODE>;
+  constexpr int kCh = G::kCh;
+  constexpr int kMeta = G::kMeta;
+  constexpr int kBK = G::kBK;
   TcPlan best;
   if (K % kBK != 0 || N < 1 || d.sm_count < 1) return best;
   const int64_t nkb = K / kBK;
@@ -526,7 +543,7 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
     if (nblk < 1) continue;
     const int64_t R = (N + nblk - 1) / nblk;
     if (R > kRows) continue;
-    const double cost = (double)nst * std::max(stage_us, (double)R * (128.0 * kCh + 16.0) / (sm_gbs * 1e3));
+    const double cost = (double)nst * std::max(stage_us, (double)R * (128.0 * kCh + G::kSB) / (sm_gbs * 1e3));
     if (best.split == 0 || cost < best_cost) {
       best_cost = cost;
       best.split = split;
@@ -536,10 +553,10 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
   }
   if (best.split == 0) return best;
   best.wslot = (uint32_t)kCh * (uint32_t)((best.R + 7) / 8) * 1024u;
-  best.sslot = ((uint32_t)best.R * 16u + 127u) / 128u * 128u;
+  best.sslot = ((uint32_t)best.R * G::kSB + 127u) / 128u * 128u;
   // deeper than about 128 KB only lengthens the queues in front of the first stages
   const uint32_t slot = best.wslot + best.sslot;
-  best.nslots = (int)std::min<uint32_t>(kMaxSlots, Lay<kCh, kMeta>::kRing / slot);
+  best.nslots = (int)std::min<uint32_t>(kMaxSlots, Lay<MODE>::kRing / slot);
   best.nslots = std::max<int>(std::min<int>(best.nslots, kMeta), std::min<int>(best.nslots, kInflightBytes / slot));
   if (best.nslots < kMeta) best.split = 0;  // the slot relay needs nslots >= kMeta
   return best;
@@ -565,12 +582,12 @@ cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* 
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // W scales: [N, K/group] bytes (a multiple of 16 per row), boxes of R rows x 16 bytes
+  // W scales: [N, K/group] bytes (a multiple of 16 per row), boxes of R rows x kSB bytes
   CUtensorMap tmS;
   {
     cuuint64_t dims[2] = {(cuuint64_t)(K / group), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / group)};
-    cuuint32_t box[2] = {16, (cuuint32_t)p.R};
+    cuuint32_t box[2] = {(cuuint32_t)Geo<MODE>::kSB, (cuuint32_t)p.R};
     if (fn(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(scales), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
