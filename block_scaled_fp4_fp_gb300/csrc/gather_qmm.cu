@@ -14,7 +14,8 @@
 //   * 8 producer warps gather the 128 activation rows with cp.async (16 bytes
 //     per copy, written in the 128-byte-swizzled K-major layout) and dequantize
 //     the 256 x 64 weight slice exactly to bf16 (e2m1 * 2^(byte-127)) into the
-//     same layout;
+//     same layout; each thread's weight codes and scales are loaded kPD stages
+//     ahead into registers;
 //   * one thread issues tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulator
 //     in tensor memory, M 128, N 256, K 16 per instruction);
 //   * after the last stage warps 0-3 read the accumulator (tcgen05.ld) and
@@ -33,6 +34,7 @@ constexpr int BN = 256;
 constexpr int BK = 64;                 // bf16 elements per stage row: 128 bytes
 constexpr int STAGES = 4;
 constexpr int kProducerWarps = 8;
+constexpr int kPD = 2;                 // weight prefetch distance (stages) in the producers' registers
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;  // + MMA warp
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
@@ -150,53 +152,74 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
     const int64_t groups_per_row = K / 32;
     const uint32_t* we = w + (int64_t)expert * N * words_per_row;
     const uint8_t* se = scales + (int64_t)expert * N * groups_per_row;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % STAGES;
-      const int round = kb / STAGES;
-      if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
-      const uint32_t a_s = base + s * STAGE_BYTES;
-      uint8_t* b_s = smem + s * STAGE_BYTES + A_BYTES;
-      // activations: 128 rows x 8 chunks of 16 bytes
+    // Each thread dequantizes kItems (row, 32-code group) items per stage.  Their
+    // codes and scales are loaded kPD stages ahead into a register ring, so the
+    // global-memory latency overlaps the dequantization of the stages between.
+    constexpr int kItems = (BN * 2) / kProducers;
+    uint4 qr[kPD + 1][kItems];
+    uint32_t sr[kPD + 1][kItems];
+    auto load_w = [&](int kb, uint4 (&q)[kItems], uint32_t (&sc)[kItems]) {
 #pragma unroll
-      for (int i = 0; i < (BM * 8) / kProducers; ++i) {
-        const int idx = t + kProducers * i;
-        const int r = idx >> 3, c = idx & 7;
-        const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
-        cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      // weights: 256 rows x 2 groups of 32 codes, dequantized to bf16
-#pragma unroll
-      for (int i = 0; i < (BN * 2) / kProducers; ++i) {
+      for (int i = 0; i < kItems; ++i) {
         const int item = t + kProducers * i;
         const int n = item >> 1, g = item & 1;
-        uint4 o[4];
         if (n0 + n < N) {
-          const uint4 q = ld_stream_v4(we + (int64_t)(n0 + n) * words_per_row + (kb * BK + g * 32) / 8);
-          const float sc = e8m0_to_f32(__ldg(se + (int64_t)(n0 + n) * groups_per_row + kb * 2 + g));
-          const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t p[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const uint32_t h2 = e2m1x2_to_f16x2((wv[j] >> (8 * b)) & 0xFFu);
-              p[b] = pack_bf16x2_rn(__fmul_rn(f16_lo_to_f32(h2), sc), __fmul_rn(f16_hi_to_f32(h2), sc));
-            }
-            o[j] = make_uint4(p[0], p[1], p[2], p[3]);
-          }
+          q[i] = ld_stream_v4(we + (int64_t)(n0 + n) * words_per_row + (kb * BK + g * 32) / 8);
+          sc[i] = __ldg(se + (int64_t)(n0 + n) * groups_per_row + kb * 2 + g);
         } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[j] = make_uint4(0, 0, 0, 0);
+          q[i] = make_uint4(0, 0, 0, 0);
+          sc[i] = 0;
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(b_s + sw128(n, g * 4 + j)) = o[j];
       }
-      // stage kb-1 is complete once its copies landed: publish it
-      if (kb > 0) {
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&full[(kb - 1) % STAGES]);
+    };
+#pragma unroll
+    for (int u = 0; u < kPD; ++u)
+      if (u < num_kb) load_w(u, qr[u], sr[u]);
+    for (int kb0 = 0; kb0 < num_kb; kb0 += kPD + 1) {
+#pragma unroll
+      for (int u = 0; u <= kPD; ++u) {
+        const int kb = kb0 + u;
+        if (kb < num_kb) {
+          if (kb + kPD < num_kb) load_w(kb + kPD, qr[(u + kPD) % (kPD + 1)], sr[(u + kPD) % (kPD + 1)]);
+          const int s = kb % STAGES;
+          const int round = kb / STAGES;
+          if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
+          const uint32_t a_s = base + s * STAGE_BYTES;
+          uint8_t* b_s = smem + s * STAGE_BYTES + A_BYTES;
+          // activations: 128 rows x 8 chunks of 16 bytes
+#pragma unroll
+          for (int i = 0; i < (BM * 8) / kProducers; ++i) {
+            const int idx = t + kProducers * i;
+            const int r = idx >> 3, c = idx & 7;
+            const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
+            cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+          // weights: 256 rows x 2 groups of 32 codes, dequantized to bf16 (exact)
+#pragma unroll
+          for (int i = 0; i < kItems; ++i) {
+            const int item = t + kProducers * i;
+            const int n = item >> 1, g = item & 1;
+            const float sc = e8m0_to_f32(sr[u][i]);
+            const uint32_t wv[4] = {qr[u][i].x, qr[u][i].y, qr[u][i].z, qr[u][i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int bb = 0; bb < 4; ++bb) {
+                const uint32_t h2 = e2m1x2_to_f16x2((wv[j] >> (8 * bb)) & 0xFFu);
+                pk[bb] = pack_bf16x2_rn(__fmul_rn(f16_lo_to_f32(h2), sc), __fmul_rn(f16_hi_to_f32(h2), sc));
+              }
+              *reinterpret_cast<uint4*>(b_s + sw128(n, g * 4 + j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+          // stage kb-1 is complete once its copies landed: publish it
+          if (kb > 0) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&full[(kb - 1) % STAGES]);
+          }
+        }
       }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
