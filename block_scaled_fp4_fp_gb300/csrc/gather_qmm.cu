@@ -11,7 +11,7 @@
 // expert's segment (tiles never straddle experts; the tile -> expert map is
 // rebuilt in every CTA by binary searches over the sorted expert ids, so no
 // workspace is needed) and one 256-column slice of N.  Per K = 64 stage:
-//   * 8 producer warps gather the 128 activation rows with cp.async (16 bytes
+//   * 16 producer warps gather the 128 activation rows with cp.async (16 bytes
 //     per copy, written in the 128-byte-swizzled K-major layout) and dequantize
 //     the 256 x 64 weight slice exactly to bf16 (e2m1 * 2^(byte-127)) into the
 //     same layout; each thread's weight codes and scales are loaded kPD stages
@@ -33,7 +33,7 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;                 // bf16 elements per stage row: 128 bytes
 constexpr int STAGES = 4;
-constexpr int kProducerWarps = 8;
+constexpr int kProducerWarps = 16;
 constexpr int kPD = 2;                 // weight prefetch distance (stages) in the producers' registers
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;  // + MMA warp
