@@ -31,6 +31,8 @@
  *     the ABI.  Launch failures return FP4_ERR_CUDA.  A device-side wait that
  *     gives up (bounded spin) records FP4_ERR_TIMEOUT, which
  *     fp4_check_device_error() reports.
+ *   - Every size (n, rows, cols, N, K, M, R, E) must be at least 1: an empty
+ *     problem returns FP4_ERR_INVALID_ARG and launches nothing.
  *   - NVFP4: e2m1 codes, groups of 16, E4M3 block scales, optional fp32 global
  *     scale gs in the multiplier form gs = amax/2688 (2688 = 448*6).
  *     MXFP4: e2m1 codes, groups of 32, E8M0 block scales.

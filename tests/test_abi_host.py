@@ -71,3 +71,12 @@ def test_validation_rejects_before_launch(B):
     assert L.qmv(odd, p, p, None, None, 64, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_ALIGNMENT
     assert L.qqmm(p, odd, p, p, None, None, 1, 8, 256, B.MODE_NVFP4, p, None) == B.FP4_ERR_ALIGNMENT
     assert L.fp4_amax_global_scale(p, 16, p, None, p, 2, None) == B.FP4_ERR_INVALID_ARG  # ws too small
+    # empty problems: every size must be at least 1
+    assert L.fp4_amax_global_scale(p, 0, p, None, p, 4096, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize(p, 4, 0, B.MODE_NVFP4, 4, 16, None, p, p, 0, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_dequantize(p, p, None, 0, 64, B.MODE_NVFP4, 4, 16, None, 0, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.qmv(p, p, p, None, None, 0, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.qmv(p, p, p, None, None, 64, 0, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.qqmm(p, p, p, p, None, None, 0, 8, 256, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.gather_qmm(p, p, p, 0, p, p, None, 2, 32, 64, B.MODE_MXFP4, 4, 32, 1, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.gather_qmm(p, p, p, 8, p, p, None, 0, 32, 64, B.MODE_MXFP4, 4, 32, 1, p, None) == B.FP4_ERR_INVALID_ARG

@@ -47,3 +47,23 @@ def test_gather_moe_full_size_sampled(B):
                                      np.random.default_rng(0).integers(0, len(rhs), 8)]))
     out, ref = run(B, 2048, 32, 4, 5760, 2880, seed=0, rows=rows)
     assert_close_to_oracle(out, ref, "gather gate/up full size")
+
+
+def test_gather_segments_on_tile_boundaries(B):
+    """Hand-built routing whose expert segments are empty, one row, and 127 /
+    128 / 129 / 256 / 300 rows long, so 128-row tiles start, end and straddle
+    every boundary case; activation rows repeat and come in any order."""
+    E, N, K = 8, 96, 128
+    sizes = [0, 1, 127, 128, 0, 129, 256, 300]
+    rhs = np.repeat(np.arange(E, dtype=np.int32), sizes)
+    R = len(rhs)
+    tokens = 200
+    lhs = np.random.default_rng(5).integers(0, tokens, R).astype(np.int32)
+    x = synth.bf16_normal((tokens, K), 1.0, seed=6)
+    w = synth.bf16_normal((E * N, K), 0.02, seed=7)
+    q, s = oracle.mxfp4_quantize(synth.to_u16(w))
+    q3, s3 = q.reshape(E, N, K // 8), s.reshape(E, N, K // 32)
+    out = B.gather_qmm(x.cuda(), torch.from_numpy(lhs).cuda(), torch.from_numpy(rhs).cuda(),
+                       torch.from_numpy(q3.view(np.int32)).cuda(), torch.from_numpy(s3).cuda())
+    ref = oracle.gather_qmm(synth.to_u16(x), lhs, rhs, q3, s3, None, oracle.MODE_MXFP4, 32)
+    assert_close_to_oracle(out, ref, "gather tile-boundary segments")
