@@ -175,6 +175,12 @@ class DecodeStack:
         for m, y in zip(self.mats, self.y):
             B.qmv(self.x[m["K"]], m["q"], m["s"], m["b"], m["gs"], mode=self.mode, y=y, stream=stream)
 
+    def stream_step(self, stream=None):
+        """The same weights moved as the tensor-core GEMV moves them, with no
+        compute (NVFP4 only): the launch-and-stream ceiling of that kernel shape."""
+        for m in self.mats:
+            self.B.fp4_debug_stream_weights(m["q"], m["s"], stream=stream)
+
     @property
     def launches(self):
         return len(self.mats)
@@ -208,7 +214,7 @@ def capture(fn, stream):
 
 
 # ------------------------------------------------------------------ components
-def bench_quantize(B, device, reps=40):
+def bench_quantize(B, device, reps=50):
     """Activation quantize 4096x5120 (0.1 % outliers x50), tiled scales; 4 rotating inputs."""
     xs = [synth.activations_with_outliers(4096, 5120, seed=i, outlier_seed=100 + i, device=device) for i in range(4)]
     res = {}
@@ -231,7 +237,7 @@ def bench_quantize(B, device, reps=40):
     return res
 
 
-def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=10):
+def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
     N, K = 17408, 5120
     w = synth.bf16_normal((N, K), 0.02, seed=1, device=device)
     gw = B.fp4_amax_global_scale(w)
@@ -253,34 +259,54 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=10):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps if reps else float("nan")
+        # the activation's global scale and quantization (tiled scales) in front of each GEMM
+        e0.record()
+        for _ in range(reps):
+            B.fp4_amax_global_scale_noalloc(x, gs_out=gx)
+            B.fp4_quantize(x, B.MODE_NVFP4, global_scale=gx, layout=B.SCALES_TILED, xq=xq, scales=xs)
+            B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms_q = e0.elapsed_time(e1) / reps if reps else float("nan")
         flops = 2.0 * M * N * K
-        res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}
+        res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops,
+                        "ms_with_x_quantize": ms_q, "TFLOP/s_with_x_quantize": flops / ms_q / 1e9}
         del x, xq, xs, out
     return res
 
 
-def bench_gather(B, device, reps=10):
-    tokens, E, topk, N, K = 2048, 32, 4, 5760, 2880
+def bench_gather(B, device, reps=20):
+    """MoE grouped W4A16 GEMMs of 2048 tokens, 32 experts, top-4: gate/up
+    (N 5760, K 2880) on the routed token rows, and down (N 2880, K 2880) on a
+    fresh [8192, 2880] input already in routed order."""
+    tokens, E, topk, H, F = 2048, 32, 4, 2880, 5760
     lhs, rhs = synth.moe_routing(tokens, E, topk, seed=0)
-    lhs_d, rhs_d = torch.from_numpy(lhs).to(device), torch.from_numpy(rhs).to(device)
-    x = synth.bf16_normal((tokens, K), 1.0, seed=1, device=device)
-    w = synth.bf16_normal((E * N, K), 0.02, seed=2, device=device)
-    q, s = B.fp4_quantize(w, B.MODE_MXFP4)
-    del w
-    q3, s3 = q.view(E, N, K // 8), s.view(E, N, K // 32)
-    out = torch.empty((len(lhs), N), dtype=torch.bfloat16, device=device)
-    for _ in range(3):  # warm-up
-        B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps if reps else float("nan")
-    flops = 2.0 * len(lhs) * N * K
-    return {"gate_up": {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}}
+    rhs_d = torch.from_numpy(rhs).to(device)
+    res = {}
+    for name, N, K, x, lhs_rows in (
+            ("gate_up", F, H, synth.bf16_normal((tokens, H), 1.0, seed=1, device=device), lhs),
+            ("down", H, H, synth.bf16_normal((len(lhs), H), 1.0, seed=3, device=device),
+             np.arange(len(lhs), dtype=np.int32))):
+        lhs_d = torch.from_numpy(lhs_rows).to(device)
+        w = synth.bf16_normal((E * N, K), 0.02, seed=2 if name == "gate_up" else 4, device=device)
+        q, s = B.fp4_quantize(w, B.MODE_MXFP4)
+        del w
+        q3, s3 = q.view(E, N, K // 8), s.view(E, N, K // 32)
+        out = torch.empty((len(lhs), N), dtype=torch.bfloat16, device=device)
+        for _ in range(3):  # warm-up
+            B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            B.gather_qmm(x, lhs_d, rhs_d, q3, s3, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps if reps else float("nan")
+        flops = 2.0 * len(lhs) * N * K
+        res[name] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}
+        del x, q, s, out
+    return res
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -306,6 +332,48 @@ def oracle_layer_time(mats, xs):
     for q, s, gs, K in mats:
         oracle.qmv(xs[K], q, s, None, oracle.MODE_NVFP4, 16, gs)
     return time.perf_counter() - t0, nbytes
+
+
+def cpu_component_baselines():
+    """The oracle timed on the host cores for the components, on bounded samples
+    (each labelled): quantize in full, qqmm on a 4-row slice, MoE gate/up on 8
+    routed rows of one expert."""
+    import oracle
+    res = {}
+    x = synth.to_u16(synth.activations_with_outliers(4096, 5120, seed=0, outlier_seed=100))
+    gs = oracle.global_scale(x)
+    t0 = time.perf_counter()
+    oracle.nvfp4_quantize(x, gs)
+    t = time.perf_counter() - t0
+    res["quantize_4096x5120"] = {"value": (x.nbytes + x.nbytes // 4 + x.nbytes // 32) / t / 1e9, "unit": "GB/s",
+                                 "sample": "4096x5120 NVFP4 in full"}
+    w = synth.to_u16(synth.bf16_normal((1024, 5120), 0.02, seed=1))  # 1024 of the 17408 weight rows
+    gw = oracle.global_scale(w)
+    wq, ws = oracle.nvfp4_quantize(w, gw)
+    xs = synth.to_u16(synth.bf16_normal((32, 5120), 1.0, seed=2))
+    gx = oracle.global_scale(xs)
+    xq, sx = oracle.nvfp4_quantize(xs, gx)
+    t0 = time.perf_counter()
+    oracle.qqmm(xq, sx, wq, ws, oracle.MODE_NVFP4, alpha=gx * gw)
+    t = time.perf_counter() - t0
+    res["qqmm_nvfp4_Mx17408x5120"] = {"value": 2.0 * 32 * 1024 * 5120 / t / 1e12, "unit": "TFLOP/s",
+                                      "sample": "32 rows x 1024 columns of M x 17408 x 5120"}
+    del w, wq, ws
+    lhs, rhs = synth.moe_routing(2048, 32, 4, seed=0)
+    e0 = int(rhs[0])
+    sel = np.nonzero(rhs == e0)[0][:8]
+    xg = synth.to_u16(synth.bf16_normal((2048, 2880), 1.0, seed=1))
+    we = synth.to_u16(synth.bf16_normal((5760, 2880), 0.02, seed=2))
+    q, sc = oracle.mxfp4_quantize(we)
+    t0 = time.perf_counter()
+    oracle.gather_qmm(xg, lhs[sel], np.zeros(len(sel), np.int32), q.reshape(1, 5760, 360), sc.reshape(1, 5760, 90),
+                      None, oracle.MODE_MXFP4, 32)
+    t = time.perf_counter() - t0
+    res["gather_qmm_mxfp4_moe"] = {"value": 2.0 * len(sel) * 5760 * 2880 / t / 1e12, "unit": "TFLOP/s",
+                                   "sample": f"gate/up, {len(sel)} routed rows of one expert"}
+    for v in res.values():
+        v.update({"kind": "oracle", "cores": oracle.num_threads()})
+    return res
 
 
 def cpu_cores():
@@ -407,6 +475,10 @@ def run_ours(args):
             torch.cuda.empty_cache()
 
     stack, graph, ms = headline
+    # the same 448 launches streaming the same weights with no compute
+    sgraph = capture(stack.stream_step, stream)
+    stream_ms = time_graph(sgraph, args.steps, args.warmup, stream)
+    del sgraph
     # e2e: pinned host activations in, every projection's output back, through the C ABI
     hx = {k: v.cpu().pin_memory() for k, v in stack.x.items()}
     hy = torch.empty((sum(m["N"] for m in stack.mats),), dtype=torch.bfloat16).pin_memory()
@@ -447,6 +519,10 @@ def run_ours(args):
             v["frac_of_bf16_peak"] = v["TFLOP/s"] / peaks["bf16_tflops"]
         for k, v in comps["quantize_4096x5120"].items():
             v["frac_of_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+        if ws == 1 and not args.no_cpu:
+            import oracle
+            oracle.build()
+            comps["cpu_oracle"] = cpu_component_baselines()
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -472,7 +548,12 @@ def run_ours(args):
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": committed_traffic("qmv_tc.cu", "qmv_tc_nvfp4_decode_layer"),
                          "kernel": "qmv_tc_kernel (tcgen05 NVFP4 GEMV)", "bytes_per_launch": per_launch_bytes,
-                         "peak_src": peaks["src"] + " hbm_gbs"},
+                         "peak_src": peaks["src"] + " hbm_gbs",
+                         "stream_ceiling": {"GB/s": stack.bytes / stream_ms / 1e6, "ms_per_step": stream_ms,
+                                            "frac_of_peak": stack.bytes / stream_ms / 1e6 / peaks["hbm_gbs"],
+                                            "qmv_frac_of_ceiling": stream_ms / ms,
+                                            "what": "fp4_debug_stream_weights over the same 448 launches: the "
+                                                    "same TMA boxes, ring and launch, no compute"}},
             "cpu_baseline": cpu,
             "e2e": {"value": ws * stack.bytes / e2e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

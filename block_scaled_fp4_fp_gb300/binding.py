@@ -44,6 +44,7 @@ SIGNATURES = {
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
     "fp4_debug_inject_wait_timeout": (_INT, [_INT]),
+    "fp4_debug_stream_weights": (_INT, [_VP, _VP, _I64, _I64, _VP]),
     "fp4_amax_global_scale_noalloc": (_INT, [_VP, _I64, _VP, _VP, _VP]),
 }
 
@@ -190,6 +191,13 @@ def gather_qmm(x: torch.Tensor, lhs_idx: torch.Tensor, rhs_idx: torch.Tensor, w:
     _check(lib().gather_qmm(_p(x), _p(lhs_idx), _p(rhs_idx), R, _p(w), _p(scales), _p(biases), E, N, K, mode, 4,
                             group_size, 1 if sorted_indices else 0, _p(out), _s(stream)), "gather_qmm")
     return out
+
+
+def fp4_debug_stream_weights(wq: torch.Tensor, scales: torch.Tensor, stream=None):
+    """Stream NVFP4 weights as qmv's tensor-core path does, computing nothing
+    (the launch-and-stream ceiling of that kernel shape)."""
+    N, K = wq.shape[0], wq.shape[1] * 8
+    _check(lib().fp4_debug_stream_weights(_p(wq), _p(scales), N, K, _s(stream)), "fp4_debug_stream_weights")
 
 
 def fp4_debug_inject_wait_timeout(enable: bool):

@@ -236,6 +236,18 @@ fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* 
                                      K, mode, out, stream));
 }
 
+fp4_status fp4_debug_stream_weights(const uint32_t* w, const uint8_t* scales, int64_t N, int64_t K,
+                                    cudaStream_t stream) {
+  if (!w || !scales || N <= 0 || K <= 0 || K % 256 != 0 || N > INT32_MAX / 2 || K > (1 << 24))
+    return FP4_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(scales, 16)) return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  if (N > (int64_t)128 * d->sm_count) return FP4_ERR_UNSUPPORTED;
+  return from_cuda(launch_weight_stream(*d, w, scales, N, K, stream));
+}
+
 fp4_status fp4_debug_inject_wait_timeout(int enable) {
   g_inject_timeout.store(enable ? 1 : 0);
   return FP4_OK;

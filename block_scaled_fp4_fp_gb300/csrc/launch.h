@@ -5,7 +5,9 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 namespace fp4 {
 
@@ -34,6 +36,7 @@ cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, c
                        int group, uint16_t* y, cudaStream_t s);
 
 // qmv_tc.cu (NVFP4 = mode 2 and MXFP4 = mode 1 on tcgen05; launch_qmv dispatches to it when supported)
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // driver's tensor-map encoder (nullptr if unavailable)
 bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K);
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s);
@@ -43,6 +46,10 @@ cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
                         const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
                         int64_t N, int64_t K, int mode, uint16_t* out, int inject_timeout,
                         cudaStream_t s);
+
+// weight_stream.cu (measurement aid: the GEMV's weight stream without the GEMV)
+cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint8_t* scales, int64_t N,
+                                 int64_t K, cudaStream_t s);
 
 // gather_qmm.cu
 cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs,

@@ -80,3 +80,5 @@ def test_validation_rejects_before_launch(B):
     assert L.qqmm(p, p, p, p, None, None, 0, 8, 256, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG
     assert L.gather_qmm(p, p, p, 0, p, p, None, 2, 32, 64, B.MODE_MXFP4, 4, 32, 1, p, None) == B.FP4_ERR_INVALID_ARG
     assert L.gather_qmm(p, p, p, 8, p, p, None, 0, 32, 64, B.MODE_MXFP4, 4, 32, 1, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_debug_stream_weights(p, p, 64, 320, None) == B.FP4_ERR_INVALID_ARG  # K % 256
+    assert L.fp4_debug_stream_weights(odd, p, 64, 256, None) == B.FP4_ERR_ALIGNMENT

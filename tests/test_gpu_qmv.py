@@ -155,3 +155,15 @@ def test_qmv_decode_layer_shapes_sampled(B, mode, proj):
                                      np.random.default_rng(proj).integers(0, N, 240)]))
     ref = oracle.qmv(synth.to_u16(x), q, s, b, mode, g, gs, rows=rows)
     assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"{name} mode {mode}")
+
+
+def test_weight_stream_ceiling_runs_clean(B):
+    """The stream-only measurement kernel reads the decode shapes' weights as the
+    tensor-core path does and leaves no device error behind."""
+    for N, K in [(5120, 5120), (17408, 5120), (5120, 17408), (7, 256)]:
+        w = synth.bf16_normal((N, K), 0.02, seed=N + K, device="cuda")
+        gs = B.fp4_amax_global_scale(w)
+        q, s = B.fp4_quantize(w, B.MODE_NVFP4, global_scale=gs)
+        B.fp4_debug_stream_weights(q, s)
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
