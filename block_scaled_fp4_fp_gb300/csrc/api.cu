@@ -244,7 +244,7 @@ fp4_status fp4_debug_stream_weights(const uint32_t* w, const uint8_t* scales, in
   const DevInfo* d = nullptr;
   fp4_status st = current(&d);
   if (st != FP4_OK) return st;
-  if (N > (int64_t)128 * d->sm_count) return FP4_ERR_UNSUPPORTED;
+  if (!qmv_tc_supported(*d, FP4_MODE_NVFP4, N, K)) return FP4_ERR_UNSUPPORTED;  // no tensor-core plan
   return from_cuda(launch_weight_stream(*d, w, scales, N, K, stream));
 }
 

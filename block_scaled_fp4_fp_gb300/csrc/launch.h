@@ -37,6 +37,8 @@ cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, c
 
 // qmv_tc.cu (NVFP4 = mode 2 and MXFP4 = mode 1 on tcgen05; launch_qmv dispatches to it when supported)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // driver's tensor-map encoder (nullptr if unavailable)
+// the NVFP4 plan: CTAs per cluster (K slices), row blocks, rows per CTA, weight ring slots
+bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nblk, int* R, int* nslots);
 bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K);
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s);

@@ -136,7 +136,7 @@ template <int MODE> struct Lay {
   // an MMA reads 16 KB of A from a code chunk's start: that stays inside the allocation
   static_assert(kRing + 16384 <= kOffBar, "A-operand reads past the allocation");
 };
-static_assert((2 * kMaxSlots + 2 * kMetaMax + 3) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
+static_assert((2 * kMaxSlots + 2 * kMetaMax + 4) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   uint64_t* done = mempty + kMetaMax;
   uint64_t* xbar = done + 1;
   uint64_t* pbar = xbar + 1;  // rank 0: the other ranks' partials have landed (byte count)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pbar + 1);
+  uint64_t* tbar = pbar + 1;  // warp 1 has allocated tensor memory (tmem_slot written)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tbar + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kPrep / 32 floats
   float* part = reinterpret_cast<float*>(smem + L::kOffRed);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L::kOffX);
@@ -215,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       mbar_init(done, 1);
       mbar_init(xbar, 1);
       mbar_init(pbar, 1);
+      mbar_init(tbar, 1);
     }
     fence_barrier_init();  // release of the barrier inits to the cluster
   }
@@ -222,11 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   // rank 0 has started and its barriers are initialized.
   __syncwarp();
   if (split > 1) cluster_arrive_relaxed();
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
   // The constant term-scale tile: B row t < 9 (tile row t, slot 0) holds the
   // E4M3 weight 2^(7-2t) for each of the k-step's four 16-element blocks;
   // rows 9..31 are zero, so B rows 9..15 add nothing.
@@ -236,10 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     reinterpret_cast<uint32_t*>(smem + L::kOffSFB)[threadIdx.x] = v;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  uint32_t tmem = 0;  // tensor-memory base: warp 1 after its allocation, group 0 after `done`
   bool failed = false;
   float partial = 0.f;  // group 0: this CTA's partial y of row 32 (warp & 3) + lane
 
@@ -266,6 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
+    // The tensor-memory allocation takes about a microsecond: it happens here,
+    // while the weights stream and the prep warps build the first operands.
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    tmem = *tmem_slot;
+    if (lane == 0) mbar_arrive(tbar);  // releases the tmem_slot write to the epilogue
     if (elect_one_sync()) {
       asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
                    :: "r"(tmem + kSfbCol), "l"(desc_sf(base + L::kOffSFB)) : "memory");
@@ -413,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     }
     // ---- epilogue (group 0, warps 2..5 = lane quadrants 2, 3, 0, 1): partial = 2^e0 sum_t D[row, t]
     if (grp == 0) {
+      mbar_wait(tbar, 0, err, failed);
       mbar_wait(done, 0, err, failed);
       tc_fence_after();
+      tmem = *tmem_slot;
       const int q = warp & 3;
       float dsum[kTerms];
 #pragma unroll
@@ -623,6 +630,16 @@ bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K) {
   if (mode == 2) return plan_qmv_tc<2>(d, N, K).split > 0;
   if (mode == 1) return plan_qmv_tc<1>(d, N, K).split > 0;
   return false;
+}
+
+bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nblk, int* R, int* nslots) {
+  const TcPlan p = plan_qmv_tc<2>(d, N, K);
+  if (p.split == 0) return false;
+  *split = p.split;
+  *nblk = p.nblk;
+  *R = p.R;
+  *nslots = p.nslots;
+  return true;
 }
 
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,

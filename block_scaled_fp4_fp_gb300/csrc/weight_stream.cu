@@ -4,7 +4,8 @@
 // (codes [N, K/2] bytes and linear E4M3 scales [N, K/16]) from HBM into shared
 // memory the way the tensor-core qmv does -- one TMA box of R rows x 128 bytes
 // of codes and one of R rows x 16 bytes of scales per K = 256 stage, a ring of
-// slots holding at most about 128 KB, one CTA per SM, programmatic dependent
+// slots holding at most about 128 KB, the same split of K over the CTAs of a
+// row block and the same rows per CTA, one CTA per SM, programmatic dependent
 // launch with consumption after griddepcontrol.wait -- and computes nothing.
 // Timed over the same weights, it is the launch-and-stream ceiling the GEMV
 // is compared with: the part of a launch no kernel of this shape can avoid.
@@ -21,11 +22,10 @@ constexpr int kThreadsS = 64;                 // warp 0: TMA producer; warp 1: c
 constexpr int kSlotsMax = 32;
 constexpr uint32_t kSmemS = 226u * 1024u;   // + 512 bytes of static barriers <= 227 KB
 constexpr uint32_t kRingS = kSmemS - 1024u;   // after aligning the base to 1024 bytes
-constexpr uint32_t kInflight = 128u * 1024u;  // as the GEMV
 
 __global__ void __launch_bounds__(kThreadsS, 1) weight_stream_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                       const __grid_constant__ CUtensorMap tmS,
-                                                                      int N, int K, int R, int nslots,
+                                                                      int N, int K, int R, int split, int nslots,
                                                                       uint32_t wslot, uint32_t sslot,
                                                                       unsigned* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
@@ -33,8 +33,11 @@ __global__ void __launch_bounds__(kThreadsS, 1) weight_stream_kernel(const __gri
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   __shared__ uint64_t full[kSlotsMax], empty[kSlotsMax];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int r0 = (int)(((int64_t)N * blockIdx.x) / gridDim.x);
-  const int nkb = K / 256;
+  const int rank = (int)(blockIdx.x % (unsigned)split);  // K slice of this CTA's row block
+  const int blk = (int)(blockIdx.x / (unsigned)split), nblk = (int)(gridDim.x / (unsigned)split);
+  const int r0 = (int)(((int64_t)N * blk) / nblk);
+  const int kb0 = (int)(((int64_t)(K / 256) * rank) / split);
+  const int nkb = (int)(((int64_t)(K / 256) * (rank + 1)) / split) - kb0;
   const uint32_t offS = (uint32_t)nslots * wslot;
   if (threadIdx.x < (unsigned)nslots) {
     mbar_init(&full[threadIdx.x], 1);
@@ -51,8 +54,8 @@ __global__ void __launch_bounds__(kThreadsS, 1) weight_stream_kernel(const __gri
     for (int i = 0; i < nkb; ++i) {
       if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
       mbar_arrive_expect_tx(&full[s], tx);
-      tma_load_2d(smem + s * wslot, &tmW, &full[s], i * 128, r0);
-      tma_load_2d(smem + offS + s * sslot, &tmS, &full[s], i * 16, r0);
+      tma_load_2d(smem + s * wslot, &tmW, &full[s], (kb0 + i) * 128, r0);
+      tma_load_2d(smem + offS + s * sslot, &tmS, &full[s], (kb0 + i) * 16, r0);
       if (++s == nslots) { s = 0; ++round; }
     }
     // no copy may still be writing shared memory when the CTA exits
@@ -74,14 +77,12 @@ cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint
                                  int64_t K, cudaStream_t s) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
-  const int64_t grid = std::min<int64_t>(N, d.sm_count);
-  const int R = (int)((N + grid - 1) / grid);
+  int split = 0, nblk = 0, R = 0, nslots = 0;
+  if (!qmv_tc_geometry(d, N, K, &split, &nblk, &R, &nslots)) return cudaErrorInvalidValue;
+  const int64_t grid = (int64_t)nblk * split;
   const uint32_t wslot = (uint32_t)((R + 7) / 8) * 1024u;
   const uint32_t sslot = ((uint32_t)R * 16u + 127u) / 128u * 128u;
-  const uint32_t slot = wslot + sslot;
-  int nslots = (int)std::min<uint32_t>(kSlotsMax, kRingS / slot);
-  nslots = std::max<int>(std::min<int>(nslots, 6), std::min<int>(nslots, kInflight / slot));
-  if (nslots < 1) return cudaErrorInvalidValue;
+  if ((uint32_t)nslots * (wslot + sslot) > kRingS || nslots > kSlotsMax) return cudaErrorInvalidValue;
   cuuint32_t estr[2] = {1, 1};
   CUtensorMap tmW, tmS;
   {
@@ -114,7 +115,8 @@ cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, weight_stream_kernel, tmW, tmS, (int)N, (int)K, R, nslots, wslot, sslot, d.err);
+  return cudaLaunchKernelEx(&cfg, weight_stream_kernel, tmW, tmS, (int)N, (int)K, R, split, nslots, wslot, sslot,
+                            d.err);
 }
 
 }  // namespace fp4

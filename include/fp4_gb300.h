@@ -220,14 +220,15 @@ fp4_status fp4_amax_global_scale_noalloc(const fp4_bf16* x, int64_t n, float* gs
 fp4_status fp4_debug_inject_wait_timeout(int enable);
 
 /* Measurement aid (no counterpart on the pages): moves NVFP4 weights from HBM
- * into shared memory exactly as qmv's tensor-core path streams them -- one TMA
- * box of R rows x 128 bytes of codes and one of R rows x 16 bytes of scales per
- * K = 256 stage, at most about 128 KB in flight per CTA, one CTA per SM,
+ * into shared memory exactly as qmv's tensor-core path streams them -- the same
+ * split of K over CTAs, rows per CTA and ring of slots, one TMA box of R rows x
+ * 128 bytes of codes and one of R rows x 16 bytes of scales per K = 256 stage,
  * programmatic dependent launch, consumption after the previous kernel -- and
  * computes nothing.  Timing it over the same weights as qmv gives the
  * launch-and-stream ceiling of that kernel shape.
  *   w       uint32[N, K/8], 16-byte aligned      scales  uint8[N, K/16], 16-byte aligned
- * Requires K % 256 == 0; N above 128 rows per SM returns FP4_ERR_UNSUPPORTED. */
+ * Requires K % 256 == 0; a shape the tensor-core path does not take returns
+ * FP4_ERR_UNSUPPORTED. */
 fp4_status fp4_debug_stream_weights(const uint32_t* w, const uint8_t* scales, int64_t N, int64_t K,
                                     cudaStream_t stream);
 
