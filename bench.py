@@ -136,12 +136,19 @@ def dist_env():
 class DecodeStack:
     """64-layer weight stack in one format, weights resident on the device."""
 
-    def __init__(self, B, mode: int, layers: int, device):
+    def __init__(self, B, mode: int, layers: int, device, fused_qkv: bool = False):
+        """fused_qkv: q, k and v of a layer stored as one [3*5120, 5120] matrix
+        (they multiply the same x), so a layer is 5 GEMVs instead of 7."""
         self.B, self.mode, self.layers = B, mode, layers
         self.mats = []
         self.bytes = 0
         for l in range(layers):
-            for p, (name, N, K) in enumerate(synth.LAYER_PROJECTIONS):
+            projs = list(enumerate(synth.LAYER_PROJECTIONS))
+            if fused_qkv:
+                self.mats.append(self._make(3 * synth.HIDDEN, synth.HIDDEN,
+                                            [synth.layer_seed(l, p) for p in range(3)], device))
+                projs = projs[3:]
+            for p, (name, N, K) in projs:
                 seed = synth.layer_seed(l, p)
                 self.mats.append(self._make(N, K, seed, device))
         self.x = {K: synth.bf16_normal((K,), 1.0, seed=7 + K, device=device)
@@ -162,7 +169,10 @@ class DecodeStack:
             nbytes = q.numel() * 4 + s.numel() * 2 + b.numel() * 2
             self.bytes += nbytes
             return {"N": N, "K": K, "q": q, "s": s, "b": b, "gs": None, "bytes": nbytes}
-        w = synth.bf16_normal((N, K), 0.02, seed=seed, device=device)
+        if isinstance(seed, list):  # rows of several projections, one after the other
+            w = torch.cat([synth.bf16_normal((N // len(seed), K), 0.02, seed=sd, device=device) for sd in seed])
+        else:
+            w = synth.bf16_normal((N, K), 0.02, seed=seed, device=device)
         gs = B.fp4_amax_global_scale(w) if self.mode == B.MODE_NVFP4 else None
         q, s = B.fp4_quantize(w, self.mode, global_scale=gs)
         del w
@@ -453,11 +463,12 @@ def run_ours(args):
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device)
 
-    modes = [("nvfp4", B.MODE_NVFP4)] + ([] if args.quick else [("mxfp4", B.MODE_MXFP4), ("affine_g64", B.MODE_AFFINE)])
+    modes = [("nvfp4", B.MODE_NVFP4)] + ([] if args.quick else [("mxfp4", B.MODE_MXFP4), ("affine_g64", B.MODE_AFFINE),
+                                                                ("nvfp4_fused_qkv", B.MODE_NVFP4)])
     results = {}
     headline = None
     for name, mode in modes:
-        stack = DecodeStack(B, mode, args.layers, device)
+        stack = DecodeStack(B, mode, args.layers, device, fused_qkv=name.endswith("fused_qkv"))
         graph = capture(stack.step, stream)
         if name == "nvfp4":
             with ClockSampler(local) as clk:
@@ -552,8 +563,9 @@ def run_ours(args):
                          "stream_ceiling": {"GB/s": stack.bytes / stream_ms / 1e6, "ms_per_step": stream_ms,
                                             "frac_of_peak": stack.bytes / stream_ms / 1e6 / peaks["hbm_gbs"],
                                             "qmv_frac_of_ceiling": stream_ms / ms,
-                                            "what": "fp4_debug_stream_weights over the same 448 launches: the "
-                                                    "same TMA boxes, ring and launch, no compute"}},
+                                            "what": f"fp4_debug_stream_weights over the same {stack.launches} "
+                                                    "launches: the same plan, TMA boxes, ring and launch, no "
+                                                    "compute"}},
             "cpu_baseline": cpu,
             "e2e": {"value": ws * stack.bytes / e2e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
