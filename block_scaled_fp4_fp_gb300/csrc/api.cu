@@ -195,7 +195,8 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
   const DevInfo* d = nullptr;
   st = current(&d);
   if (st != FP4_OK) return st;
-  return from_cuda(launch_qmv(*d, x, w, scales, biases, global_scale_w, N, K, mode, group_size, y, stream));
+  return from_cuda(launch_qmv(*d, x, w, scales, biases, global_scale_w, N, K, mode, group_size, y,
+                              g_inject_timeout.load(), stream));
 }
 
 fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
@@ -233,7 +234,7 @@ fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* 
   st = current(&d);
   if (st != FP4_OK) return st;
   return from_cuda(launch_gather_qmm(*d, x, lhs_idx, rhs_idx, R, w, static_cast<const uint8_t*>(scales), E, N,
-                                     K, mode, out, stream));
+                                     K, mode, out, g_inject_timeout.load(), stream));
 }
 
 fp4_status fp4_debug_stream_weights(const uint32_t* w, const uint8_t* scales, int64_t N, int64_t K,

@@ -61,7 +61,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ lhs, const int32_t* __restrict__ rhs,
     int R, const uint32_t* __restrict__ w, const uint8_t* __restrict__ scales, int E, int N, int K,
-    uint16_t* __restrict__ out, unsigned* __restrict__ err) {
+    uint16_t* __restrict__ out, unsigned* __restrict__ err, int inject_timeout) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -70,8 +70,9 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* accum_full = bars + 2 * STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
-  int* tile_info = reinterpret_cast<int*>(bars + 2 * STAGES + 2);  // expert, row0, rows
+  uint64_t* never = bars + 2 * STAGES + 1;  // fault injection: a barrier nothing arrives at
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+  int* tile_info = reinterpret_cast<int*>(bars + 2 * STAGES + 3);  // expert, row0, rows
   int* row_src = tile_info + 4;                                     // 128 activation rows
 
   const int warp = threadIdx.x >> 5;
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum_full, 1);
+    mbar_init(never, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -228,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   } else {
     // ------------------------------------------------------------ MMA warp --
     if (elect_one_sync()) {
+      if (inject_timeout) {
+        bool injected = false;  // separate flag: the injected expiry must not stop later waits
+        mbar_wait(never, 0, err, injected, 2000000LL);
+      }
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % STAGES;
         mbar_wait(&full[s], (kb / STAGES) & 1, err, failed);
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
 cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs,
                               const int32_t* rhs, int64_t R, const uint32_t* w,
                               const uint8_t* scales, int64_t E, int64_t N, int64_t K, int mode,
-                              uint16_t* out, cudaStream_t s) {
+                              uint16_t* out, int inject_timeout, cudaStream_t s) {
   (void)mode;
   if (SMEM_BYTES > d.smem_optin) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gather_qmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -304,7 +310,7 @@ cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t
   const int64_t m_tiles = (R + BM - 1) / BM + E;  // upper bound on per-expert tiles
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)m_tiles);
   gather_qmm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(x, lhs, rhs, (int)R, w, scales, (int)E, (int)N,
-                                                       (int)K, out, d.err);
+                                                       (int)K, out, d.err, inject_timeout);
   return cudaGetLastError();
 }
 

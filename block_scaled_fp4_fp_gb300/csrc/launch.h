@@ -33,7 +33,7 @@ cudaError_t launch_dequantize(const DevInfo& d, const uint32_t* wq, const void* 
 // qmv.cu
 cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, const void* scales,
                        const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode,
-                       int group, uint16_t* y, cudaStream_t s);
+                       int group, uint16_t* y, int inject_timeout, cudaStream_t s);
 
 // qmv_tc.cu (NVFP4 = mode 2 and MXFP4 = mode 1 on tcgen05; launch_qmv dispatches to it when supported)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // driver's tensor-map encoder (nullptr if unavailable)
@@ -41,7 +41,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // driver's tensor-map encoder (
 bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nblk, int* R, int* nslots);
 bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K);
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s);
+                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject_timeout, cudaStream_t s);
 
 // qqmm.cu
 cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
@@ -57,6 +57,6 @@ cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint
 cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs,
                               const int32_t* rhs, int64_t R, const uint32_t* w,
                               const uint8_t* scales, int64_t E, int64_t N, int64_t K, int mode,
-                              uint16_t* out, cudaStream_t s);
+                              uint16_t* out, int inject_timeout, cudaStream_t s);
 
 }  // namespace fp4

@@ -136,7 +136,7 @@ template <int MODE> struct Lay {
   // an MMA reads 16 KB of A from a code chunk's start: that stays inside the allocation
   static_assert(kRing + 16384 <= kOffBar, "A-operand reads past the allocation");
 };
-static_assert((2 * kMaxSlots + 2 * kMetaMax + 4) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
+static_assert((2 * kMaxSlots + 2 * kMetaMax + 5) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
                                                               const float* __restrict__ gs_w, int N, int K,
                                                               int R, int split, int nslots, uint32_t wslot,
                                                               uint32_t sslot, uint16_t* __restrict__ y,
-                                                              unsigned* __restrict__ err) {
+                                                              unsigned* __restrict__ err, int inject_timeout) {
   using F = Fmt<MODE>;
   using G = Geo<MODE>;
   using L = Lay<MODE>;
@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   uint64_t* xbar = done + 1;
   uint64_t* pbar = xbar + 1;  // rank 0: the other ranks' partials have landed (byte count)
   uint64_t* tbar = pbar + 1;  // warp 1 has allocated tensor memory (tmem_slot written)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tbar + 1);
+  uint64_t* never = tbar + 1; // fault injection: a barrier nothing arrives at
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kPrep / 32 floats
   float* part = reinterpret_cast<float*>(smem + L::kOffRed);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L::kOffX);
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       mbar_init(xbar, 1);
       mbar_init(pbar, 1);
       mbar_init(tbar, 1);
+      mbar_init(never, 1);
     }
     fence_barrier_init();  // release of the barrier inits to the cluster
   }
@@ -272,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     tmem = *tmem_slot;
     if (lane == 0) mbar_arrive(tbar);  // releases the tmem_slot write to the epilogue
     if (elect_one_sync()) {
+      if (inject_timeout) {
+        bool injected = false;  // separate flag: the injected expiry must not stop later waits
+        mbar_wait(never, 0, err, injected, 2000000LL);
+      }
       asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
                    :: "r"(tmem + kSfbCol), "l"(desc_sf(base + L::kOffSFB)) : "memory");
       const uint32_t sfb_t = tmem + kSfbCol;
@@ -558,7 +564,7 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
 
 template <int MODE>
 cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
+                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject, cudaStream_t s) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
   const TcPlan p = plan_qmv_tc<MODE>(d, N, K);
@@ -605,7 +611,7 @@ cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, qmv_tc_kernel<MODE>, tmW, tmS, x, gs_w, (int)N, (int)K, p.R, p.split,
-                            p.nslots, p.wslot, p.sslot, y, d.err);
+                            p.nslots, p.wslot, p.sslot, y, d.err, inject);
 }
 
 }  // namespace
@@ -643,9 +649,9 @@ bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nb
 }
 
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
-  if (mode == 2) return launch_mode_tc<2>(d, x, w, scales, gs_w, N, K, y, s);
-  if (mode == 1) return launch_mode_tc<1>(d, x, w, scales, gs_w, N, K, y, s);
+                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject_timeout, cudaStream_t s) {
+  if (mode == 2) return launch_mode_tc<2>(d, x, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 1) return launch_mode_tc<1>(d, x, w, scales, gs_w, N, K, y, inject_timeout, s);
   return cudaErrorInvalidValue;
 }
 

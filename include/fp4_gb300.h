@@ -213,10 +213,12 @@ fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* 
 fp4_status fp4_amax_global_scale_noalloc(const fp4_bf16* x, int64_t n, float* gs_out, float* amax_out,
                                          cudaStream_t stream);
 
-/* Test hook, off by default: when `enable` is nonzero the next qqmm launches
- * make their MMA-issuing thread wait on a barrier nothing arrives at, with a
- * 1 ms limit, before doing its normal work.  The wait expires, the kernel
- * records FP4_ERR_TIMEOUT and still completes; nothing faults or hangs. */
+/* Test hook, off by default: when `enable` is nonzero the next launches of the
+ * tensor-core kernels -- qqmm, qmv's NVFP4/MXFP4 path and gather_qmm -- make
+ * their MMA-issuing thread wait on a barrier nothing arrives at, with a 1 ms
+ * limit, before doing their normal work.  The wait expires, the kernel records
+ * FP4_ERR_TIMEOUT and still completes with a correct result; nothing faults or
+ * hangs. */
 fp4_status fp4_debug_inject_wait_timeout(int enable);
 
 /* Measurement aid (no counterpart on the pages): moves NVFP4 weights from HBM

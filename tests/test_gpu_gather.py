@@ -67,3 +67,19 @@ def test_gather_segments_on_tile_boundaries(B):
                        torch.from_numpy(q3.view(np.int32)).cuda(), torch.from_numpy(s3).cuda())
     ref = oracle.gather_qmm(synth.to_u16(x), lhs, rhs, q3, s3, None, oracle.MODE_MXFP4, 32)
     assert_close_to_oracle(out, ref, "gather tile-boundary segments")
+
+
+def test_gather_timeout_injection_reports_and_recovers(B):
+    B.fp4_check_device_error()
+    B.fp4_debug_inject_wait_timeout(True)
+    try:
+        out, ref = run(B, 16, 4, 2, 64, 128, seed=31)
+        torch.cuda.synchronize()
+        assert B.fp4_check_device_error() == B.FP4_ERR_TIMEOUT
+    finally:
+        B.fp4_debug_inject_wait_timeout(False)
+    assert_close_to_oracle(out, ref, "gather after injected timeout")
+    out, ref = run(B, 16, 4, 2, 64, 128, seed=31)
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    assert_close_to_oracle(out, ref, "gather after recovery")

@@ -167,3 +167,39 @@ def test_weight_stream_ceiling_runs_clean(B):
         B.fp4_debug_stream_weights(q, s)
     torch.cuda.synchronize()
     assert B.fp4_check_device_error() == B.FP4_OK
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+def test_qmv_timeout_injection_reports_and_recovers(B, mode):
+    """The tensor-core GEMV's MMA thread first waits 1 ms on a barrier nothing
+    arrives at: the kernel reports FP4_ERR_TIMEOUT and still returns the right y."""
+    N, K = 512, 2048
+    q, s, b, gs, g = make_weights(mode, N, K, seed=21)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    x = synth.bf16_normal((K,), 1.0, seed=22)
+    ref = oracle.qmv(synth.to_u16(x), q, s, None, mode, g, gs)
+    B.fp4_check_device_error()
+    B.fp4_debug_inject_wait_timeout(True)
+    try:
+        y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
+        torch.cuda.synchronize()
+        assert B.fp4_check_device_error() == B.FP4_ERR_TIMEOUT
+    finally:
+        B.fp4_debug_inject_wait_timeout(False)
+    assert_close_to_oracle(y, ref, f"qmv mode {mode} after injected timeout")
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    assert_close_to_oracle(y, ref, f"qmv mode {mode} after recovery")
+
+
+def test_qmv_nvfp4_extreme_outlier_in_x(B):
+    """One element of x 10^4 times the others: the term expansion's error is
+    bounded by 2^-17 of its slice's max|x| per element, far inside the bar."""
+    N, K = 1024, 5120
+    q, s, b, gs, g = make_weights(2, N, K, seed=23)
+    qd, sd, bd, gsd = to_dev(2, q, s, b, gs)
+    x = synth.bf16_normal((K,), 1.0, seed=24)
+    x[1234] = 1.0e4
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=2)
+    assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs), "nvfp4 x outlier 1e4")
