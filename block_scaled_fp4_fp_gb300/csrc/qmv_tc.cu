@@ -8,16 +8,17 @@
 // The tensor core decodes the weights: W streams by TMA as the block-scaled
 // FP4 A operand of tcgen05.mma.kind::mxf4nvf4 (E4M3 scales per 16, applied by
 // the hardware), so no instruction touches a weight.  The bf16 activation x is
-// written as kTerms = 9 FP4 terms in radix 4 over one power-of-two scale per
+// written as kTerms = 6 FP4 terms in radix 8 over one power-of-two scale per
 // CTA slice of K:
-//     x = 2^e0 * (sum_t d_t 2^(7 - 2t) + r),   d_t in {-2, ..., 2},
-// with max|x| / 2^e0 in [128, 256).  Rounding r_t 2^(2t-7) to the nearest
-// integer and subtracting keeps every digit in [-2, 2] (exact e2m1 codes);
-// the term weights 2^7 ... 2^-9 are exact E4M3 values, and |r| <= 2^-10, at
-// most 2^-17 of max|x|.  The terms are rows 0..8 of the B operand (N = 16;
-// rows 9..15 carry zero scales), so the term-scale tile is one constant tile.
-// The MMA yields D[row, t] = sum_k W[row, k] d_t[k] 2^(7-2t) in fp32 tensor
-// memory; the epilogue forms y = gs_w 2^e0 sum_t D[row, t].
+//     x = 2^e0 * (sum_t d_t 2^(6 - 3t) + r),   d_t in {-4, ..., 4},
+// with max|x| / 2^e0 in [128, 256).  Rounding r_t 2^(3t-6) to the nearest
+// integer and subtracting keeps every digit in [-4, 4]; term t stores d_t / 2
+// (0, +-0.5, ..., +-2: exact e2m1 values) under the term scale 2^(7 - 3t)
+// (2^7 ... 2^-8: exact E4M3 and E8M0 values), and |r| <= 2^-10, at most 2^-17
+// of max|x|.  The terms are rows 0..5 of one 8-row B atom (rows 6, 7 hold zero
+// codes; B rows 8..15 read an all-zero atom), so the term-scale tile is one
+// constant tile.  The MMA yields D[row, t] = sum_k W[row, k] d_t[k] 2^(6-3t)
+// in fp32 tensor memory; the epilogue forms y = gs_w 2^e0 sum_t D[row, t].
 //
 // Work split.  A cluster of `split` CTAs owns R <= 128 consecutive rows; CTA
 // rank i of the cluster takes the i-th slice of the K stages (K = 256 each),
@@ -34,18 +35,19 @@
 //           slots, in flight).  Issued before griddepcontrol.wait (programmatic
 //           dependent launch: W is not written by the kernel this one
 //           overlaps);
-//   warp 1: tensor memory allocation; one thread copies each stage's four
-//           weight-scale tiles to tensor memory (tcgen05.cp) and issues 4 MMAs
-//           (M 128, N 16, K 64) into four independent accumulators, then one
-//           commit that frees the stage's operands.  A-operand rows >= R read
-//           whatever follows the slot; their scales are zero;
-//   warps 2-17: four groups of four warps; group g prepares local stages
-//           i % 4 == g into a ring of kMeta operand slots: the x terms, then,
-//           once the stage's weights have landed, the weights' scales
-//           permuted into the 128x4 tile order tcgen05.cp reads.  A group that
-//           finds operand slot m free again (stage i - kMeta done) passes the
-//           weight slot of that stage back to the TMA producer.  After the
-//           last stage group 0 reads D and forms the partials.
+//   warp 1: tensor memory allocation; one thread issues each stage's
+//           4 MMAs (M 128, N 16, K 64) into four independent accumulators,
+//           then one commit that frees the stage's operands.  A-operand rows
+//           >= R read whatever follows the slot; their scales are zero;
+//   warps 2-17: four groups of four warps (one per tensor-memory lane
+//           quadrant); group g prepares local stages i % 4 == g into a ring of
+//           kMeta operand slots: the x terms in shared memory, then, once the
+//           stage's weights have landed, each thread stores its row's 16
+//           scale bytes straight into the slot's scale columns of tensor
+//           memory (tcgen05.st).  A group that finds operand slot m free again
+//           (stage i - kMeta done) passes the weight slot of that stage back
+//           to the TMA producer.  After the last stage group 0 reads D and
+//           forms the partials.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -58,7 +60,7 @@ namespace fp4 {
 
 namespace {
 
-constexpr int kTerms = 9;           // x expansion terms (B rows 0..8)
+constexpr int kTerms = 6;           // x expansion terms (B rows 0..5)
 constexpr int kMetaMax = 6;         // ring of per-stage MMA operands built by the prep warps, at most
 constexpr int kMaxSlots = 32;       // weight ring slots at most
 constexpr uint32_t kInflightBytes = 128u * 1024u;  // weight bytes a CTA keeps in flight at most
@@ -86,9 +88,9 @@ template <> struct Fmt<2> {
   static constexpr int kMeta = 6;   // operand ring depth
   static constexpr int kGroup = 16;
   static constexpr uint32_t kIdesc = fp4::kIdesc;
-  // E4M3 byte of the term weight 2^(7-2t) (exact: 2^7 ... 2^-9)
+  // E4M3 byte of the term scale 2^(7-3t) (exact: 2^7 ... 2^-8, the last one subnormal)
   __host__ __device__ static constexpr uint32_t term_scale(int t) {
-    return (7 - 2 * t >= -6) ? (uint32_t)((7 - 2 * t + 7) << 3) : (1u << (7 - 2 * t + 9));
+    return (7 - 3 * t >= -6) ? (uint32_t)((7 - 3 * t + 7) << 3) : (1u << (7 - 3 * t + 9));
   }
 };
 template <> struct Fmt<1> {
@@ -96,8 +98,8 @@ template <> struct Fmt<1> {
   static constexpr int kMeta = 4;   // stages are twice as large: a shallower ring keeps kMeta weight slots
   static constexpr int kGroup = 32;
   static constexpr uint32_t kIdesc = fp4::kIdesc | (1u << 23);
-  // E8M0 byte of 2^(7-2t)
-  __host__ __device__ static constexpr uint32_t term_scale(int t) { return (uint32_t)(127 + 7 - 2 * t); }
+  // E8M0 byte of 2^(7-3t)
+  __host__ __device__ static constexpr uint32_t term_scale(int t) { return (uint32_t)(127 + 7 - 3 * t); }
 };
 template <int MODE> struct Geo {
   static constexpr int kCh = Fmt<MODE>::kCh;
@@ -106,13 +108,12 @@ template <int MODE> struct Geo {
   static constexpr int kSB = kBK / Fmt<MODE>::kGroup;             // scale bytes per row per stage
   static constexpr int kTiles = kSB / 4;                         // 128x4 scale tiles per stage
   static constexpr int kSpk = 64 / Fmt<MODE>::kGroup;             // scales per row per k-step
-  static constexpr uint32_t kSFABytes = (uint32_t)kTiles * 512;  // weight-scale tiles of one operand slot
-  static_assert(kSB % 16 == 0, "scale boxes are whole 16-byte rows");
+  static_assert(kSB == 16, "a row brings one 16-byte word of scales per stage: four scale tiles");
   static_assert(kSfaCol + kMeta * kTiles * 4 <= kTmemCols, "scale columns exceed the allocation");
 };
 
-// Shared memory (from a 1024-aligned base): [weight ring | term atoms | term-8
-// atoms | weight-scale tiles | term-scale tile | x slice | partials | barriers].
+// Shared memory (from a 1024-aligned base): [weight ring | term atoms | zero
+// atom | term-scale tile | x slice | partials | barriers].
 // The weight ring is split at launch into code slots and, after them, scale slots.
 constexpr int kMaxKSlice = 17408;  // elements of x per CTA
 constexpr uint32_t kSmemBytes = 227u * 1024u;
@@ -122,13 +123,11 @@ template <int MODE> struct Lay {
   using G = Geo<MODE>;
   static_assert(G::kMeta >= kGroups && G::kMeta <= kMetaMax, "a group's stages must not share an operand slot");
   static constexpr uint32_t kAtoms = G::kMeta * G::kCh;  // term atoms in the operand ring (kCh per slot)
-  static constexpr uint32_t kFixed = 2 * kAtoms * 1024 + G::kMeta * G::kSFABytes + 512 + kMaxKSlice * 2 +
-                                     kRedBytes + kBarBytes + 1024;
+  static constexpr uint32_t kFixed = (kAtoms + 1) * 1024 + 512 + kMaxKSlice * 2 + kRedBytes + kBarBytes + 1024;
   static constexpr uint32_t kRing = (kSmemBytes - kFixed) / 1024u * 1024u;
-  static constexpr uint32_t kOffB = kRing;                   // terms 0..7: atom kCh m + h of slot m
-  static constexpr uint32_t kOffB8 = kOffB + kAtoms * 1024;  // term 8 (+ 7 unused rows), same index
-  static constexpr uint32_t kOffSFA = kOffB8 + kAtoms * 1024;
-  static constexpr uint32_t kOffSFB = kOffSFA + G::kMeta * G::kSFABytes;
+  static constexpr uint32_t kOffB = kRing;                  // B rows 0..7 (terms, 2 zero rows): atom kCh m + h of slot m
+  static constexpr uint32_t kOffZ = kOffB + kAtoms * 1024;  // B rows 8..15 of every stage: zero codes
+  static constexpr uint32_t kOffSFB = kOffZ + 1024;
   static constexpr uint32_t kOffX = kOffSFB + 512;             // x slice (bf16)
   static constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;  // [split][128] fp32 partials (rank 0)
   static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
@@ -186,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   uint64_t* tbar = pbar + 1;  // warp 1 has allocated tensor memory (tmem_slot written)
   uint64_t* never = tbar + 1; // fault injection: a barrier nothing arrives at
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
-  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // kPrep / 32 floats
+  uint32_t* red = tmem_slot + 4;  // kPrep / 32 warp maxima of |x| (bf16 bits)
   float* part = reinterpret_cast<float*>(smem + L::kOffRed);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L::kOffX);
   const uint32_t offS = (uint32_t)nslots * wslot;  // linear-scale slots follow the code slots
@@ -233,6 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     const int row = threadIdx.x >> 2, word = threadIdx.x & 3;
     const uint32_t v = (row < kTerms && word == 0) ? F::term_scale(row) * 0x01010101u : 0u;
     reinterpret_cast<uint32_t*>(smem + L::kOffSFB)[threadIdx.x] = v;
+  }
+  // zero codes: rows 6, 7 (bytes 768..1023) of every term atom, and the zero atom
+  for (uint32_t i = threadIdx.x; i < L::kAtoms * 64 + 256; i += kThreads) {
+    const uint32_t off = i < L::kAtoms * 64 ? (i >> 6) * 1024 + 768 + (i & 63) * 4 : L::kAtoms * 1024 + (i - L::kAtoms * 64) * 4;
+    *reinterpret_cast<uint32_t*>(smem + L::kOffB + off) = 0u;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
@@ -285,19 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       for (int i = 0; i < nst; ++i) {
         mbar_wait(&mfull[m], mround & 1, err, failed);  // the group also saw the weights land
         tc_fence_after();
-        const uint32_t sfa_t = tmem + kSfaCol + 4 * G::kTiles * m;
-        const uint32_t sfa_s = base + L::kOffSFA + m * G::kSFABytes;
-#pragma unroll
-        for (int j = 0; j < G::kTiles; ++j)  // scale tiles start on 4-column boundaries of tensor memory
-          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
-                       :: "r"(sfa_t + 4 * j), "l"(desc_sf(sfa_s + 512 * j)) : "memory");
+        const uint32_t sfa_t = tmem + kSfaCol + 4 * G::kTiles * m;  // 4-column aligned tiles
 #pragma unroll
         for (int j = 0; j < 4 * kCh; ++j) {
           // k-step j (K = 64): chunk h = j / 4, 32 bytes further per k-step along the swizzled rows
           const int h = j >> 2, jj = j & 3;
           const uint64_t adesc = desc_sw128(base + s * wslot + h * wchunk, 1024) + (uint64_t)(2 * jj);
-          // B rows 0..7: the chunk's term atom; rows 8..15: its term-8 atom, L::kAtoms KB further
-          const uint64_t bdesc = desc_sw128(base + L::kOffB + (m * kCh + h) * 1024, L::kAtoms * 1024) + (uint64_t)(2 * jj);
+          // B rows 0..7: the chunk's term atom; rows 8..15: the zero atom
+          const uint32_t batom = L::kOffB + (uint32_t)(m * kCh + h) * 1024;
+          const uint64_t bdesc = desc_sw128(base + batom, L::kOffZ - batom) + (uint64_t)(2 * jj);
           // scale columns j kSpk .. of the stage: tile (j kSpk) / 4, scale-factor id (j kSpk) % 4
           const uint32_t tile = (uint32_t)((j * G::kSpk) >> 2);
           const uint32_t sf_id = (uint32_t)((j * G::kSpk) & 3);
@@ -348,14 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
       m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
     }
-    uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-    if (lane == 0) red[pa >> 5] = __uint_as_float(mb << 16);
+    const uint32_t mb = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
+    if (lane == 0) red[pa >> 5] = mb;
     asm volatile("bar.sync 1, %0;" :: "n"(kPrep) : "memory");  // prep warps only
-    float amax = 0.f;
+    uint32_t mball = 0;
 #pragma unroll
-    for (int i = 0; i < kPrep / 32; ++i) amax = fmaxf(amax, red[i]);
+    for (int i = 0; i < kPrep / 32; ++i) mball = max(mball, red[i]);
+    const float amax = __uint_as_float(mball << 16);
     // e0: max|x| / 2^e0 in [128, 256) (bf16 magnitudes sort as integers; a NaN
     // or infinity in the slice shows as a value above the largest finite one)
     const bool finite = amax <= 3.3895313892515355e38f;
@@ -367,19 +366,25 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     }
     const float pre = ldexpf(1.0f, -e0);
 
+    // tensor memory (warp 1 allocated it at the start): this warp's lane quadrant
+    mbar_wait(tbar, 0, err, failed);
+    tc_fence_after();
+    const int srow = 32 * (warp & 3) + lane;  // the weight row whose scales this thread moves
+    const uint32_t tmem_lane = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16);
     // stage bookkeeping without divisions: operand slot m (round mr), weight slot s (round wr)
     int m = grp, mr = 0, s = grp, wr = 0;
     const int lo = pt & 15, hi4 = ((pt >> 4) & 7) << 4;
     for (int i = grp; i < nst; i += kGroups) {
       if (i >= kMeta) {
         mbar_wait(&mempty[m], (mr - 1) & 1, err, failed);  // operand slot m is free: stage i - kMeta is done
+        tc_fence_after();  // its MMAs have read the slot's scale columns
         if (pt == 0) {
           int sj = s - kMeta;  // weight slot of stage i - kMeta (nslots >= kMeta)
           if (sj < 0) sj += nslots;
           mbar_arrive(&wempty[sj]);
         }
       }
-      // (a) x terms for elements 256 h + 2pt, + 1 of this stage (radix-4 digits, see the header)
+      // (a) x terms for elements 256 h + 2pt, + 1 of this stage (radix-8 digits, see the header)
 #pragma unroll
       for (int h = 0; h < kCh; ++h) {
         const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + i * kBK + h * kChunk + 2 * pt);
@@ -387,35 +392,33 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
         uint8_t* batom = smem + L::kOffB + (m * kCh + h) * 1024;
 #pragma unroll
         for (int t = 0; t < kTerms; ++t) {
-          // d = rint(r / 2^(7-2t)): one fused multiply-add onto 1.5 * 2^23 rounds the
-          // exact product to an integer; subtracting the constant back is exact
-          const float inv = __int_as_float((127 - (7 - 2 * t)) << 23);  // 2^-(7-2t)
-          const float w = __int_as_float((127 + (7 - 2 * t)) << 23);    // 2^(7-2t)
-          const float d0 = __fsub_rn(__fmaf_rn(r0v, inv, 12582912.0f), 12582912.0f);
-          const float d1 = __fsub_rn(__fmaf_rn(r1v, inv, 12582912.0f), 12582912.0f);
-          r0v = __fmaf_rn(-w, d0, r0v);  // exact: |result| <= w / 2
-          r1v = __fmaf_rn(-w, d1, r1v);
-          const uint8_t code = (uint8_t)e2m1x2_rn(d0, d1);  // exact: digits in [-2, 2]
-          // byte pt of term row t (row 0 of the term-8 atom for t = 8), 128-byte swizzle
-          if (t < 8) batom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
-          else batom[L::kAtoms * 1024 + hi4 + lo] = code;
+          // v = d / 2 with d = rint(r / 2^(6-3t)): one fused multiply-add onto 1.5 * 2^22
+          // rounds the exact product r 2^(3t-7) to a multiple of 1/2 (ties to even d);
+          // subtracting the constant back is exact
+          const float inv = __int_as_float((127 + 3 * t - 7) << 23);  // 2^(3t-7)
+          const float w = __int_as_float((127 + 7 - 3 * t) << 23);    // 2^(7-3t), the term scale
+          const float v0 = __fsub_rn(__fmaf_rn(r0v, inv, 6291456.0f), 6291456.0f);
+          const float v1 = __fsub_rn(__fmaf_rn(r1v, inv, 6291456.0f), 6291456.0f);
+          r0v = __fmaf_rn(-w, v0, r0v);  // exact: |result| <= 2^(6-3t) / 2
+          r1v = __fmaf_rn(-w, v1, r1v);
+          const uint8_t code = (uint8_t)e2m1x2_rn(v0, v1);  // exact: v in {0, +-0.5, ..., +-2}
+          // byte pt of term row t, 128-byte swizzle
+          batom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
         }
       }
-      // (b) weight scales of row pt, once the stage has landed: kSB bytes -> word w of
-      // tile w, 16-byte row (pt % 32), slot pt / 32; rows >= rows get 0
+      // (b) weight scales of row srow, once the stage has landed: its 16 scale bytes,
+      // word j -> the four tensor-memory columns of scale tile j of operand slot m (the
+      // MMA reads the column of this lane's quadrant; every one holds the row's
+      // scales).  Rows >= rows get 0.
       mbar_wait(&wfull[s], wr & 1, err, failed);
-      uint8_t* sfa = smem + L::kOffSFA + m * G::kSFABytes;
-      const uint32_t so = (uint32_t)((pt & 31) * 16 + (pt >> 5) * 4);
-#pragma unroll
-      for (int v = 0; v < G::kSB / 16; ++v) {
-        uint4 sv = make_uint4(0, 0, 0, 0);
-        if (pt < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + pt * G::kSB + 16 * v);
-        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 0) * 512 + so) = sv.x;
-        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 1) * 512 + so) = sv.y;
-        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 2) * 512 + so) = sv.z;
-        *reinterpret_cast<uint32_t*>(sfa + (4 * v + 3) * 512 + so) = sv.w;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      uint4 sv = make_uint4(0, 0, 0, 0);
+      if (srow < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + srow * G::kSB);
+      asm volatile(
+          "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %2, %2, %2, %2, %3, %3, %3, %3, %4, %4, %4, %4};"
+          :: "r"(tmem_lane + kSfaCol + 4 * G::kTiles * m), "r"(sv.x), "r"(sv.y), "r"(sv.z), "r"(sv.w) : "memory");
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the term bytes, for the MMA
       mbar_arrive(&mfull[m]);
       m += kGroups;
       if (m >= kMeta) { m -= kMeta; ++mr; }
@@ -429,21 +432,21 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       tc_fence_after();
       tmem = *tmem_slot;
       const int q = warp & 3;
+      // columns 0..7 of the four accumulators (terms 0..5, two zero columns)
+      uint32_t d[4][8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(d[a][0]), "=r"(d[a][1]), "=r"(d[a][2]), "=r"(d[a][3]), "=r"(d[a][4]), "=r"(d[a][5]),
+              "=r"(d[a][6]), "=r"(d[a][7])
+            : "r"(tmem + ((uint32_t)(32 * q) << 16) + 16 * a));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       float dsum[kTerms];
 #pragma unroll
-      for (int t = 0; t < kTerms; ++t) dsum[t] = 0.f;
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        uint32_t d[16];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-            : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]), "=r"(d[7]),
-              "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]), "=r"(d[14]), "=r"(d[15])
-            : "r"(tmem + ((uint32_t)(32 * q) << 16) + 16 * a));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int t = 0; t < kTerms; ++t) dsum[t] += __uint_as_float(d[t]);
-      }
+      for (int t = 0; t < kTerms; ++t)
+        dsum[t] = (__uint_as_float(d[0][t]) + __uint_as_float(d[1][t])) +
+                  (__uint_as_float(d[2][t]) + __uint_as_float(d[3][t]));
       float acc = 0.f;
 #pragma unroll
       for (int t = kTerms - 1; t >= 0; --t) acc += dsum[t];
