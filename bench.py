@@ -136,21 +136,31 @@ def dist_env():
 class DecodeStack:
     """64-layer weight stack in one format, weights resident on the device."""
 
-    def __init__(self, B, mode: int, layers: int, device, fused_qkv: bool = False):
-        """fused_qkv: q, k and v of a layer stored as one [3*5120, 5120] matrix
-        (they multiply the same x), so a layer is 5 GEMVs instead of 7."""
+    def __init__(self, B, mode: int, layers: int, device, layout: str = "split"):
+        """layout "split": one matrix per projection, 7 GEMVs a layer.  "fused":
+        the projections that multiply the same x stored as one matrix, as serving
+        engines store them -- q|k|v as [3*5120, 5120] and gate|up as [2*17408,
+        5120] -- so a layer is 4 GEMVs (qkv, o, gate_up, down) over the same
+        weights (each output slice is that projection's y).  "fused_qkv": only
+        q|k|v fused, 5 GEMVs a layer."""
         self.B, self.mode, self.layers = B, mode, layers
         self.mats = []
         self.bytes = 0
+        projs = list(enumerate(synth.LAYER_PROJECTIONS))  # q, k, v, o, gate, up, down
+        if layout == "split":
+            groups = [[p] for p in range(len(projs))]
+        elif layout == "fused_qkv":
+            groups = [[0, 1, 2], [3], [4], [5], [6]]
+        elif layout == "fused":
+            groups = [[0, 1, 2], [3], [4, 5], [6]]
+        else:
+            raise ValueError(layout)
         for l in range(layers):
-            projs = list(enumerate(synth.LAYER_PROJECTIONS))
-            if fused_qkv:
-                self.mats.append(self._make(3 * synth.HIDDEN, synth.HIDDEN,
-                                            [synth.layer_seed(l, p) for p in range(3)], device))
-                projs = projs[3:]
-            for p, (name, N, K) in projs:
-                seed = synth.layer_seed(l, p)
-                self.mats.append(self._make(N, K, seed, device))
+            for grp in groups:
+                N = sum(projs[p][1][1] for p in grp)
+                K = projs[grp[0]][1][2]
+                seeds = [synth.layer_seed(l, p) for p in grp]
+                self.mats.append(self._make(N, K, seeds if len(grp) > 1 else seeds[0], device))
         self.x = {K: synth.bf16_normal((K,), 1.0, seed=7 + K, device=device)
                   for K in {k for _, _, k in synth.LAYER_PROJECTIONS}}
         self.y = [torch.empty((m["N"],), dtype=torch.bfloat16, device=device) for m in self.mats]
@@ -404,8 +414,9 @@ def run_case(args):
     B.fp4_init(0)
     c = args.case
     if c.startswith("qmv_"):
-        mode = {"qmv_nvfp4": B.MODE_NVFP4, "qmv_mxfp4": B.MODE_MXFP4, "qmv_affine": B.MODE_AFFINE}[c]
-        stack = DecodeStack(B, mode, 4, dev)  # 4 layers: 0.84 GB of weights, well above L2
+        layout = "fused" if c.endswith("_fused") else "split"
+        mode = {"qmv_nvfp4": B.MODE_NVFP4, "qmv_mxfp4": B.MODE_MXFP4, "qmv_affine": B.MODE_AFFINE}[c.replace("_fused", "")]
+        stack = DecodeStack(B, mode, 4, dev, layout=layout)  # 4 layers: 0.84 GB of weights, well above L2
         for _ in range(3):
             stack.step()
     elif c.startswith("qqmm_m"):
@@ -463,14 +474,17 @@ def run_ours(args):
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device)
 
-    modes = [("nvfp4", B.MODE_NVFP4)] + ([] if args.quick else [("mxfp4", B.MODE_MXFP4), ("affine_g64", B.MODE_AFFINE),
-                                                                ("nvfp4_fused_qkv", B.MODE_NVFP4)])
+    # the headline: NVFP4 weights in the fused layout (4 GEMVs a layer); the
+    # per-projection layout and the other formats are components
+    modes = [("nvfp4_fused", B.MODE_NVFP4, "fused")] + (
+        [] if args.quick else [("nvfp4", B.MODE_NVFP4, "split"), ("mxfp4_fused", B.MODE_MXFP4, "fused"),
+                               ("mxfp4", B.MODE_MXFP4, "split"), ("affine_g64", B.MODE_AFFINE, "split")])
     results = {}
     headline = None
-    for name, mode in modes:
-        stack = DecodeStack(B, mode, args.layers, device, fused_qkv=name.endswith("fused_qkv"))
+    for name, mode, layout in modes:
+        stack = DecodeStack(B, mode, args.layers, device, layout=layout)
         graph = capture(stack.step, stream)
-        if name == "nvfp4":
+        if name == "nvfp4_fused":
             with ClockSampler(local) as clk:
                 if ws > 1:
                     torch.distributed.barrier()
@@ -480,13 +494,13 @@ def run_ours(args):
         else:
             ms = time_graph(graph, args.steps, args.warmup, stream)
         results[name] = {"ms_per_step": ms, "GB/s": stack.bytes / ms / 1e6, "bytes_per_step": stack.bytes,
-                         "launches_per_step": stack.launches}
-        if name != "nvfp4":
+                         "launches_per_step": stack.launches, "layout": layout}
+        if name != "nvfp4_fused":
             del stack, graph
             torch.cuda.empty_cache()
 
     stack, graph, ms = headline
-    # the same 448 launches streaming the same weights with no compute
+    # the same launches streaming the same weights with no compute
     sgraph = capture(stack.stream_step, stream)
     stream_ms = time_graph(sgraph, args.steps, args.warmup, stream)
     del sgraph
@@ -552,6 +566,10 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "fp4-e2m1 x bf16, f32 acc", "data": "synthetic",
             "config": {"workload": "decode qmv over a 64-layer hidden-5120 stack (q,k,v,o 5120x5120; gate,up "
                                    "17408x5120; down 5120x17408), NVFP4 g16 weights, bf16 x, one token",
+                       "layout": "q|k|v stored as one [15360, 5120] matrix and gate|up as one [34816, 5120] "
+                                 "matrix (they multiply the same x): 4 GEMVs a layer, the same weights and "
+                                 "outputs; one matrix per projection (7 GEMVs a layer) is "
+                                 "components.decode_qmv.nvfp4",
                        "layers": args.layers, "weight_bytes_per_step": stack.bytes,
                        "tokens_per_s": 1e3 / ms, "l2": "inputs larger than L2 (13.4 GB stack)",
                        "parallelism": f"replicas x{ws}"},
@@ -588,7 +606,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no other formats/components)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
-                    help="profiling case: qmv_nvfp4|qmv_mxfp4|qmv_affine|qqmm_m<M>|quantize|gather")
+                    help="profiling case: qmv_nvfp4[_fused]|qmv_mxfp4[_fused]|qmv_affine|qqmm_m<M>|quantize|gather")
     args = ap.parse_args()
     if args.case:
         run_case(args)

@@ -6,48 +6,52 @@
 // route: x against NVFP4 W stored [N, K]).
 //
 // The tensor core decodes the weights: W streams by TMA as the block-scaled
-// FP4 A operand of tcgen05.mma.kind::mxf4nvf4 (E4M3 scales per 16, applied by
-// the hardware), so no instruction touches a weight.  The bf16 activation x is
-// written as kTerms = 6 FP4 terms in radix 8 over one power-of-two scale per
-// CTA slice of K:
+// FP4 B operand of tcgen05.mma.kind::mxf4nvf4 (E4M3 scales per 16, or E8M0
+// per 32, applied by the hardware), so no instruction touches a weight.  The
+// bf16 activation x is written as kTerms = 6 FP4 terms in radix 8 over one
+// power-of-two scale per CTA slice of K:
 //     x = 2^e0 * (sum_t d_t 2^(6 - 3t) + r),   d_t in {-4, ..., 4},
 // with max|x| / 2^e0 in [128, 256).  Rounding r_t 2^(3t-6) to the nearest
 // integer and subtracting keeps every digit in [-4, 4]; term t stores d_t / 2
 // (0, +-0.5, ..., +-2: exact e2m1 values) under the term scale 2^(7 - 3t)
 // (2^7 ... 2^-8: exact E4M3 and E8M0 values), and |r| <= 2^-10, at most 2^-17
-// of max|x|.  The terms are rows 0..5 of one 8-row B atom (rows 6, 7 hold zero
-// codes; B rows 8..15 read an all-zero atom), so the term-scale tile is one
-// constant tile.  The MMA yields D[row, t] = sum_k W[row, k] d_t[k] 2^(6-3t)
-// in fp32 tensor memory; the epilogue forms y = gs_w 2^e0 sum_t D[row, t].
+// of max|x|.  The terms are rows 0..5 of the A operand (M = 128; rows 6..127
+// feed accumulator lanes nothing reads), the W rows of the CTA are the B
+// operand (N = its row count rounded up to 16, at most 256), so one MMA of
+// K = 64 covers up to 256 rows: the cost of such an MMA barely depends on N.
+// The MMA yields D[t, n] = sum_k d_t[k] 2^(6-3t) W[n, k] in fp32 tensor
+// memory (lane t, column n); the epilogue forms y = gs_w 2^e0 sum_t D[t, n].
 //
-// Work split.  A cluster of `split` CTAs owns R <= 128 consecutive rows; CTA
-// rank i of the cluster takes the i-th slice of the K stages (K = 256 each),
-// so a light problem runs fewer, fuller stages per CTA.  Each CTA sums its
-// slice into fp32 partials; ranks 1.. store theirs into rank 0's shared
-// memory with asynchronous remote stores (distributed shared memory) that a
-// barrier there counts by bytes, and rank 0 adds them in rank order -- the
-// same order on every run -- and writes y.
+// Work split.  A cluster of `split` CTAs owns R <= 256 consecutive rows; CTA
+// rank i of the cluster takes the i-th slice of the K stages (K = 256 each for
+// NVFP4, 512 for MXFP4).  Each CTA sums its slice into fp32 partials; ranks
+// 1.. store theirs into rank 0's shared memory with asynchronous remote stores
+// (distributed shared memory) that a barrier there counts by bytes, and rank 0
+// adds them in rank order -- the same order on every run -- and writes y.
 //   warp 0: barrier setup (one barrier per lane), then the TMA producer: per
-//           stage one box of R rows x 128 bytes of W (128-byte swizzle, so
+//           stage kCh boxes of R rows x 128 bytes of W (128-byte swizzle, so
 //           rows land as the 8-row atoms the MMA reads) and one box of R rows
-//           x 16 bytes of W's linear E4M3 scales, into a ring sized in bytes
-//           (a slot holds ceil(R/8) KB of codes; about 128 KB, at least kMeta
-//           slots, in flight).  Issued before griddepcontrol.wait (programmatic
-//           dependent launch: W is not written by the kernel this one
-//           overlaps);
-//   warp 1: tensor memory allocation; one thread issues each stage's
-//           4 MMAs (M 128, N 16, K 64) into four independent accumulators,
-//           then one commit that frees the stage's operands.  A-operand rows
-//           >= R read whatever follows the slot; their scales are zero;
+//           x 16 bytes of W's linear scales, into a ring sized in bytes (a
+//           slot holds kCh ceil(R/8) KB of codes; about 128 KB, at least
+//           two slots, in flight).  Issued before griddepcontrol.wait
+//           (programmatic dependent launch: W is not written by the kernel
+//           this one overlaps);
+//   warp 1: tensor memory allocation; one thread issues each stage's 4 kCh
+//           MMAs (M 128, N <= 256, K 64) into one accumulator, then one commit
+//           that frees the stage's operands (and, when the ring holds fewer
+//           than kMeta weight slots, a second that frees its weight slot).  B
+//           rows >= R read whatever follows the slot; the accumulator columns
+//           they feed are not read;
 //   warps 2-17: four groups of four warps (one per tensor-memory lane
-//           quadrant); group g prepares local stages i % 4 == g into a ring of
-//           kMeta operand slots: the x terms in shared memory, then, once the
-//           stage's weights have landed, each thread stores its row's 16
-//           scale bytes straight into the slot's scale columns of tensor
-//           memory (tcgen05.st).  A group that finds operand slot m free again
-//           (stage i - kMeta done) passes the weight slot of that stage back
-//           to the TMA producer.  After the last stage group 0 reads D and
-//           forms the partials.
+//           quadrant); group g prepares the stages i % 4 == g in operand slot
+//           g: the x terms in shared memory, then, once the stage's weights
+//           have landed, each warp stores the stage's W scales into the slot's
+//           scale columns of its lane quadrant (tcgen05.st; B row n's scales
+//           sit in lane n % 32, column n / 32 of the k-step's group).  A group
+//           that finds its operand slot free again (stage i - 4 done) passes
+//           the weight slot of that stage back to the TMA producer (when the
+//           ring holds kMeta slots or more).  After the last stage the four
+//           warps of lane quadrant 0 read D's term lanes and form the partials.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -60,34 +64,36 @@ namespace fp4 {
 
 namespace {
 
-constexpr int kTerms = 6;           // x expansion terms (B rows 0..5)
-constexpr int kMetaMax = 6;         // ring of per-stage MMA operands built by the prep warps, at most
+constexpr int kTerms = 6;           // x expansion terms (A rows 0..5)
+constexpr int kMeta = 4;            // operand slots: one per prep group
 constexpr int kMaxSlots = 32;       // weight ring slots at most
 constexpr uint32_t kInflightBytes = 128u * 1024u;  // weight bytes a CTA keeps in flight at most
 constexpr int kChunk = 256;         // codes per TMA box (128 bytes per row)
-constexpr int kRows = 128;          // rows per CTA at most (one M = 128 tile)
-constexpr int kMaxSplit = 8;        // CTAs per cluster at most (portable cluster size)
+constexpr int kRows = 256;          // W rows per CTA at most (MMA N <= 256)
+constexpr int kMaxSplit = 4;        // CTAs per cluster at most (the plan takes 1, 2 or 4)
 constexpr int kGroups = 4;          // prep groups; group g prepares local stages i % kGroups == g
-constexpr int kGroupThreads = 128;  // one group = 4 warps, two elements per thread per stage
+constexpr int kGroupThreads = 128;  // one group = 4 warps, one per lane quadrant
 constexpr int kPrep = kGroups * kGroupThreads;
-constexpr int kThreads = 64 + kPrep;  // TMA warp, MMA warp, prep warps (group 0 also runs the epilogue)
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSfbCol = 64;         // D: four accumulators of 16 columns in [0, 64); term scales
-constexpr uint32_t kSfaCol = 80;         // weight scales of operand slot m: kSfaCol + 16 m + 4 j
-static_assert(kMaxSlots <= 32 && kMetaMax <= 32, "one barrier pair per lane of warp 0");
-// kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, N = 16, M = 128; bit 23 selects E8M0 scales
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr int kThreads = 64 + kPrep;  // TMA warp, MMA warp, prep warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfaCol = 256;   // term scales: one 4-column group
+constexpr uint32_t kSfbCol = 288;   // W scales of operand slot m, k-step group j: kSfbCol + 32 m + 8 j
+                                    // (rows 0..127; rows 128..255 four columns further)
+static_assert(kMeta == kGroups, "group g owns operand slot g");
+static_assert(kSfbCol + kMeta * 32 <= kTmemCols, "scale columns exceed the allocation");
+static_assert(kMaxSlots <= 32 && kMeta <= 32, "one barrier pair per lane of warp 0");
+// kind::mxf4nvf4 descriptor: E2M1 A/B, K-major, M = 128 (N is set per launch); bit 23 selects E8M0 scales
+constexpr uint32_t kIdescM = (1u << 7) | (1u << 10) | ((128u >> 4) << 24);
 
-// Per format: a stage is kCh chunks of 256 elements; a row carries kSB scale
-// bytes per stage, which tcgen05.cp moves as kSB / 4 tiles of 128x4 scales.
-// NVFP4 (E4M3 per 16): k-step j (K = 64) reads tile j; MXFP4 (E8M0 per 32):
-// half j & 1 of tile j / 2, through the scale-factor id.
+// Per format: a stage is kCh chunks of 256 elements; a row carries kSB = 16
+// scale bytes per stage, word j of which covers k-steps (K = 64) j kSpk / 4 ..
+// NVFP4 (E4M3 per 16): k-step j reads word j; MXFP4 (E8M0 per 32): half j & 1
+// of word j / 2, through the scale-factor id.
 template <int MODE> struct Fmt;
 template <> struct Fmt<2> {
   static constexpr int kCh = 1;
-  static constexpr int kMeta = 6;   // operand ring depth
   static constexpr int kGroup = 16;
-  static constexpr uint32_t kIdesc = fp4::kIdesc;
+  static constexpr uint32_t kIdesc = kIdescM;
   // E4M3 byte of the term scale 2^(7-3t) (exact: 2^7 ... 2^-8, the last one subnormal)
   __host__ __device__ static constexpr uint32_t term_scale(int t) {
     return (7 - 3 * t >= -6) ? (uint32_t)((7 - 3 * t + 7) << 3) : (1u << (7 - 3 * t + 9));
@@ -95,47 +101,45 @@ template <> struct Fmt<2> {
 };
 template <> struct Fmt<1> {
   static constexpr int kCh = 2;
-  static constexpr int kMeta = 4;   // stages are twice as large: a shallower ring keeps kMeta weight slots
   static constexpr int kGroup = 32;
-  static constexpr uint32_t kIdesc = fp4::kIdesc | (1u << 23);
+  static constexpr uint32_t kIdesc = kIdescM | (1u << 23);
   // E8M0 byte of 2^(7-3t)
   __host__ __device__ static constexpr uint32_t term_scale(int t) { return (uint32_t)(127 + 7 - 3 * t); }
 };
 template <int MODE> struct Geo {
   static constexpr int kCh = Fmt<MODE>::kCh;
-  static constexpr int kMeta = Fmt<MODE>::kMeta;
-  static constexpr int kBK = 256 * kCh;                          // codes per stage
-  static constexpr int kSB = kBK / Fmt<MODE>::kGroup;             // scale bytes per row per stage
-  static constexpr int kTiles = kSB / 4;                         // 128x4 scale tiles per stage
-  static constexpr int kSpk = 64 / Fmt<MODE>::kGroup;             // scales per row per k-step
-  static_assert(kSB == 16, "a row brings one 16-byte word of scales per stage: four scale tiles");
-  static_assert(kSfaCol + kMeta * kTiles * 4 <= kTmemCols, "scale columns exceed the allocation");
+  static constexpr int kBK = 256 * kCh;               // codes per stage
+  static constexpr int kSB = kBK / Fmt<MODE>::kGroup;  // scale bytes per row per stage
+  static constexpr int kSpk = 64 / Fmt<MODE>::kGroup;  // scales per row per k-step
+  static_assert(kSB == 16, "a row brings one 16-byte word of scales per stage");
 };
 
-// Shared memory (from a 1024-aligned base): [weight ring | term atoms | zero
-// atom | term-scale tile | x slice | partials | barriers].
-// The weight ring is split at launch into code slots and, after them, scale slots.
+// Shared memory (from a 1024-aligned base): [weight ring | term atoms |
+// term-scale tile | x slice | partials | barriers].  The weight ring is split
+// at launch into code slots and, after them, scale slots.  The epilogue reuses
+// the x slice for the term lanes of D.
 constexpr int kMaxKSlice = 17408;  // elements of x per CTA
 constexpr uint32_t kSmemBytes = 227u * 1024u;
 constexpr uint32_t kBarBytes = 1024;
 constexpr uint32_t kRedBytes = kMaxSplit * kRows * 4;
 template <int MODE> struct Lay {
   using G = Geo<MODE>;
-  static_assert(G::kMeta >= kGroups && G::kMeta <= kMetaMax, "a group's stages must not share an operand slot");
-  static constexpr uint32_t kAtoms = G::kMeta * G::kCh;  // term atoms in the operand ring (kCh per slot)
-  static constexpr uint32_t kFixed = (kAtoms + 1) * 1024 + 512 + kMaxKSlice * 2 + kRedBytes + kBarBytes + 1024;
+  static constexpr uint32_t kAtoms = kMeta * G::kCh;  // term atoms: A rows 0..7 of chunk h of slot m
+  static constexpr uint32_t kFixed = kAtoms * 1024 + 512 + kMaxKSlice * 2 + kRedBytes + kBarBytes + 1024;
   static constexpr uint32_t kRing = (kSmemBytes - kFixed) / 1024u * 1024u;
-  static constexpr uint32_t kOffB = kRing;                  // B rows 0..7 (terms, 2 zero rows): atom kCh m + h of slot m
-  static constexpr uint32_t kOffZ = kOffB + kAtoms * 1024;  // B rows 8..15 of every stage: zero codes
-  static constexpr uint32_t kOffSFB = kOffZ + 1024;
-  static constexpr uint32_t kOffX = kOffSFB + 512;             // x slice (bf16)
-  static constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;  // [split][128] fp32 partials (rank 0)
+  static constexpr uint32_t kOffT = kRing;                     // atom kCh m + h
+  static constexpr uint32_t kOffSFA = kOffT + kAtoms * 1024;  // term-scale tile
+  static constexpr uint32_t kOffX = kOffSFA + 512;              // x slice (bf16); later D's term lanes
+  static constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;  // [split][256] fp32 partials (rank 0)
   static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
   static_assert(kOffBar + kBarBytes + 1024 <= kSmemBytes, "shared memory layout overflows");
-  // an MMA reads 16 KB of A from a code chunk's start: that stays inside the allocation
-  static_assert(kRing + 16384 <= kOffBar, "A-operand reads past the allocation");
+  // an MMA reads 128 A rows (16 KB) from a term atom and up to 256 B rows (32 KB)
+  // from a code chunk's start: both stay inside the allocation
+  static_assert(kOffT + (kAtoms - 1) * 1024 + 16384 <= kOffBar, "A-operand reads past the allocation");
+  static_assert(kRing + 32768 <= kOffBar, "B-operand reads past the allocation");
+  static_assert(kTerms * kRows * 4 <= kMaxKSlice * 2, "the term lanes of D fit in the x slice");
 };
-static_assert((2 * kMaxSlots + 2 * kMetaMax + 5) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
+static_assert((2 * kMaxSlots + 2 * kMeta + 5) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -169,7 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   using G = Geo<MODE>;
   using L = Lay<MODE>;
   constexpr int kCh = G::kCh;
-  constexpr int kMeta = G::kMeta;
   constexpr int kBK = G::kBK;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // weight slot landed (TMA bytes)
   uint64_t* wempty = wfull + kMaxSlots;                           // weight slot consumed (relayed)
   uint64_t* mfull = wempty + kMaxSlots;                           // stage operands built (prep group)
-  uint64_t* mempty = mfull + kMetaMax;                            // stage operands consumed (MMA commit)
-  uint64_t* done = mempty + kMetaMax;
+  uint64_t* mempty = mfull + kMeta;                               // stage operands consumed (MMA commit)
+  uint64_t* done = mempty + kMeta;
   uint64_t* xbar = done + 1;
   uint64_t* pbar = xbar + 1;  // rank 0: the other ranks' partials have landed (byte count)
   uint64_t* tbar = pbar + 1;  // warp 1 has allocated tensor memory (tmem_slot written)
@@ -197,10 +200,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   const int nblk = (int)(gridDim.x / (unsigned)split);
   const int r0 = (int)(((int64_t)N * blk) / nblk);
   const int r1 = (int)(((int64_t)N * (blk + 1)) / nblk);
-  const int rows = r1 - r0;  // <= R <= 128
+  const int rows = r1 - r0;  // <= R <= 256
+  const int nmma = (R + 15) & ~15;  // MMA N
   const int nkb = K / kBK;
   const int kb0 = (int)(((int64_t)nkb * rank) / split);
   const int nst = (int)(((int64_t)nkb * (rank + 1)) / split) - kb0;  // this CTA's stages (>= 1)
+  // weight slots go back to the TMA producer through the prep group that reuses the
+  // stage's operand slot (kMeta stages later), or, when the ring holds fewer than
+  // kMeta slots, through a second MMA commit per stage
+  const bool relay = nslots >= kMeta;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) {  // one barrier (pair) per lane
@@ -225,24 +233,17 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   // rank 0 has started and its barriers are initialized.
   __syncwarp();
   if (split > 1) cluster_arrive_relaxed();
-  // The constant term-scale tile: B row t < 9 (tile row t, slot 0) holds the
-  // E4M3 weight 2^(7-2t) for each of the k-step's four 16-element blocks;
-  // rows 9..31 are zero, so B rows 9..15 add nothing.
+  // The constant term-scale tile (A scales): row t < 6 holds the weight
+  // 2^(7-3t) of term t for each of the k-step's four blocks; the other rows
+  // are zero.  tcgen05.cp gives lane t (quadrant 0) these bytes in its column.
   if (threadIdx.x < 128) {
     const int row = threadIdx.x >> 2, word = threadIdx.x & 3;
     const uint32_t v = (row < kTerms && word == 0) ? F::term_scale(row) * 0x01010101u : 0u;
-    reinterpret_cast<uint32_t*>(smem + L::kOffSFB)[threadIdx.x] = v;
-  }
-  // zero codes: rows 6, 7 (bytes 768..1023) of every term atom, and the zero atom
-  for (uint32_t i = threadIdx.x; i < L::kAtoms * 64 + 256; i += kThreads) {
-    const uint32_t off = i < L::kAtoms * 64 ? (i >> 6) * 1024 + 768 + (i & 63) * 4 : L::kAtoms * 1024 + (i - L::kAtoms * 64) * 4;
-    *reinterpret_cast<uint32_t*>(smem + L::kOffB + off) = 0u;
+    reinterpret_cast<uint32_t*>(smem + L::kOffSFA)[threadIdx.x] = v;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
-  uint32_t tmem = 0;  // tensor-memory base: warp 1 after its allocation, group 0 after `done`
   bool failed = false;
-  float partial = 0.f;  // group 0: this CTA's partial y of row 32 (warp & 3) + lane
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (weights)
@@ -275,52 +276,52 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     tc_fence_before();
     __syncwarp();
     tc_fence_after();
-    tmem = *tmem_slot;
-    if (lane == 0) mbar_arrive(tbar);  // releases the tmem_slot write to the epilogue
+    const uint32_t tmem = *tmem_slot;
+    if (lane == 0) mbar_arrive(tbar);  // releases the tmem_slot write to the prep warps
     if (elect_one_sync()) {
       if (inject_timeout) {
         bool injected = false;  // separate flag: the injected expiry must not stop later waits
         mbar_wait(never, 0, err, injected, 2000000LL);
       }
       asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;"
-                   :: "r"(tmem + kSfbCol), "l"(desc_sf(base + L::kOffSFB)) : "memory");
-      const uint32_t sfb_t = tmem + kSfbCol;
-      int m = 0, mround = 0, s = 0;
+                   :: "r"(tmem + kSfaCol), "l"(desc_sf(base + L::kOffSFA)) : "memory");
+      const uint32_t idesc_n = F::kIdesc | ((uint32_t)(nmma >> 3) << 17);
+      int m = 0, s = 0;
       for (int i = 0; i < nst; ++i) {
-        mbar_wait(&mfull[m], mround & 1, err, failed);  // the group also saw the weights land
+        mbar_wait(&mfull[m], (i / kMeta) & 1, err, failed);  // the group also saw the weights land
         tc_fence_after();
-        const uint32_t sfa_t = tmem + kSfaCol + 4 * G::kTiles * m;  // 4-column aligned tiles
+        const uint32_t sfb_t = tmem + kSfbCol + 32 * m;  // 4-column aligned groups
 #pragma unroll
         for (int j = 0; j < 4 * kCh; ++j) {
           // k-step j (K = 64): chunk h = j / 4, 32 bytes further per k-step along the swizzled rows
           const int h = j >> 2, jj = j & 3;
-          const uint64_t adesc = desc_sw128(base + s * wslot + h * wchunk, 1024) + (uint64_t)(2 * jj);
-          // B rows 0..7: the chunk's term atom; rows 8..15: the zero atom
-          const uint32_t batom = L::kOffB + (uint32_t)(m * kCh + h) * 1024;
-          const uint64_t bdesc = desc_sw128(base + batom, L::kOffZ - batom) + (uint64_t)(2 * jj);
-          // scale columns j kSpk .. of the stage: tile (j kSpk) / 4, scale-factor id (j kSpk) % 4
-          const uint32_t tile = (uint32_t)((j * G::kSpk) >> 2);
+          // A: the chunk's term atom (rows 8..127 read the atoms after it); B: the W rows
+          const uint64_t adesc = desc_sw128(base + L::kOffT + (m * kCh + h) * 1024, 1024) + (uint64_t)(2 * jj);
+          const uint64_t bdesc = desc_sw128(base + s * wslot + h * wchunk, 1024) + (uint64_t)(2 * jj);
+          // scale words: group (j kSpk) / 4, scale-factor id (j kSpk) % 4
+          const uint32_t grp = (uint32_t)((j * G::kSpk) >> 2);
           const uint32_t sf_id = (uint32_t)((j * G::kSpk) & 3);
-          const uint32_t idesc = F::kIdesc | (sf_id << 29) | (sf_id << 4);
-          // k-step j accumulates into tile j % 4 of D, so consecutive MMAs of a stage do
-          // not wait on each other; the epilogue adds the four tiles
-          const uint32_t acc = (i > 0 || j >= 4) ? 1u : 0u;
+          const uint32_t idesc = idesc_n | (sf_id << 29) | (sf_id << 4);
+          const uint32_t acc = (i > 0 || j > 0) ? 1u : 0u;
           if (MODE == 2)
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-                :: "r"(tmem + 16 * (j & 3)), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_t + 4 * tile), "r"(sfb_t),
+                :: "r"(tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem + kSfaCol), "r"(sfb_t + 8 * grp),
                    "r"(acc) : "memory");
           else
             asm volatile(
                 "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-                :: "r"(tmem + 16 * (j & 3)), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_t + 4 * tile), "r"(sfb_t),
+                :: "r"(tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem + kSfaCol), "r"(sfb_t + 8 * grp),
                    "r"(acc) : "memory");
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(smem_u32(&mempty[m])) : "memory");
-        if (++m == kMeta) { m = 0; ++mround; }
+        if (!relay)
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                       :: "r"(smem_u32(&wempty[s])) : "memory");
+        if (++m == kMeta) m = 0;
         if (++s == nslots) s = 0;
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -329,11 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   } else {
     // ------------------------------------------- prep warps (2..17), then epilogue
     const int pa = threadIdx.x - 64;           // 0..kPrep-1
-    const int grp = pa / kGroupThreads;        // prep group
+    const int grp = pa / kGroupThreads;        // prep group = operand slot
     const int pt = pa % kGroupThreads;         // thread within the group
     if (split > 1 && rank > 0) cluster_wait();  // (see the arrival after the barrier inits)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // this CTA's slice of x (bf16, nst * 512 bytes) -> shared memory in one bulk copy
+    // this CTA's slice of x (bf16, nst * kBK * 2 bytes) -> shared memory in one bulk copy
     const uint32_t xbytes = (uint32_t)nst * (kBK * 2);
     if (pa == 0) {
       mbar_arrive_expect_tx(xbar, xbytes);
@@ -369,16 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     // tensor memory (warp 1 allocated it at the start): this warp's lane quadrant
     mbar_wait(tbar, 0, err, failed);
     tc_fence_after();
-    const int srow = 32 * (warp & 3) + lane;  // the weight row whose scales this thread moves
-    const uint32_t tmem_lane = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16);
-    // stage bookkeeping without divisions: operand slot m (round mr), weight slot s (round wr)
-    int m = grp, mr = 0, s = grp, wr = 0;
+    const uint32_t tmem = *tmem_slot;
+    const int q4 = warp & 3;
+    const uint32_t sfb_lane = tmem + ((uint32_t)(32 * q4) << 16) + kSfbCol + 32 * grp;
+    // stage bookkeeping: weight slot s (round wr) of stage i (the ring may hold
+    // fewer slots than there are groups)
+    int s = grp % nslots, wr = grp / nslots;
     const int lo = pt & 15, hi4 = ((pt >> 4) & 7) << 4;
     for (int i = grp; i < nst; i += kGroups) {
       if (i >= kMeta) {
-        mbar_wait(&mempty[m], (mr - 1) & 1, err, failed);  // operand slot m is free: stage i - kMeta is done
-        tc_fence_after();  // its MMAs have read the slot's scale columns
-        if (pt == 0) {
+        mbar_wait(&mempty[grp], ((i / kMeta) - 1) & 1, err, failed);  // stage i - kMeta is done
+        tc_fence_after();  // its MMAs have read the slot's terms and scale columns
+        if (relay && pt == 0) {
           int sj = s - kMeta;  // weight slot of stage i - kMeta (nslots >= kMeta)
           if (sj < 0) sj += nslots;
           mbar_arrive(&wempty[sj]);
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       for (int h = 0; h < kCh; ++h) {
         const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + i * kBK + h * kChunk + 2 * pt);
         float r0v = bf16_lo(xv) * pre, r1v = bf16_hi(xv) * pre;
-        uint8_t* batom = smem + L::kOffB + (m * kCh + h) * 1024;
+        uint8_t* tatom = smem + L::kOffT + (grp * kCh + h) * 1024;
 #pragma unroll
         for (int t = 0; t < kTerms; ++t) {
           // v = d / 2 with d = rint(r / 2^(6-3t)): one fused multiply-add onto 1.5 * 2^22
@@ -402,72 +405,109 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
           r0v = __fmaf_rn(-w, v0, r0v);  // exact: |result| <= 2^(6-3t) / 2
           r1v = __fmaf_rn(-w, v1, r1v);
           const uint8_t code = (uint8_t)e2m1x2_rn(v0, v1);  // exact: v in {0, +-0.5, ..., +-2}
-          // byte pt of term row t, 128-byte swizzle
-          batom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
+          // byte pt of A row t, 128-byte swizzle
+          tatom[t * 128 + ((hi4 ^ (t << 4))) + lo] = code;
         }
       }
-      // (b) weight scales of row srow, once the stage has landed: its 16 scale bytes,
-      // word j -> the four tensor-memory columns of scale tile j of operand slot m (the
-      // MMA reads the column of this lane's quadrant; every one holds the row's
-      // scales).  Rows >= rows get 0.
+      // (b) the stage's W scales, once it has landed.  B row n's scale word j sits in
+      // lane n % 32 (written in every lane quadrant), column 8j + n / 32 for rows
+      // 0..127 and 8j + 4 + (n - 128) / 32 for rows 128..255; this thread moves
+      // rows 32c + lane (c = 0..7).  Rows >= rows get 0.
+      if (!relay && i >= nslots) {
+        // the slot's previous stage (i - nslots) is done with it, so the producer has
+        // (or will have) issued this stage's load and wfull[s] is at most one phase
+        // behind the phase waited for below
+        const int ip = i - nslots;
+        mbar_wait(&mempty[ip % kMeta], (ip / kMeta) & 1, err, failed);
+      }
       mbar_wait(&wfull[s], wr & 1, err, failed);
-      uint4 sv = make_uint4(0, 0, 0, 0);
-      if (srow < rows) sv = *reinterpret_cast<const uint4*>(smem + offS + s * sslot + srow * G::kSB);
+      const uint8_t* sc = smem + offS + s * sslot;
+      uint4 v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int row = 32 * c + lane;
+        v[c] = row < rows ? *reinterpret_cast<const uint4*>(sc + row * G::kSB) : make_uint4(0, 0, 0, 0);
+      }
       asm volatile(
-          "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %2, %2, %2, %2, %3, %3, %3, %3, %4, %4, %4, %4};"
-          :: "r"(tmem_lane + kSfaCol + 4 * G::kTiles * m), "r"(sv.x), "r"(sv.y), "r"(sv.z), "r"(sv.w) : "memory");
+          "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+          "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+          :: "r"(sfb_lane), "r"(v[0].x), "r"(v[1].x), "r"(v[2].x), "r"(v[3].x), "r"(v[4].x), "r"(v[5].x), "r"(v[6].x),
+             "r"(v[7].x), "r"(v[0].y), "r"(v[1].y), "r"(v[2].y), "r"(v[3].y), "r"(v[4].y), "r"(v[5].y), "r"(v[6].y),
+             "r"(v[7].y), "r"(v[0].z), "r"(v[1].z), "r"(v[2].z), "r"(v[3].z), "r"(v[4].z), "r"(v[5].z), "r"(v[6].z),
+             "r"(v[7].z), "r"(v[0].w), "r"(v[1].w), "r"(v[2].w), "r"(v[3].w), "r"(v[4].w), "r"(v[5].w), "r"(v[6].w),
+             "r"(v[7].w) : "memory");
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the term bytes, for the MMA
-      mbar_arrive(&mfull[m]);
-      m += kGroups;
-      if (m >= kMeta) { m -= kMeta; ++mr; }
+      mbar_arrive(&mfull[grp]);
       s += kGroups;
-      if (s >= nslots) { s -= nslots; ++wr; }
+      while (s >= nslots) { s -= nslots; ++wr; }
     }
-    // ---- epilogue (group 0, warps 2..5 = lane quadrants 2, 3, 0, 1): partial = 2^e0 sum_t D[row, t]
-    if (grp == 0) {
-      mbar_wait(tbar, 0, err, failed);
+    // ---- epilogue: the lane-quadrant-0 warps (one per group) each take 64
+    // columns of D: lanes 0..5 hold the terms of a column; they go through
+    // shared memory (the x slice, no longer read) and each thread adds one
+    // column's six terms.  partial = 2^e0 sum_t D[t, n].
+    if (q4 == 0) {
       mbar_wait(done, 0, err, failed);
       tc_fence_after();
-      tmem = *tmem_slot;
-      const int q = warp & 3;
-      // columns 0..7 of the four accumulators (terms 0..5, two zero columns)
-      uint32_t d[4][8];
+      float* dt = reinterpret_cast<float*>(xs);  // [kTerms][kRows]
+      const int c0 = 64 * grp;
+      if (c0 < nmma) {
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-            : "=r"(d[a][0]), "=r"(d[a][1]), "=r"(d[a][2]), "=r"(d[a][3]), "=r"(d[a][4]), "=r"(d[a][5]),
-              "=r"(d[a][6]), "=r"(d[a][7])
-            : "r"(tmem + ((uint32_t)(32 * q) << 16) + 16 * a));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      float dsum[kTerms];
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = c0 + 16 * cc;
+          if (c < nmma) {  // warp-uniform
+            uint32_t d[16];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]), "=r"(d[7]),
+                  "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]), "=r"(d[14]), "=r"(d[15])
+                : "r"(tmem + (uint32_t)c));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (lane < kTerms) {
+              uint4* dst = reinterpret_cast<uint4*>(dt + lane * kRows + c);
 #pragma unroll
-      for (int t = 0; t < kTerms; ++t)
-        dsum[t] = (__uint_as_float(d[0][t]) + __uint_as_float(d[1][t])) +
-                  (__uint_as_float(d[2][t]) + __uint_as_float(d[3][t]));
-      float acc = 0.f;
+              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(d[4 * v], d[4 * v + 1], d[4 * v + 2], d[4 * v + 3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      float partial[2];
 #pragma unroll
-      for (int t = kTerms - 1; t >= 0; --t) acc += dsum[t];
-      partial = finite ? ldexpf(acc, e0) : __int_as_float(0x7FC00000);
-      const int row = 32 * q + lane;
+      for (int k = 0; k < 2; ++k) {
+        const int n = c0 + lane + 32 * k;
+        float acc = 0.f;
+        if (n < rows) {
+#pragma unroll
+          for (int t = kTerms - 1; t >= 0; --t) acc += dt[t * kRows + n];
+        }
+        partial[k] = finite ? ldexpf(acc, e0) : __int_as_float(0x7FC00000);
+      }
       if (rank > 0) {
-        // asynchronous store into rank 0's partials; its barrier counts the bytes
-        if (row < rows)
-          asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
-                       :: "r"(map_rank(part + rank * kRows + row, 0)), "r"(__float_as_uint(partial)),
-                          "r"(map_rank(pbar, 0)) : "memory");
+        // asynchronous stores into rank 0's partials; its barrier counts the bytes
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int n = c0 + lane + 32 * k;
+          if (n < rows)
+            asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                         :: "r"(map_rank(part + rank * kRows + n, 0)), "r"(__float_as_uint(partial[k])),
+                            "r"(map_rank(pbar, 0)) : "memory");
+        }
       } else {
         if (split > 1) {
-          if (pa == 0) mbar_arrive_expect_tx(pbar, (uint32_t)(split - 1) * (uint32_t)rows * 4u);
+          if (grp == 0 && lane == 0) mbar_arrive_expect_tx(pbar, (uint32_t)(split - 1) * (uint32_t)rows * 4u);
           mbar_wait(pbar, 0, err, failed);  // every other rank's partials have landed
         }
-        if (row < rows) {
-          float acc_y = partial;
-          for (int c = 1; c < split; ++c) acc_y += part[c * kRows + row];
-          const float g = gs_w ? __ldg(gs_w) : 1.0f;
-          y[r0 + row] = (uint16_t)f32_to_bf16_rn(acc_y * g);
+        const float g = gs_w ? __ldg(gs_w) : 1.0f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int n = c0 + lane + 32 * k;
+          if (n < rows) {
+            float acc_y = partial[k];
+            for (int c = 1; c < split; ++c) acc_y += part[c * kRows + n];
+            y[r0 + n] = (uint16_t)f32_to_bf16_rn(acc_y * g);
+          }
         }
       }
     }
@@ -476,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(*tmem_slot), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -523,21 +563,26 @@ struct TcPlan {
   uint32_t sslot = 0;  // bytes of linear scales per slot
 };
 
-// Choose the K split: per CTA the time is about (stages) x max(fixed issue cost
-// of a stage, the stage's bytes at an even share of HBM bandwidth); the split
-// with the smallest estimate wins (ties go to the smaller split).
+// Choose the row blocks and the K split (1, 2 or 4 CTAs per cluster: clusters
+// of 3, 5 or more measured slower to schedule).  A CTA's time is about the
+// larger of its MMA issue time (stages x about 0.2 us per 4 MMAs of K = 64,
+// whatever N) and its bytes at an even share of HBM bandwidth among the CTAs
+// (capped at what one SM draws), plus a small cost per stage and a fixed cost
+// for a cluster launch and the partial exchange; the plan with the smallest
+// estimate wins (ties go to the smaller split).  The weight ring holds about
+// 128 KB in flight, at least kMeta slots if it can (for the slot relay) and
+// at least two.
 template <int MODE>
 TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
   using G = Geo<MODE>;
   constexpr int kCh = G::kCh;
-  constexpr int kMeta = G::kMeta;
   constexpr int kBK = G::kBK;
   TcPlan best;
   if (K % kBK != 0 || N < 1 || d.sm_count < 1) return best;
   const int64_t nkb = K / kBK;
-  const double stage_us = 0.2 * kCh, sm_gbs = 43.0;
+  const double stage_us = 0.2 * kCh, hbm_gbs = 6500.0, sm_gbs = 80.0, per_stage_us = 0.05, cluster_us = 0.6;
   double best_cost = 0.0;
-  for (int split = 1; split <= kMaxSplit; ++split) {
+  for (int split : {1, 2, 4}) {
     if (nkb < split) break;
     const int64_t nst = (nkb + split - 1) / split;
     if (nst * kBK > kMaxKSlice) continue;
@@ -546,22 +591,27 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
     if (nblk < 1) continue;
     const int64_t R = (N + nblk - 1) / nblk;
     if (R > kRows) continue;
-    const double cost = (double)nst * std::max(stage_us, (double)R * (128.0 * kCh + G::kSB) / (sm_gbs * 1e3));
+    const uint32_t wslot = (uint32_t)kCh * (uint32_t)((R + 7) / 8) * 1024u;
+    const uint32_t sslot = ((uint32_t)R * G::kSB + 127u) / 128u * 128u;
+    if (Lay<MODE>::kRing / (wslot + sslot) < 2u) continue;
+    const double bw = std::min(sm_gbs, hbm_gbs / (double)(nblk * split));
+    const double bytes = (double)nst * (double)R * (128.0 * kCh + G::kSB);
+    const double cost = std::max((double)nst * stage_us, bytes / (bw * 1e3)) + (double)nst * per_stage_us +
+                        (split > 1 ? cluster_us : 0.0);
     if (best.split == 0 || cost < best_cost) {
       best_cost = cost;
       best.split = split;
       best.nblk = (int)nblk;
       best.R = (int)R;
+      best.wslot = wslot;
+      best.sslot = sslot;
     }
   }
   if (best.split == 0) return best;
-  best.wslot = (uint32_t)kCh * (uint32_t)((best.R + 7) / 8) * 1024u;
-  best.sslot = ((uint32_t)best.R * G::kSB + 127u) / 128u * 128u;
   // deeper than about 128 KB only lengthens the queues in front of the first stages
   const uint32_t slot = best.wslot + best.sslot;
   best.nslots = (int)std::min<uint32_t>(kMaxSlots, Lay<MODE>::kRing / slot);
   best.nslots = std::max<int>(std::min<int>(best.nslots, kMeta), std::min<int>(best.nslots, kInflightBytes / slot));
-  if (best.nslots < kMeta) best.split = 0;  // the slot relay needs nslots >= kMeta
   return best;
 }
 

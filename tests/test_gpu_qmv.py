@@ -157,6 +157,37 @@ def test_qmv_decode_layer_shapes_sampled(B, mode, proj):
     assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"{name} mode {mode}")
 
 
+@pytest.mark.parametrize("mode", [2, 1])
+def test_qmv_fp4_wide_row_blocks_every_row(B, mode):
+    """Row blocks above 128 rows (W rows are the MMA's N, up to 256 per CTA):
+    [34816, 2048] puts 230 rows in each of 152 blocks.  For MXFP4 a weight slot
+    is then ~62 KB, the ring holds two, and the MMA commits free them (the
+    path where the ring holds fewer slots than there are prep groups)."""
+    N, K = 34816, 2048
+    q, s, b, gs, g = make_weights(mode, N, K, seed=31 + mode)
+    x = synth.activations_with_outliers(1, K, seed=5).view(-1)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
+    assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, mode, g, gs), f"mode {mode} {N}x{K}")
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("N", [3 * synth.HIDDEN, 2 * 17408])
+def test_qmv_fused_decode_shapes_sampled(B, mode, N):
+    """The fused decode projections (q|k|v [15360, 5120], gate|up [34816, 5120])
+    in the launch configuration the bench uses; the oracle checks a seeded
+    sample of rows, including the first and last of the matrix."""
+    K = synth.HIDDEN
+    q, s, b, gs, g = make_weights(mode, N, K, seed=N + mode)
+    x = synth.bf16_normal((K,), 1.0, seed=98)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode)
+    rows = np.unique(np.concatenate([np.arange(8), N - 1 - np.arange(8),
+                                     np.random.default_rng(N).integers(0, N, 240)]))
+    ref = oracle.qmv(synth.to_u16(x), q, s, None, mode, g, gs, rows=rows)
+    assert_close_to_oracle(y[torch.from_numpy(rows).cuda()], ref, f"fused {N}x{K} mode {mode}")
+
+
 def test_weight_stream_ceiling_runs_clean(B):
     """The stream-only measurement kernel reads the decode shapes' weights as the
     tensor-core path does and leaves no device error behind."""
