@@ -139,7 +139,7 @@ template <int MODE> struct Lay {
   static_assert(kRing + 32768 <= kOffBar, "B-operand reads past the allocation");
   static_assert(kTerms * kRows * 4 <= kMaxKSlice * 2, "the term lanes of D fit in the x slice");
 };
-static_assert((2 * kMaxSlots + 2 * kMeta + 5) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
+static_assert((2 * kMaxSlots + 2 * kMeta + 4) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) |
@@ -183,8 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   uint64_t* mfull = wempty + kMaxSlots;                           // stage operands built (prep group)
   uint64_t* mempty = mfull + kMeta;                               // stage operands consumed (MMA commit)
   uint64_t* done = mempty + kMeta;
-  uint64_t* xbar = done + 1;
-  uint64_t* pbar = xbar + 1;  // rank 0: the other ranks' partials have landed (byte count)
+  uint64_t* pbar = done + 1;  // rank 0: the other ranks' partials have landed (byte count)
   uint64_t* tbar = pbar + 1;  // warp 1 has allocated tensor memory (tmem_slot written)
   uint64_t* never = tbar + 1; // fault injection: a barrier nothing arrives at
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
@@ -222,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     }
     if (lane == 0) {
       mbar_init(done, 1);
-      mbar_init(xbar, 1);
       mbar_init(pbar, 1);
       mbar_init(tbar, 1);
       mbar_init(never, 1);
@@ -334,16 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     const int pt = pa % kGroupThreads;         // thread within the group
     if (split > 1 && rank > 0) cluster_wait();  // (see the arrival after the barrier inits)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // this CTA's slice of x (bf16, nst * kBK * 2 bytes) -> shared memory in one bulk copy
-    const uint32_t xbytes = (uint32_t)nst * (kBK * 2);
-    if (pa == 0) {
-      mbar_arrive_expect_tx(xbar, xbytes);
-      bulk_load(xs, x + (int64_t)kb0 * kBK, xbytes, xbar);
-    }
-    mbar_wait(xbar, 0, err, failed);
+    // this CTA's slice of x (bf16, nst * kBK * 2 bytes) -> shared memory and its max|x|,
+    // by ordinary loads: a bulk copy would queue behind the weight boxes already in
+    // flight from this SM
+    const uint4* xg = reinterpret_cast<const uint4*>(x + (int64_t)kb0 * kBK);
     uint32_t m2 = 0;
     for (int v = pa; v < nst * (kBK / 8); v += kPrep) {
-      const uint4 q = reinterpret_cast<const uint4*>(xs)[v];
+      const uint4 q = __ldg(xg + v);
+      reinterpret_cast<uint4*>(xs)[v] = q;
       m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
       m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
       m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
@@ -351,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     }
     const uint32_t mb = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
     if (lane == 0) red[pa >> 5] = mb;
-    asm volatile("bar.sync 1, %0;" :: "n"(kPrep) : "memory");  // prep warps only
+    asm volatile("bar.sync 1, %0;" :: "n"(kPrep) : "memory");  // prep warps only; x is in shared memory
     uint32_t mball = 0;
 #pragma unroll
     for (int i = 0; i < kPrep / 32; ++i) mball = max(mball, red[i]);
@@ -452,23 +448,24 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       tc_fence_after();
       float* dt = reinterpret_cast<float*>(xs);  // [kTerms][kRows]
       const int c0 = 64 * grp;
-      if (c0 < nmma) {
+      if (c0 < nmma) {  // warp-uniform; chunks at or past nmma hold nothing this CTA reads
+        uint32_t d[4][16];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = c0 + 16 * cc;
-          if (c < nmma) {  // warp-uniform
-            uint32_t d[16];
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-                : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]), "=r"(d[7]),
-                  "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]), "=r"(d[14]), "=r"(d[15])
-                : "r"(tmem + (uint32_t)c));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (lane < kTerms) {
-              uint4* dst = reinterpret_cast<uint4*>(dt + lane * kRows + c);
+        for (int cc = 0; cc < 4; ++cc)
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+              : "=r"(d[cc][0]), "=r"(d[cc][1]), "=r"(d[cc][2]), "=r"(d[cc][3]), "=r"(d[cc][4]), "=r"(d[cc][5]),
+                "=r"(d[cc][6]), "=r"(d[cc][7]), "=r"(d[cc][8]), "=r"(d[cc][9]), "=r"(d[cc][10]), "=r"(d[cc][11]),
+                "=r"(d[cc][12]), "=r"(d[cc][13]), "=r"(d[cc][14]), "=r"(d[cc][15])
+              : "r"(tmem + (uint32_t)(c0 + 16 * cc)));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (lane < kTerms) {
 #pragma unroll
-              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(d[4 * v], d[4 * v + 1], d[4 * v + 2], d[4 * v + 3]);
-            }
+          for (int cc = 0; cc < 4; ++cc) {
+            uint4* dst = reinterpret_cast<uint4*>(dt + lane * kRows + c0 + 16 * cc);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(d[cc][4 * v], d[cc][4 * v + 1], d[cc][4 * v + 2], d[cc][4 * v + 3]);
           }
         }
       }
