@@ -418,20 +418,35 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       }
       mbar_wait(&wfull[s], wr & 1, err, failed);
       const uint8_t* sc = smem + offS + s * sslot;
-      uint4 v[8];
+      if (nmma > 128) {  // warp-uniform
+        uint4 v[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int row = 32 * c + lane;
-        v[c] = row < rows ? *reinterpret_cast<const uint4*>(sc + row * G::kSB) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 8; ++c) {
+          const int row = 32 * c + lane;
+          v[c] = row < rows ? *reinterpret_cast<const uint4*>(sc + row * G::kSB) : make_uint4(0, 0, 0, 0);
+        }
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+            "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+            :: "r"(sfb_lane), "r"(v[0].x), "r"(v[1].x), "r"(v[2].x), "r"(v[3].x), "r"(v[4].x), "r"(v[5].x), "r"(v[6].x),
+               "r"(v[7].x), "r"(v[0].y), "r"(v[1].y), "r"(v[2].y), "r"(v[3].y), "r"(v[4].y), "r"(v[5].y), "r"(v[6].y),
+               "r"(v[7].y), "r"(v[0].z), "r"(v[1].z), "r"(v[2].z), "r"(v[3].z), "r"(v[4].z), "r"(v[5].z), "r"(v[6].z),
+               "r"(v[7].z), "r"(v[0].w), "r"(v[1].w), "r"(v[2].w), "r"(v[3].w), "r"(v[4].w), "r"(v[5].w), "r"(v[6].w),
+               "r"(v[7].w) : "memory");
+      } else {  // N <= 128: the MMA reads only the first four columns of each group
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = 32 * c + lane;
+          v[c] = row < rows ? *reinterpret_cast<const uint4*>(sc + row * G::kSB) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(v);  // word j of row c at w[4 c + j]
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(sfb_lane + 8 * j), "r"(w[j]), "r"(w[4 + j]), "r"(w[8 + j]), "r"(w[12 + j]) : "memory");
+        }
       }
-      asm volatile(
-          "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-          "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-          :: "r"(sfb_lane), "r"(v[0].x), "r"(v[1].x), "r"(v[2].x), "r"(v[3].x), "r"(v[4].x), "r"(v[5].x), "r"(v[6].x),
-             "r"(v[7].x), "r"(v[0].y), "r"(v[1].y), "r"(v[2].y), "r"(v[3].y), "r"(v[4].y), "r"(v[5].y), "r"(v[6].y),
-             "r"(v[7].y), "r"(v[0].z), "r"(v[1].z), "r"(v[2].z), "r"(v[3].z), "r"(v[4].z), "r"(v[5].z), "r"(v[6].z),
-             "r"(v[7].z), "r"(v[0].w), "r"(v[1].w), "r"(v[2].w), "r"(v[3].w), "r"(v[4].w), "r"(v[5].w), "r"(v[6].w),
-             "r"(v[7].w) : "memory");
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the term bytes, for the MMA
