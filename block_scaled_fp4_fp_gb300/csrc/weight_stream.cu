@@ -4,7 +4,7 @@
 // (codes [N, K/2] bytes and linear E4M3 scales [N, K/16]) from HBM into shared
 // memory the way the tensor-core qmv does -- one TMA box of R rows x 128 bytes
 // of codes and one of R rows x 16 bytes of scales per K = 256 stage, a ring of
-// slots holding at most about 128 KB, the same split of K over the CTAs of a
+// slots holding what the GEMV's plan holds, the same split of K over the CTAs of a
 // row block and the same rows per CTA, one CTA per SM, programmatic dependent
 // launch with consumption after griddepcontrol.wait -- and computes nothing.
 // Timed over the same weights, it is the launch-and-stream ceiling the GEMV
