@@ -7,19 +7,23 @@
 // are dequantized by producer warps in shared memory before bf16 tensor-core
 // MMAs).
 //
-// Design: rows arrive sorted by expert.  Each CTA owns one 128-row tile of one
-// expert's segment (tiles never straddle experts; the tile -> expert map is
-// rebuilt in every CTA by binary searches over the sorted expert ids, so no
-// workspace is needed) and one 256-column slice of N.  Per K = 64 stage:
-//   * 16 producer warps gather the 128 activation rows with cp.async (16 bytes
-//     per copy, written in the 128-byte-swizzled K-major layout) and dequantize
-//     the 256 x 64 weight slice exactly to bf16 (e2m1 * 2^(byte-127)) into the
-//     same layout; each thread's weight codes and scales are loaded kPD stages
-//     ahead into registers;
-//   * one thread issues tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulator
-//     in tensor memory, M 128, N 256, K 16 per instruction);
-//   * after the last stage warps 0-3 read the accumulator (tcgen05.ld) and
-//     store bf16 rows of `out` in routed-row order.
+// Design: rows arrive sorted by expert.  Each CTA owns one tile of up to 256
+// rows of one expert's segment (tiles never straddle experts; the tile ->
+// expert map is rebuilt in every CTA by binary searches over the sorted expert
+// ids, so no workspace is needed) and one 256-column slice of N.  Per K = 64
+// stage:
+//   * 16 producer warps gather the tile's activation rows with cp.async (16
+//     bytes per copy, written in the 128-byte-swizzled K-major layout) and
+//     dequantize the 256 x 64 weight slice exactly to bf16 (e2m1 *
+//     2^(byte-127)) into the same layout, once for both 128-row halves of the
+//     tile; each thread's weight codes and scales are loaded kPD stages ahead
+//     into registers;
+//   * one thread issues tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulators
+//     in tensor memory, M 128, N 256, K 16 per instruction): one MMA per half
+//     that holds rows, each into its own 256-column accumulator;
+//   * after the last stage warps 0-7 (lane quadrant warp % 4, half warp / 4)
+//     read the accumulators (tcgen05.ld) and store bf16 rows of `out` in
+//     routed-row order.
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,19 +33,21 @@ namespace fp4 {
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                // rows per MMA (one accumulator)
+constexpr int TM = 2 * BM;             // rows per tile: two MMA halves share each weight slice
 constexpr int BN = 256;
 constexpr int BK = 64;                 // bf16 elements per stage row: 128 bytes
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int kProducerWarps = 16;
 constexpr int kPD = 2;                 // weight prefetch distance (stages) in the producers' registers
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;  // + MMA warp
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t A_HALF = BM * BK * 2;   // 16 KB: one 128-row half of the activations
+constexpr uint32_t A_BYTES = 2 * A_HALF;   // 32 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 2048;
+constexpr uint32_t TMEM_COLS = 512;        // accumulator of half h at column 256 h
 // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, K-major, N>>3, M>>4
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(BM >> 4) << 24);
@@ -73,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   uint64_t* never = bars + 2 * STAGES + 1;  // fault injection: a barrier nothing arrives at
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
   int* tile_info = reinterpret_cast<int*>(bars + 2 * STAGES + 3);  // expert, row0, rows
-  int* row_src = tile_info + 4;                                     // 128 activation rows
+  int* row_src = tile_info + 4;                                     // TM activation rows
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -94,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
         while (lo < hi) { const int mid = (lo + hi) >> 1; if (__ldg(rhs + mid) < e + 1) lo = mid + 1; else hi = mid; }
         hi_b = lo;
       }
-      const int tiles = (hi_b - lo_b + BM - 1) / BM;
+      const int tiles = (hi_b - lo_b + TM - 1) / TM;
       int incl = tiles;
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -105,12 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
       const unsigned hit = __ballot_sync(0xffffffffu, mine);
       if (hit) {
         const int src = __ffs(hit) - 1;
-        const int r0 = lo_b + (tile_id - excl) * BM;
+        const int r0 = lo_b + (tile_id - excl) * TM;
         const int re = __shfl_sync(0xffffffffu, r0, src);
         const int rend = __shfl_sync(0xffffffffu, hi_b, src);
         fe = e0 + src;
         frow = re;
-        frows = min(BM, rend - re);
+        frows = min(TM, rend - re);
         found = 1;
       }
       prefix += __shfl_sync(0xffffffffu, incl, 31);
@@ -134,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   const int expert = tile_info[0];
   if (expert < 0) return;  // uniform: this grid slot has no tile
   const int row0 = tile_info[1], rows = tile_info[2];
-  for (int r = threadIdx.x; r < BM; r += blockDim.x) row_src[r] = (r < rows) ? __ldg(lhs + row0 + r) : 0;
+  for (int r = threadIdx.x; r < TM; r += blockDim.x) row_src[r] = (r < rows) ? __ldg(lhs + row0 + r) : 0;
+  const int halves = rows > BM ? 2 : 1;  // 128-row halves holding rows (uniform)
   if (warp == kProducerWarps) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
@@ -188,13 +195,16 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
           if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
           const uint32_t a_s = base + s * STAGE_BYTES;
           uint8_t* b_s = smem + s * STAGE_BYTES + A_BYTES;
-          // activations: 128 rows x 8 chunks of 16 bytes
+          // activations: up to 256 rows x 8 chunks of 16 bytes (half h at A_HALF h;
+          // a second half with no rows is not copied, its MMA is not issued)
 #pragma unroll
-          for (int i = 0; i < (BM * 8) / kProducers; ++i) {
+          for (int i = 0; i < (TM * 8) / kProducers; ++i) {
             const int idx = t + kProducers * i;
             const int r = idx >> 3, c = idx & 7;
-            const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
-            cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
+            if (r < BM * halves) {
+              const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
+              cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
+            }
           }
           asm volatile("cp.async.commit_group;" ::: "memory");
           // weights: 256 rows x 2 groups of 32 codes, dequantized to bf16 (exact)
@@ -243,11 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
           const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-          asm volatile(
-              "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-              :: "r"(tmem), "l"(adesc + (uint64_t)(2 * k)), "l"(bdesc + (uint64_t)(2 * k)), "r"(IDESC), "r"(acc)
-              : "memory");
+          for (int hh = 0; hh < halves; ++hh)  // half hh: its 128 rows (16 KB further), its accumulator
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                :: "r"(tmem + 256u * hh), "l"(adesc + (uint64_t)(2 * k + (A_HALF >> 4) * hh)),
+                   "l"(bdesc + (uint64_t)(2 * k)), "r"(IDESC), "r"(acc)
+                : "memory");
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(smem_u32(&empty[s])) : "memory");
@@ -258,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   }
 
   // -------------------------------------------------------------- epilogue --
-  if (warp < 4) {
+  if (warp < 4 * halves) {
     mbar_wait(accum_full, 0, err, failed);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int r = 32 * warp + lane;
+    const int q = warp & 3, hh = warp >> 2;  // lane quadrant, half
+    const int r = BM * hh + 32 * q + lane;
     uint16_t* orow = out + (int64_t)(row0 + r) * N;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 16) {
@@ -270,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
           "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
           : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
             "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-          : "r"(tmem + ((uint32_t)(32 * warp) << 16) + c));
+          : "r"(tmem + ((uint32_t)(32 * q) << 16) + 256u * hh + c));
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       const int col = n0 + c;
       if (r < rows) {
@@ -307,7 +320,7 @@ cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t
   cudaError_t e = cudaFuncSetAttribute(gather_qmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int64_t m_tiles = (R + BM - 1) / BM + E;  // upper bound on per-expert tiles
+  const int64_t m_tiles = (R + TM - 1) / TM + E;  // upper bound on per-expert tiles
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)m_tiles);
   gather_qmm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(x, lhs, rhs, (int)R, w, scales, (int)E, (int)N,
                                                        (int)K, out, d.err, inject_timeout);

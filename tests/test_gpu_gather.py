@@ -51,10 +51,12 @@ def test_gather_moe_full_size_sampled(B):
 
 def test_gather_segments_on_tile_boundaries(B):
     """Hand-built routing whose expert segments are empty, one row, and 127 /
-    128 / 129 / 256 / 300 rows long, so 128-row tiles start, end and straddle
-    every boundary case; activation rows repeat and come in any order."""
-    E, N, K = 8, 96, 128
-    sizes = [0, 1, 127, 128, 0, 129, 256, 300]
+    128 / 129 / 255 / 256 / 257 / 384 / 513 rows long, so the tiles of up to
+    256 rows (two 128-row MMA halves) start, end and straddle every boundary
+    case: one half, both halves, a one-row tail; activation rows repeat and
+    come in any order."""
+    E, N, K = 11, 96, 128
+    sizes = [0, 1, 127, 128, 0, 129, 255, 256, 257, 384, 513]
     rhs = np.repeat(np.arange(E, dtype=np.int32), sizes)
     R = len(rhs)
     tokens = 200
