@@ -336,14 +336,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     // by ordinary loads: a bulk copy would queue behind the weight boxes already in
     // flight from this SM
     const uint4* xg = reinterpret_cast<const uint4*>(x + (int64_t)kb0 * kBK);
+    const int nx = nst * (kBK / 8);  // 16-byte chunks of the slice
+    constexpr int kXLoads = (kMaxKSlice / 8 + kPrep - 1) / kPrep;
+    uint4 xq[kXLoads];
+#pragma unroll
+    for (int u = 0; u < kXLoads; ++u)  // every load in flight before the first use
+      xq[u] = pa + kPrep * u < nx ? __ldg(xg + pa + kPrep * u) : make_uint4(0, 0, 0, 0);
     uint32_t m2 = 0;
-    for (int v = pa; v < nst * (kBK / 8); v += kPrep) {
-      const uint4 q = __ldg(xg + v);
-      reinterpret_cast<uint4*>(xs)[v] = q;
-      m2 = __vmaxu2(m2, q.x & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, q.y & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, q.z & 0x7FFF7FFFu);
-      m2 = __vmaxu2(m2, q.w & 0x7FFF7FFFu);
+#pragma unroll
+    for (int u = 0; u < kXLoads; ++u) {
+      if (pa + kPrep * u < nx) reinterpret_cast<uint4*>(xs)[pa + kPrep * u] = xq[u];
+      m2 = __vmaxu2(m2, xq[u].x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, xq[u].y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, xq[u].z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, xq[u].w & 0x7FFF7FFFu);
     }
     const uint32_t mb = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
     if (lane == 0) red[pa >> 5] = mb;
