@@ -150,7 +150,7 @@ fp4_status fp4_dequantize(const uint32_t* wq, const void* scales, const fp4_bf16
  * kernel of this library writes weights and releases its dependents early, so
  * any sequence of calls through this header is ordered; a caller's own kernel
  * that writes w and triggers its dependents early must not directly precede qmv.
- * A NaN or infinity in x gives non-finite rows (NVFP4 tensor-core path: NaN). */
+ * A NaN or infinity in x gives non-finite rows (tensor-core path, NVFP4 and MXFP4: NaN). */
 fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
                const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, int bits,
                int group_size, fp4_bf16* y, cudaStream_t stream);
