@@ -206,6 +206,13 @@ class DecodeStack:
         return len(self.mats)
 
 
+WORKLOAD = ("decode qmv over a 64-layer hidden-5120 stack (q,k,v,o 5120x5120; gate,up 17408x5120; "
+            "down 5120x17408), NVFP4 g16 weights, bf16 x, one token")
+LAYOUT = ("q|k|v stored as one [15360, 5120] matrix and gate|up as one [34816, 5120] matrix (they "
+          "multiply the same x): 4 GEMVs a layer, the same weights and outputs; one matrix per "
+          "projection (7 GEMVs a layer) is components.decode_qmv.nvfp4")
+
+
 def time_graph(graph, steps, warmup, stream):
     # replay() launches on the current stream: make it the stream the events see
     with torch.cuda.stream(stream):
@@ -451,7 +458,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "decode qmv, NVFP4 weights (hidden 5120, MLP 17408); oracle on layer 0 (7 projections)",
+        "config": {"workload": WORKLOAD, "layout": LAYOUT,
                    "l2": "inputs larger than L2 per step"},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": "layer 0 of 64: q,k,v,o,gate,up,down NVFP4 GEMV in the C oracle (fp64)"},
@@ -564,12 +571,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp4-e2m1 x bf16, f32 acc", "data": "synthetic",
-            "config": {"workload": "decode qmv over a 64-layer hidden-5120 stack (q,k,v,o 5120x5120; gate,up "
-                                   "17408x5120; down 5120x17408), NVFP4 g16 weights, bf16 x, one token",
-                       "layout": "q|k|v stored as one [15360, 5120] matrix and gate|up as one [34816, 5120] "
-                                 "matrix (they multiply the same x): 4 GEMVs a layer, the same weights and "
-                                 "outputs; one matrix per projection (7 GEMVs a layer) is "
-                                 "components.decode_qmv.nvfp4",
+            "config": {"workload": WORKLOAD, "layout": LAYOUT,
                        "layers": args.layers, "weight_bytes_per_step": stack.bytes,
                        "tokens_per_s": 1e3 / ms, "l2": "inputs larger than L2 (13.4 GB stack)",
                        "parallelism": f"replicas x{ws}"},
