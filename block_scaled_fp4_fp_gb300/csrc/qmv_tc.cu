@@ -52,7 +52,8 @@
 //           that finds its operand slot free again (stage i - 4 done) passes
 //           the weight slot of that stage back to the TMA producer (when the
 //           ring holds kMeta slots or more).  After the last stage the four
-//           warps of lane quadrant 0 read D's term lanes and form the partials.
+//           warps of lane quadrant 0 read D's term lanes (16x256b loads) and
+//           add them per column with warp shuffles into the partials.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -118,8 +119,7 @@ template <int MODE> struct Geo {
 
 // Shared memory (from a 1024-aligned base): [weight ring | term atoms |
 // term-scale tile | x slice | partials | barriers].  The weight ring is split
-// at launch into code slots and, after them, scale slots.  The epilogue reuses
-// the x slice for the term lanes of D.
+// at launch into code slots and, after them, scale slots.
 constexpr int kMaxKSlice = 17408;  // elements of x per CTA
 constexpr uint32_t kSmemBytes = 227u * 1024u;
 constexpr uint32_t kBarBytes = 1024;
@@ -131,7 +131,7 @@ template <int MODE> struct Lay {
   static constexpr uint32_t kRing = (kSmemBytes - kFixed) / 1024u * 1024u;
   static constexpr uint32_t kOffT = kRing;                     // atom kCh m + h
   static constexpr uint32_t kOffSFA = kOffT + kAtoms * 1024;  // term-scale tile
-  static constexpr uint32_t kOffX = kOffSFA + 512;              // x slice (bf16); later D's term lanes
+  static constexpr uint32_t kOffX = kOffSFA + 512;              // x slice (bf16)
   static constexpr uint32_t kOffRed = kOffX + kMaxKSlice * 2;  // [split][256] fp32 partials (rank 0)
   static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
   static_assert(kOffBar + kBarBytes + 1024 <= kSmemBytes, "shared memory layout overflows");
@@ -139,7 +139,6 @@ template <int MODE> struct Lay {
   // from a code chunk's start: both stay inside the allocation
   static_assert(kOffT + (kAtoms - 1) * 1024 + 16384 <= kOffBar, "A-operand reads past the allocation");
   static_assert(kRing + 32768 <= kOffBar, "B-operand reads past the allocation");
-  static_assert(kTerms * kRows * 4 <= kMaxKSlice * 2, "the term lanes of D fit in the x slice");
 };
 static_assert((2 * kMaxSlots + 2 * kMeta + 5) * 8 + 16 + (kPrep / 32) * 4 <= kBarBytes, "barrier area");
 
@@ -470,52 +469,48 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
       while (s >= nslots) { s -= nslots; ++wr; }
     }
     // ---- epilogue: the lane-quadrant-0 warps (one per group) each take 64
-    // columns of D: lanes 0..5 hold the terms of a column; they go through
-    // shared memory (the x slice, no longer read) and each thread adds one
-    // column's six terms.  partial = 2^e0 sum_t D[t, n].
+    // columns of D.  A 16x256b load gives thread T lane T / 4 (and lane T / 4 + 8)
+    // at columns 8 j + 2 (T % 4) + {0, 1} of each 8-column block j; the sum over
+    // the term lanes 0..5 is a butterfly over T's bits 2..4, after which thread T
+    // keeps block T / 4.  partial = 2^e0 sum_t D[t, n].
     if (q4 == 0) {
       mbar_wait(done, 0, err, failed);
       tc_fence_after();
-      float* dt = reinterpret_cast<float*>(xs);  // [kTerms][kRows]
       const int c0 = 64 * grp;
-      if (c0 < nmma) {  // warp-uniform; chunks at or past nmma hold nothing this CTA reads
-        uint32_t d[4][16];
+      float sum[2] = {0.f, 0.f};
+      if (c0 < nmma) {  // warp-uniform
+        uint32_t d[2][16];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int h = 0; h < 2; ++h)
           asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-              : "=r"(d[cc][0]), "=r"(d[cc][1]), "=r"(d[cc][2]), "=r"(d[cc][3]), "=r"(d[cc][4]), "=r"(d[cc][5]),
-                "=r"(d[cc][6]), "=r"(d[cc][7]), "=r"(d[cc][8]), "=r"(d[cc][9]), "=r"(d[cc][10]), "=r"(d[cc][11]),
-                "=r"(d[cc][12]), "=r"(d[cc][13]), "=r"(d[cc][14]), "=r"(d[cc][15])
-              : "r"(tmem + (uint32_t)(c0 + 16 * cc)));
+              "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+              : "=r"(d[h][0]), "=r"(d[h][1]), "=r"(d[h][2]), "=r"(d[h][3]), "=r"(d[h][4]), "=r"(d[h][5]),
+                "=r"(d[h][6]), "=r"(d[h][7]), "=r"(d[h][8]), "=r"(d[h][9]), "=r"(d[h][10]), "=r"(d[h][11]),
+                "=r"(d[h][12]), "=r"(d[h][13]), "=r"(d[h][14]), "=r"(d[h][15])
+              : "r"(tmem + (uint32_t)(c0 + 32 * h)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (lane < kTerms) {
+        const bool term = (lane >> 2) < kTerms;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint4* dst = reinterpret_cast<uint4*>(dt + lane * kRows + c0 + 16 * cc);
+        for (int b = 0; b < 8; ++b) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(d[cc][4 * v], d[cc][4 * v + 1], d[cc][4 * v + 2], d[cc][4 * v + 3]);
+          for (int e = 0; e < 2; ++e) {
+            float v = term ? __uint_as_float(d[b >> 2][4 * (b & 3) + e]) : 0.f;
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            if (b == (lane >> 2)) sum[e] = v;
           }
         }
       }
-      __syncwarp();
+      const int nb = c0 + 8 * (lane >> 2) + 2 * (lane & 3);  // this thread's columns nb, nb + 1
       float partial[2];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int n = c0 + lane + 32 * k;
-        float acc = 0.f;
-        if (n < rows) {
-#pragma unroll
-          for (int t = kTerms - 1; t >= 0; --t) acc += dt[t * kRows + n];
-        }
-        partial[k] = finite ? ldexpf(acc, e0) : __int_as_float(0x7FC00000);
-      }
+      for (int k = 0; k < 2; ++k) partial[k] = finite ? ldexpf(sum[k], e0) : __int_as_float(0x7FC00000);
       if (rank > 0) {
         // asynchronous stores into rank 0's partials; its barrier counts the bytes
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int n = c0 + lane + 32 * k;
+          const int n = nb + k;
           if (n < rows)
             asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                          :: "r"(map_rank(part + rank * kRows + n, 0)), "r"(__float_as_uint(partial[k])),
@@ -529,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
         const float g = gs_w ? __ldg(gs_w) : 1.0f;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int n = c0 + lane + 32 * k;
+          const int n = nb + k;
           if (n < rows) {
             float acc_y = partial[k];
             for (int c = 1; c < split; ++c) acc_y += part[c * kRows + n];
