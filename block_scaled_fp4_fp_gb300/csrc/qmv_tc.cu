@@ -1,4 +1,4 @@
-// qmv_tc.cu -- NVFP4 decode GEMV on the 5th-generation tensor cores.
+// qmv_tc.cu -- NVFP4 / MXFP4 decode GEMV on the 5th-generation tensor cores.
 //
 // Pages: "epic: NVIDIA Volta (sm_70) inference acceleration program #1536"
 // (Baseline: the decode step is the qmv weight stream; the V100 kernel is
@@ -48,12 +48,13 @@
 //           g: the x terms in shared memory, then, once the stage's weights
 //           have landed, each warp stores the stage's W scales into the slot's
 //           scale columns of its lane quadrant (tcgen05.st; B row n's scales
-//           sit in lane n % 32, column n / 32 of the k-step's group).  A group
-//           that finds its operand slot free again (stage i - 4 done) passes
-//           the weight slot of that stage back to the TMA producer (when the
-//           ring holds kMeta slots or more).  After the last stage the four
-//           warps of lane quadrant 0 read D's term lanes (16x256b loads) and
-//           add them per column with warp shuffles into the partials.
+//           sit in lane n % 32, column (n % 128) / 32 of the k-step's group,
+//           four columns further for rows 128..255).  A group that finds its
+//           operand slot free again (stage i - 4 done) passes the weight slot
+//           of that stage back to the TMA producer (when the ring holds kMeta
+//           slots or more).  After the last stage the four warps of lane
+//           quadrant 0 read D's term lanes (16x256b loads) and add them per
+//           column with warp shuffles into the partials.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
