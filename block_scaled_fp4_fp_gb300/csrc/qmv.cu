@@ -394,7 +394,7 @@ cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, c
                        const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode,
                        int group, uint16_t* y, int inject_timeout, cudaStream_t s) {
   // the tensor-core GEMV (NVFP4, MXFP4) needs K % 256 (NVFP4) or K % 512 (MXFP4) == 0,
-  // 16-byte aligned scale rows and <= 128 rows per SM
+  // 16-byte aligned scale rows and <= 256 rows per SM
   if ((mode == 2 || mode == 1) && (reinterpret_cast<uintptr_t>(scales) & 15) == 0 &&
       qmv_tc_supported(d, mode, N, K))
     return launch_qmv_tc(d, mode, x, w, static_cast<const uint8_t*>(scales), gs_w, N, K, y, inject_timeout, s);

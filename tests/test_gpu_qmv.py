@@ -59,10 +59,12 @@ def test_qmv_small(B, mode, N, K):
 
 @pytest.mark.parametrize("mode", [2, 1])
 @pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (9, 256), (129, 768), (1000, 2048), (20000, 512),
-                                 (333, 1536)])
+                                 (333, 1536), (40000, 256)])
 def test_qmv_fp4_tensor_core_ragged_rows(B, mode, N, K):
-    """Row counts that leave partial 8-row atoms per CTA, and N above 128 rows
-    per SM or K off the stage size (which take the mma.sync kernel)."""
+    """Row counts that leave partial 8-row atoms per CTA, row blocks above 128
+    rows (20000 rows: the B rows past 128 take the second scale group), and N
+    above 256 rows per SM or K off the stage size (which take the mma.sync
+    kernel)."""
     q, s, b, gs, g = make_weights(mode, N, K, seed=N)
     x = synth.activations_with_outliers(1, K, seed=3).view(-1)
     qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
