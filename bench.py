@@ -133,6 +133,24 @@ def dist_env():
 
 
 # ----------------------------------------------------------------- decode stack
+def layer_groups(layout: str):
+    """The GEMVs of one decode layer: (N, K, projection indices stacked as rows)
+    for "split" (one matrix per projection), "fused_qkv" (q|k|v as one) or
+    "fused" (q|k|v and gate|up as one each -- the matrices that multiply the
+    same x)."""
+    projs = synth.LAYER_PROJECTIONS  # q, k, v, o, gate, up, down: (name, N, K)
+    groups = {"split": [[p] for p in range(len(projs))],
+              "fused_qkv": [[0, 1, 2], [3], [4], [5], [6]],
+              "fused": [[0, 1, 2], [3], [4, 5], [6]]}
+    if layout not in groups:
+        raise ValueError(layout)
+    out = []
+    for grp in groups[layout]:
+        assert len({projs[p][2] for p in grp}) == 1, "stacked projections share K"
+        out.append((sum(projs[p][1] for p in grp), projs[grp[0]][2], grp))
+    return out
+
+
 class DecodeStack:
     """64-layer weight stack in one format, weights resident on the device."""
 
@@ -146,19 +164,8 @@ class DecodeStack:
         self.B, self.mode, self.layers = B, mode, layers
         self.mats = []
         self.bytes = 0
-        projs = list(enumerate(synth.LAYER_PROJECTIONS))  # q, k, v, o, gate, up, down
-        if layout == "split":
-            groups = [[p] for p in range(len(projs))]
-        elif layout == "fused_qkv":
-            groups = [[0, 1, 2], [3], [4], [5], [6]]
-        elif layout == "fused":
-            groups = [[0, 1, 2], [3], [4, 5], [6]]
-        else:
-            raise ValueError(layout)
         for l in range(layers):
-            for grp in groups:
-                N = sum(projs[p][1][1] for p in grp)
-                K = projs[grp[0]][1][2]
+            for N, K, grp in layer_groups(layout):
                 seeds = [synth.layer_seed(l, p) for p in grp]
                 self.mats.append(self._make(N, K, seeds if len(grp) > 1 else seeds[0], device))
         self.x = {K: synth.bf16_normal((K,), 1.0, seed=7 + K, device=device)
