@@ -132,6 +132,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the process group (the slowest
+    rank's time is the job's); the values unchanged without one."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(bytes_per_rank: int, ms: float, world: int) -> float:
+    """Whole-job weight throughput: every rank streams its own replica of the
+    stack (replicas, weak scaling), so the job moves world x bytes per step."""
+    return world * bytes_per_rank / ms / 1e6
+
+
 # ----------------------------------------------------------------- decode stack
 def layer_groups(layout: str):
     """The GEMVs of one decode layer: (N, K, projection indices stacked as rows)
@@ -540,12 +557,8 @@ def run_ours(args):
     h2d = sum(v.numel() * 2 for v in hx.values())
     d2h = hy.numel() * 2
 
-    # max over ranks
-    t = torch.tensor([ms, e2e_ms], device=device)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms, e2e_ms = t.tolist()
-    value = ws * stack.bytes / ms / 1e6
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], device)
+    value = job_gbs(stack.bytes, ms, ws)
     comps = {"decode_qmv": results}
     if not args.quick and rank == 0:
         comps["quantize_4096x5120"] = bench_quantize(B, device)
@@ -594,7 +607,7 @@ def run_ours(args):
                                                     "launches: the same plan, TMA boxes, ring and launch, no "
                                                     "compute"}},
             "cpu_baseline": cpu,
-            "e2e": {"value": ws * stack.bytes / e2e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_gbs(stack.bytes, e2e_ms, ws), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": stack.launches * args.steps,
             "clocks": clocks,

@@ -59,3 +59,43 @@ def test_reference_arm_json_line():
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def _ranks_worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, e2e = bench.max_over_ranks([1.0 + rank, 10.0 - rank], "cpu")
+        q.put((rank, ms, e2e, bench.job_gbs(1000000, ms, world)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_timing_takes_the_slowest_rank():
+    """World size 2 on gloo: both ranks report the maximum of each time, and the
+    job throughput counts both replicas' bytes over that time."""
+    import multiprocessing as mp
+    import socket
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        port = s_.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_ranks_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [o[1:3] for o in out] == [(2.0, 10.0), (2.0, 10.0)]
+    assert all(abs(o[3] - 2 * 1000000 / 2.0 / 1e6) < 1e-12 for o in out)
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    """Under torchrun only rank 0 runs the oracle and prints; rank 1 exits 0 silently."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == "", (r.stdout, r.stderr[-1000:])
