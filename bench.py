@@ -17,6 +17,7 @@ exchange step), timings are max-reduced, value = all ranks' bytes / time.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -130,6 +131,37 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+@contextlib.contextmanager
+def nvtx(name: str):
+    """An NVTX range around a host-side region (visible to Nsight tools); a
+    no-op where NVTX is unavailable."""
+    pushed = False
+    try:
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:
+        pass
+    try:
+        yield
+    finally:
+        if pushed:
+            try:
+                torch.cuda.nvtx.range_pop()
+            except Exception:
+                pass
+
+
+def device_info(index: int) -> dict:
+    """Name, SM count and compute capability of the GPU, and the host's cores."""
+    info = {"host_cores": os.cpu_count()}
+    try:
+        p = torch.cuda.get_device_properties(index)
+        info.update(name=p.name, sm_count=p.multi_processor_count, cc=f"{p.major}.{p.minor}")
+    except Exception as e:  # the line is still printed without them
+        info["error"] = type(e).__name__
+    return info
 
 
 def max_over_ranks(values, device):
@@ -516,14 +548,15 @@ def run_ours(args):
         stack = DecodeStack(B, mode, args.layers, device, layout=layout)
         graph = capture(stack.step, stream)
         if name == "nvfp4_fused":
-            with ClockSampler(local) as clk:
+            with ClockSampler(local) as clk, nvtx(f"decode {name}"):
                 if ws > 1:
                     torch.distributed.barrier()
                 ms = time_graph(graph, args.steps, args.warmup, stream)
             clocks = clk.summary()
             headline = (stack, graph, ms)
         else:
-            ms = time_graph(graph, args.steps, args.warmup, stream)
+            with nvtx(f"decode {name}"):
+                ms = time_graph(graph, args.steps, args.warmup, stream)
         results[name] = {"ms_per_step": ms, "GB/s": stack.bytes / ms / 1e6, "bytes_per_step": stack.bytes,
                          "launches_per_step": stack.launches, "layout": layout}
         if name != "nvfp4_fused":
@@ -533,7 +566,8 @@ def run_ours(args):
     stack, graph, ms = headline
     # the same launches streaming the same weights with no compute
     sgraph = capture(stack.stream_step, stream)
-    stream_ms = time_graph(sgraph, args.steps, args.warmup, stream)
+    with nvtx("stream ceiling"):
+        stream_ms = time_graph(sgraph, args.steps, args.warmup, stream)
     del sgraph
     # e2e: pinned host activations in, every projection's output back, through the C ABI
     hx = {k: v.cpu().pin_memory() for k, v in stack.x.items()}
@@ -553,7 +587,8 @@ def run_ours(args):
         hy.copy_(dy, non_blocking=True)
 
     g2 = capture(e2e_step, stream)
-    e2e_ms = time_graph(g2, args.steps, args.warmup, stream)
+    with nvtx("e2e"):
+        e2e_ms = time_graph(g2, args.steps, args.warmup, stream)
     h2d = sum(v.numel() * 2 for v in hx.values())
     d2h = hy.numel() * 2
 
@@ -611,6 +646,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": stack.launches * args.steps,
             "clocks": clocks,
+            "device": device_info(local),
             "components": comps,
         }
         print(json.dumps(line), flush=True)

@@ -99,3 +99,14 @@ def test_reference_arm_other_ranks_do_no_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "0"], capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == "", (r.stdout, r.stderr[-1000:])
+
+
+def test_nvtx_ranges_and_device_info_never_raise():
+    """The bench's NVTX ranges and device record must not break a run: without a
+    GPU (or NVTX) the range is a no-op and the record says what it could not read."""
+    with bench.nvtx("test range"):
+        x = 1 + 1
+    assert x == 2
+    info = bench.device_info(0)
+    assert info["host_cores"] >= 1
+    assert ("name" in info and info["sm_count"] >= 1) or "error" in info
