@@ -182,22 +182,7 @@ def job_gbs(bytes_per_rank: int, ms: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------- decode stack
-def layer_groups(layout: str):
-    """The GEMVs of one decode layer: (N, K, projection indices stacked as rows)
-    for "split" (one matrix per projection), "fused_qkv" (q|k|v as one) or
-    "fused" (q|k|v and gate|up as one each -- the matrices that multiply the
-    same x)."""
-    projs = synth.LAYER_PROJECTIONS  # q, k, v, o, gate, up, down: (name, N, K)
-    groups = {"split": [[p] for p in range(len(projs))],
-              "fused_qkv": [[0, 1, 2], [3], [4], [5], [6]],
-              "fused": [[0, 1, 2], [3], [4, 5], [6]]}
-    if layout not in groups:
-        raise ValueError(layout)
-    out = []
-    for grp in groups[layout]:
-        assert len({projs[p][2] for p in grp}) == 1, "stacked projections share K"
-        out.append((sum(projs[p][1] for p in grp), projs[grp[0]][2], grp))
-    return out
+layer_groups = synth.layer_groups
 
 
 class DecodeStack:
@@ -215,30 +200,19 @@ class DecodeStack:
         self.bytes = 0
         for l in range(layers):
             for N, K, grp in layer_groups(layout):
-                seeds = [synth.layer_seed(l, p) for p in grp]
-                self.mats.append(self._make(N, K, seeds if len(grp) > 1 else seeds[0], device))
-        self.x = {K: synth.bf16_normal((K,), 1.0, seed=7 + K, device=device)
-                  for K in {k for _, _, k in synth.LAYER_PROJECTIONS}}
+                self.mats.append(self._make(l, N, K, grp, device))
+        self.x = {K: synth.decode_x(K, device=device) for K in {k for _, _, k in synth.LAYER_PROJECTIONS}}
         self.y = [torch.empty((m["N"],), dtype=torch.bfloat16, device=device) for m in self.mats]
 
-    def _make(self, N, K, seed, device):
+    def _make(self, layer, N, K, grp, device):
         B = self.B
         if self.mode == B.MODE_AFFINE:
-            # synthetic affine-4 g64 weights: uniform codes, per-group bf16 scale/bias in the
-            # range the affine quantizer gives for N(0, 0.02) groups (scale ~ 0.11/15, bias ~ -0.055)
-            g = torch.Generator(device=device)
-            g.manual_seed(seed)
-            q = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), generator=g, device=device, dtype=torch.int64)
-            q = q.to(torch.int32)
-            s = (0.11 / 15 * (1 + 0.1 * torch.rand((N, K // 64), generator=g, device=device))).to(torch.bfloat16)
-            b = (-0.055 * (1 + 0.1 * torch.rand((N, K // 64), generator=g, device=device))).to(torch.bfloat16)
+            # uniform synthetic codes (the library has no affine quantizer), seeded by the group's first projection
+            q, s, b = synth.affine_synthetic(N, K, synth.layer_seed(layer, grp[0]), device=device)
             nbytes = q.numel() * 4 + s.numel() * 2 + b.numel() * 2
             self.bytes += nbytes
             return {"N": N, "K": K, "q": q, "s": s, "b": b, "gs": None, "bytes": nbytes}
-        if isinstance(seed, list):  # rows of several projections, one after the other
-            w = torch.cat([synth.bf16_normal((N // len(seed), K), 0.02, seed=sd, device=device) for sd in seed])
-        else:
-            w = synth.bf16_normal((N, K), 0.02, seed=seed, device=device)
+        w = synth.decode_weight(layer, grp, device=device)
         gs = B.fp4_amax_global_scale(w) if self.mode == B.MODE_NVFP4 else None
         q, s = B.fp4_quantize(w, self.mode, global_scale=gs)
         del w

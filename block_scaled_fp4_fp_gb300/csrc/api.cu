@@ -12,7 +12,8 @@ namespace fp4 {
 namespace {
 
 // Device error word, one per device context.  Bounded waits that expire
-// atomically OR kErrTimeout into it; fp4_check_device_error reads and clears it.
+// atomically OR kErrTimeout into it, index checks kErrIndex;
+// fp4_check_device_error reads and clears it.
 __device__ unsigned g_device_error;
 
 constexpr int kMaxDevices = 64;
@@ -52,6 +53,12 @@ fp4_status current(const DevInfo** out) {
   if (cudaGetDevice(&dev) != cudaSuccess) return FP4_ERR_CUDA;
   return init_device(dev, out);
 }
+
+}  // namespace
+
+int current_device_info(const DevInfo** out) { return (int)current(out); }
+
+namespace {
 
 fp4_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return FP4_OK;
@@ -106,7 +113,7 @@ fp4_status fp4_check_device_error(cudaStream_t stream) {
   if (v != 0) {
     const unsigned zero = 0;
     if (cudaMemcpy(d->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FP4_ERR_CUDA;
-    return FP4_ERR_TIMEOUT;
+    return (v & kErrTimeout) ? FP4_ERR_TIMEOUT : FP4_ERR_INVALID_ARG;
   }
   return FP4_OK;
 }

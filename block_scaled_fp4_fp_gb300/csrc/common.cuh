@@ -17,8 +17,10 @@
 
 namespace fp4 {
 
-// Error word bits written by bounded waits.
+// Error word bits: a bounded wait expired; a kernel found an index argument
+// outside its contract (gather_qmm's expert ids).
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrIndex = 2u;
 
 // Limit of one bounded wait, in SM clock cycles (~0.5 s at 2 GHz).  A thread
 // whose wait expired once stops waiting (later waits try once and return), so

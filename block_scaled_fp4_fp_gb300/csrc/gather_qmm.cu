@@ -136,6 +136,17 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
     mbar_init(never, 1);
     fence_barrier_init();
   }
+  // The first CTA checks the routing contract once: every expert id in [0, E)
+  // and non-decreasing.  A row outside it gets no tile (its output row is not
+  // written); the error word reports it as an invalid argument.
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    bool bad = false;
+    for (int i = threadIdx.x; i < R; i += blockDim.x) {
+      const int e = __ldg(rhs + i);
+      bad |= e < 0 || e >= E || (i + 1 < R && e > __ldg(rhs + i + 1));
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) record_error(err, kErrIndex);
+  }
   __syncthreads();
   const int expert = tile_info[0];
   if (expert < 0) return;  // uniform: this grid slot has no tile

@@ -18,6 +18,10 @@ struct DevInfo {
   unsigned* err = nullptr; // device address of the error word on this device
 };
 
+// api.cu: the current device's cached properties (initialized on first use);
+// returns an fp4_status value
+int current_device_info(const DevInfo** out);
+
 // quant.cu
 size_t amax_workspace_bytes(int64_t n);
 cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* gs_out,

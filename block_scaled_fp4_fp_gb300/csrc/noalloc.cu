@@ -58,18 +58,12 @@ extern "C" fp4_status fp4_amax_global_scale_noalloc(const fp4_bf16* x, int64_t n
   if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(gs_out) & 3) ||
       (amax_out && (reinterpret_cast<uintptr_t>(amax_out) & 3)))
     return FP4_ERR_ALIGNMENT;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FP4_ERR_CUDA;
-  fp4_status st = fp4_init(dev);  // compute capability 10.3 check; allocates nothing
+  const DevInfo* d = nullptr;  // cached per device: compute capability checked, SM count; allocates nothing
+  fp4_status st = (fp4_status)current_device_info(&d);
   if (st != FP4_OK) return st;
   uint32_t* scratch = nullptr;
   st = scratch_for_current_device(&scratch);
   if (st != FP4_OK) return st;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP4_ERR_CUDA;
-  DevInfo d;
-  d.device = dev;
-  d.sm_count = sms;
-  const cudaError_t e = launch_amax(d, x, n, gs_out, amax_out, scratch, kNoAllocPartials, stream);
+  const cudaError_t e = launch_amax(*d, x, n, gs_out, amax_out, scratch, kNoAllocPartials, stream);
   return e == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }

@@ -90,3 +90,49 @@ def from_u16(a: np.ndarray, device="cpu") -> torch.Tensor:
     """numpy uint16 bit patterns -> bf16 tensor."""
     a = np.ascontiguousarray(a, dtype=np.uint16)
     return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
+
+
+# ------------------------------------------------------------- decode stack
+def layer_groups(layout: str):
+    """The GEMVs of one decode layer as (N, K, projection indices stacked as
+    rows): "split" is one matrix per projection, "fused_qkv" stores q|k|v as one
+    matrix, "fused" stores q|k|v and gate|up as one each (the projections that
+    multiply the same x)."""
+    projs = LAYER_PROJECTIONS
+    groups = {"split": [[p] for p in range(len(projs))],
+              "fused_qkv": [[0, 1, 2], [3], [4], [5], [6]],
+              "fused": [[0, 1, 2], [3], [4, 5], [6]]}
+    if layout not in groups:
+        raise ValueError(layout)
+    out = []
+    for grp in groups[layout]:
+        assert len({projs[p][2] for p in grp}) == 1, "stacked projections share K"
+        out.append((sum(projs[p][1] for p in grp), projs[grp[0]][2], grp))
+    return out
+
+
+def decode_weight(layer: int, grp, device="cpu") -> torch.Tensor:
+    """bf16 weights of one GEMV of the decode stack: the projections of ``grp``
+    (indices into LAYER_PROJECTIONS) drawn as bf16(0.02 N(0, 1)) with their own
+    seeds and stacked as rows."""
+    parts = [bf16_normal((LAYER_PROJECTIONS[p][1], LAYER_PROJECTIONS[p][2]), 0.02, seed=layer_seed(layer, p),
+                         device=device) for p in grp]
+    return parts[0] if len(parts) == 1 else torch.cat(parts)
+
+
+def decode_x(K: int, device="cpu") -> torch.Tensor:
+    """The decode stack's activation vector for inputs of width K: bf16 N(0, 1)."""
+    return bf16_normal((K,), 1.0, seed=7 + K, device=device)
+
+
+def affine_synthetic(N: int, K: int, seed: int, group: int = 64, device="cpu"):
+    """Synthetic affine-4 weights of the decode stack: uniform random packed
+    codes (int32 [N, K/8]) and per-group bf16 scale and bias drawn around the
+    range an affine quantizer gives for N(0, 0.02) groups (scale ~ 0.11/15,
+    bias ~ -0.055).  Returns (codes, scales, biases)."""
+    g = _gen(seed, device)
+    q = torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), generator=g, device=device, dtype=torch.int64)
+    q = q.to(torch.int32)
+    s = (0.11 / 15 * (1 + 0.1 * torch.rand((N, K // group), generator=g, device=device))).to(torch.bfloat16)
+    b = (-0.055 * (1 + 0.1 * torch.rand((N, K // group), generator=g, device=device))).to(torch.bfloat16)
+    return q, s, b

@@ -80,8 +80,9 @@ const char* fp4_status_string(fp4_status status);
 
 /* Synchronizes `stream`, then reports and clears the device error word of the
  * current device: FP4_ERR_TIMEOUT if any bounded wait of an earlier launch
- * expired since the last check, FP4_ERR_CUDA if the stream reports an error,
- * else FP4_OK. */
+ * expired since the last check, FP4_ERR_INVALID_ARG if a kernel found an index
+ * argument outside its contract (gather_qmm's expert ids), FP4_ERR_CUDA if the
+ * stream reports an error, else FP4_OK. */
 fp4_status fp4_check_device_error(cudaStream_t stream);
 
 /* Padded scale-tile dimensions for `rows` x `scale_cols` scales
@@ -183,7 +184,10 @@ fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const
  *   out      bf16[R, N], 16-byte aligned
  * mode MXFP4 (group 32).  sorted != 0 promises rhs_idx is non-decreasing (rows
  * grouped by expert), which this version requires.  Requires K % 64 == 0 and
- * N % 16 == 0. */
+ * N % 16 == 0.  The expert ids live in device memory, so the kernel checks them:
+ * an id outside [0, E) or a decrease leaves the affected output rows unwritten
+ * and makes the next fp4_check_device_error return FP4_ERR_INVALID_ARG.
+ * lhs_idx values must lie in [0, T); they are not checked. */
 fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* rhs_idx, int64_t R,
                       const uint32_t* w, const void* scales, const fp4_bf16* biases, int64_t E,
                       int64_t N, int64_t K, fp4_mode mode, int bits, int group_size, int sorted,

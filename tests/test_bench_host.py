@@ -16,17 +16,17 @@ from block_scaled_fp4_fp_gb300 import synth  # noqa: E402
 
 
 def test_layer_groups_cover_the_same_weights():
-    split = bench.layer_groups("split")
+    split = synth.layer_groups("split")
     assert [(n, k) for n, k, _ in split] == [(p[1], p[2]) for p in synth.LAYER_PROJECTIONS]
-    fused = bench.layer_groups("fused")
+    fused = synth.layer_groups("fused")
     assert [(n, k, g) for n, k, g in fused] == [(15360, 5120, [0, 1, 2]), (5120, 5120, [3]),
                                                (34816, 5120, [4, 5]), (5120, 17408, [6])]
     for layout in ("fused", "fused_qkv"):
-        groups = bench.layer_groups(layout)
+        groups = synth.layer_groups(layout)
         assert sorted(p for _, _, g in groups for p in g) == list(range(7))
         assert sum(n * k for n, k, _ in groups) == sum(n * k for n, k, _ in split)
     with pytest.raises(ValueError):
-        bench.layer_groups("other")
+        synth.layer_groups("other")
 
 
 def test_committed_traffic_needs_the_current_source(tmp_path, monkeypatch):

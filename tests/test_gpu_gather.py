@@ -49,6 +49,26 @@ def test_gather_moe_full_size_sampled(B):
     assert_close_to_oracle(out, ref, "gather gate/up full size")
 
 
+def test_gather_moe_down_full_size_sampled(B):
+    """The MoE down projection as the bench runs it: 8192 routed rows already in
+    expert order (lhs is the identity), 32 experts of 2880 x 2880 MXFP4 weights;
+    sampled rows: the first and last rows of expert segments and random ones."""
+    _, rhs = synth.moe_routing(2048, 32, 4, seed=0)
+    R, E, N, K = len(rhs), 32, 2880, 2880
+    lhs = np.arange(R, dtype=np.int32)
+    x = synth.bf16_normal((R, K), 1.0, seed=3)
+    w = synth.bf16_normal((E * N, K), 0.02, seed=4)
+    q, s = oracle.mxfp4_quantize(synth.to_u16(w))
+    q3, s3 = q.reshape(E, N, K // 8), s.reshape(E, N, K // 32)
+    out = B.gather_qmm(x.cuda(), torch.from_numpy(lhs).cuda(), torch.from_numpy(rhs).cuda(),
+                       torch.from_numpy(q3.view(np.int32)).cuda(), torch.from_numpy(s3).cuda())
+    starts = np.searchsorted(rhs, np.arange(E))
+    rows = np.unique(np.concatenate([starts[::4], starts[1::4] - 1, [0, R - 1],
+                                     np.random.default_rng(3).integers(0, R, 16)]))
+    ref = oracle.gather_qmm(synth.to_u16(x), lhs, rhs, q3, s3, None, oracle.MODE_MXFP4, 32, rows=rows)
+    assert_close_to_oracle(out[torch.as_tensor(rows).cuda()], ref, "gather down full size")
+
+
 def test_gather_segments_on_tile_boundaries(B):
     """Hand-built routing whose expert segments are empty, one row, and 127 /
     128 / 129 / 255 / 256 / 257 / 384 / 513 rows long, so the tiles of up to
@@ -85,3 +105,31 @@ def test_gather_timeout_injection_reports_and_recovers(B):
     torch.cuda.synchronize()
     assert B.fp4_check_device_error() == B.FP4_OK
     assert_close_to_oracle(out, ref, "gather after recovery")
+
+
+@pytest.mark.parametrize("bad", ["out_of_range", "negative", "unsorted"])
+def test_gather_routing_contract_violation_is_reported(B, bad):
+    """Expert ids live in device memory, so the kernel checks them: an id outside
+    [0, E) or a decreasing pair is reported by fp4_check_device_error as an
+    invalid argument (the rows it affects get no tile; every access stays inside
+    the buffers), and the next valid call reports nothing."""
+    tokens, E, N, K = 32, 4, 64, 128
+    lhs = np.arange(tokens, dtype=np.int32)
+    rhs = np.repeat(np.arange(E, dtype=np.int32), tokens // E)
+    if bad == "out_of_range":
+        rhs[-1] = E
+    elif bad == "negative":
+        rhs[0] = -1
+    else:
+        rhs[3], rhs[20] = rhs[20], rhs[3]
+    x = synth.bf16_normal((tokens, K), 1.0, seed=51).cuda()
+    w = synth.bf16_normal((E * N, K), 0.02, seed=52)
+    q, s = oracle.mxfp4_quantize(synth.to_u16(w))
+    q3 = torch.from_numpy(q.reshape(E, N, K // 8).view(np.int32)).cuda()
+    s3 = torch.from_numpy(s.reshape(E, N, K // 32)).cuda()
+    B.fp4_check_device_error()
+    B.gather_qmm(x, torch.from_numpy(lhs).cuda(), torch.from_numpy(rhs).cuda(), q3, s3)
+    assert B.fp4_check_device_error() == B.FP4_ERR_INVALID_ARG
+    good = np.repeat(np.arange(E, dtype=np.int32), tokens // E)
+    B.gather_qmm(x, torch.from_numpy(lhs).cuda(), torch.from_numpy(good).cuda(), q3, s3)
+    assert B.fp4_check_device_error() == B.FP4_OK

@@ -236,3 +236,37 @@ def test_qmv_nvfp4_extreme_outlier_in_x(B):
     x[1234] = 1.0e4
     y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=2)
     assert_close_to_oracle(y, oracle.qmv(synth.to_u16(x), q, s, None, 2, 16, gs), "nvfp4 x outlier 1e4")
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("outlier", [1.0e3, 1.0e4])
+def test_qmv_fp4_outlier_bound_per_row(B, mode, outlier):
+    """The tensor-core GEMV's x expansion, checked row by row: one element of x
+    is ``outlier`` times the N(0, 1) rest, and the rows whose weight code is 0
+    at that column (their exact result does not see the outlier, y ~ 1) must
+    still meet the expansion's stated bound, |y - y_exact| <= 2^-17 max|x|
+    sum_k |deq(W)[n, k]| (the truncated radix-8 remainder of every element)
+    plus half a bf16 ulp of the output and an fp32 accumulation allowance."""
+    N, K, col = 1024, 5120, 1234
+    q, s, b, gs, g = make_weights(mode, N, K, seed=40 + mode)
+    qd, sd, bd, gsd = to_dev(mode, q, s, b, gs)
+    x = synth.bf16_normal((K,), 1.0, seed=41)
+    x[col] = outlier
+    y = B.qmv(x.cuda(), qd, sd, None, gsd, mode=mode).float().cpu().double().numpy()
+    xb = synth.to_u16(x)
+    exact = oracle.qmv(xb, q, s, None, mode, g, gs)
+    deq = oracle.dequantize_f64(q, s, None, mode, g, gs)
+    code = (q[:, col // 8] >> np.uint32(4 * (col % 8))) & np.uint32(0x7)
+    rows = np.nonzero(code == 0)[0]
+    assert len(rows) >= 16, "too few rows with a zero code at the outlier's column"
+    xf = oracle.bf16_bits_to_f64(xb)
+    xmax = np.max(np.abs(xf))
+    absw = np.abs(deq[rows]).sum(axis=1)
+    absprod = np.abs(deq[rows] * xf[None, :]).sum(axis=1)
+    mag = np.maximum(np.abs(exact[rows]), np.abs(y[rows]))
+    half_ulp = np.where(mag > 0, 2.0 ** (np.floor(np.log2(np.maximum(mag, 1e-300))) - 8), 0.0)
+    bound = 2.0 ** -17 * xmax * absw + half_ulp + 2.0 ** -20 * absprod
+    err = np.abs(y[rows] - exact[rows])
+    worst = int(np.argmax(err / bound))
+    assert np.all(err <= bound), (f"row {rows[worst]}: |y - exact| = {err[worst]:.3e} > bound {bound[worst]:.3e} "
+                                  f"(exact {exact[rows[worst]]:.4f})")

@@ -62,6 +62,23 @@ def test_qqmm_prefill_full_size_sampled(B, mode, M):
     assert_close_to_oracle(out, ref, f"qqmm mode {mode} M={M}")
 
 
+@pytest.mark.parametrize("mode", [2, 1])
+def test_qqmm_prefill_m8192_sampled(B, mode):
+    """The largest prefill GEMM, 8192 x 17408 x 5120, in the bench's launch
+    configuration: more than 256 output rows (the first and last 128-row tiles
+    in part, a tile boundary and random rows) against columns of the first and
+    last 256-column tiles, a tile boundary and random columns."""
+    M, N = 8192, 17408
+    rng = np.random.default_rng(8192 + mode)
+    mrows = np.unique(np.concatenate([np.arange(64), np.arange(120, 136), np.arange(M - 64, M),
+                                      rng.integers(0, M, 128)]))
+    assert len(mrows) >= 256
+    ncols = np.unique(np.concatenate([np.arange(32), np.arange(250, 262), np.arange(N - 32, N),
+                                      rng.integers(0, N, 40)]))
+    out, ref = run(B, mode, M, N, 5120, seed=0, mrows=mrows, ncols=ncols)
+    assert_close_to_oracle(out, ref, f"qqmm mode {mode} M={M}")
+
+
 def test_qqmm_timeout_injection_reports_and_recovers(B):
     B.fp4_debug_inject_wait_timeout(True)
     try:
