@@ -323,5 +323,29 @@ def gather_qmm(x, lhs, rhs, w, scales, biases, mode, group, rows=None):
     return out
 
 
+GROUP_OF = {MODE_NVFP4: 16, MODE_MXFP4: 32}
+
+
+def quantize_dequantize(x, mode, gs=None):
+    """fp_quantize_dequantize: quantize bf16 ``x`` [rows, cols] (NVFP4 with the
+    optional multiplier-form global scale ``gs``, or MXFP4) and dequantize it
+    back to bf16 bits -- the activation that the one-row route of QQMatmul
+    multiplies ("mlx 0.30.7.3 -> 0.30.7.6", qqmm.cpp, QQMatmul::eval_gpu: with
+    quantized W and one row, x goes through fp_quantize_dequantize into an array
+    of x's own dtype, then fp_qmv).  Composition of the pinned quantizer and
+    bf16 dequantizer; pinned by tests/test_oracle_qqmv.py."""
+    q, s = quantize(x, mode, gs)
+    return dequantize_bf16(q, s, None, mode, GROUP_OF[mode], gs)
+
+
+def qqmv(x, w, scales, mode, gs_x=None, gs_w=None, rows=None):
+    """The one-row quantized-activation GEMV: y = x_hat . deq(W)^T in fp64, where
+    x_hat = quantize_dequantize(x) (bf16) and deq(W) includes the NVFP4 weight
+    global scale ``gs_w`` (applied by this library's epilogue; MLX's fp_qmv
+    leaves it to the caller)."""
+    xh = quantize_dequantize(_c(x, np.uint16).reshape(1, -1), mode, gs_x)
+    return qmv(xh.ravel(), w, scales, None, mode, GROUP_OF[mode], gs_w, rows)
+
+
 def num_threads() -> int:
     return lib().orc_num_threads()
