@@ -188,20 +188,24 @@ layer_groups = synth.layer_groups
 class DecodeStack:
     """64-layer weight stack in one format, weights resident on the device."""
 
-    def __init__(self, B, mode: int, layers: int, device, layout: str = "split"):
+    def __init__(self, B, mode: int, layers: int, device, layout: str = "split", qx: bool = False):
         """layout "split": one matrix per projection, 7 GEMVs a layer.  "fused":
         the projections that multiply the same x stored as one matrix, as serving
         engines store them -- q|k|v as [3*5120, 5120] and gate|up as [2*17408,
         5120] -- so a layer is 4 GEMVs (qkv, o, gate_up, down) over the same
         weights (each output slice is that projection's y).  "fused_qkv": only
-        q|k|v fused, 5 GEMVs a layer."""
-        self.B, self.mode, self.layers = B, mode, layers
+        q|k|v fused, 5 GEMVs a layer.  qx: the quantized-activation route (qqmv:
+        x quantized and dequantized inside each GEMV; NVFP4 with a static
+        activation global scale, as a calibrated checkpoint carries one)."""
+        self.B, self.mode, self.layers, self.qx = B, mode, layers, qx
         self.mats = []
         self.bytes = 0
         for l in range(layers):
             for N, K, grp in layer_groups(layout):
                 self.mats.append(self._make(l, N, K, grp, device))
         self.x = {K: synth.decode_x(K, device=device) for K in {k for _, _, k in synth.LAYER_PROJECTIONS}}
+        self.gs_x = {K: (B.fp4_amax_global_scale(v) if qx and mode == B.MODE_NVFP4 else None)
+                     for K, v in self.x.items()}
         self.y = [torch.empty((m["N"],), dtype=torch.bfloat16, device=device) for m in self.mats]
 
     def _make(self, layer, N, K, grp, device):
@@ -223,7 +227,10 @@ class DecodeStack:
     def step(self, stream=None):
         B = self.B
         for m, y in zip(self.mats, self.y):
-            B.qmv(self.x[m["K"]], m["q"], m["s"], m["b"], m["gs"], mode=self.mode, y=y, stream=stream)
+            if self.qx:
+                B.qqmv(self.x[m["K"]], m["q"], m["s"], self.gs_x[m["K"]], m["gs"], mode=self.mode, y=y, stream=stream)
+            else:
+                B.qmv(self.x[m["K"]], m["q"], m["s"], m["b"], m["gs"], mode=self.mode, y=y, stream=stream)
 
     def stream_step(self, stream=None):
         """The same weights moved as the tensor-core GEMV moves them, with no
@@ -513,13 +520,17 @@ def run_ours(args):
 
     # the headline: NVFP4 weights in the fused layout (4 GEMVs a layer); the
     # per-projection layout and the other formats are components
-    modes = [("nvfp4_fused", B.MODE_NVFP4, "fused")] + (
-        [] if args.quick else [("nvfp4", B.MODE_NVFP4, "split"), ("mxfp4_fused", B.MODE_MXFP4, "fused"),
-                               ("mxfp4", B.MODE_MXFP4, "split"), ("affine_g64", B.MODE_AFFINE, "split")])
+    modes = [("nvfp4_fused", B.MODE_NVFP4, "fused", False)] + (
+        [] if args.quick else [("nvfp4", B.MODE_NVFP4, "split", False), ("mxfp4_fused", B.MODE_MXFP4, "fused", False),
+                               ("mxfp4", B.MODE_MXFP4, "split", False),
+                               ("affine_g64", B.MODE_AFFINE, "split", False),
+                               ("affine_g64_fused", B.MODE_AFFINE, "fused", False),
+                               ("nvfp4_fused_quantized_x", B.MODE_NVFP4, "fused", True),
+                               ("mxfp4_fused_quantized_x", B.MODE_MXFP4, "fused", True)])
     results = {}
     headline = None
-    for name, mode, layout in modes:
-        stack = DecodeStack(B, mode, args.layers, device, layout=layout)
+    for name, mode, layout, qx in modes:
+        stack = DecodeStack(B, mode, args.layers, device, layout=layout, qx=qx)
         graph = capture(stack.step, stream)
         if name == "nvfp4_fused":
             with ClockSampler(local) as clk, nvtx(f"decode {name}"):
@@ -532,7 +543,9 @@ def run_ours(args):
             with nvtx(f"decode {name}"):
                 ms = time_graph(graph, args.steps, args.warmup, stream)
         results[name] = {"ms_per_step": ms, "GB/s": stack.bytes / ms / 1e6, "bytes_per_step": stack.bytes,
-                         "launches_per_step": stack.launches, "layout": layout}
+                         "frac_of_hbm": stack.bytes / ms / 1e6 / peaks["hbm_gbs"],
+                         "launches_per_step": stack.launches, "layout": layout,
+                         "entry_point": "qqmv (x quantized inside the GEMV)" if qx else "qmv"}
         if name != "nvfp4_fused":
             del stack, graph
             torch.cuda.empty_cache()

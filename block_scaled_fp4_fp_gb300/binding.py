@@ -40,6 +40,7 @@ SIGNATURES = {
     "fp4_quantize": (_INT, [_VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP, _VP, _INT, _VP]),
     "fp4_dequantize": (_INT, [_VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _INT, _VP, _VP]),
     "qmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
+    "qqmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP, _VP]),
     "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
@@ -166,6 +167,18 @@ def qmv(x: torch.Tensor, w: torch.Tensor, scales: torch.Tensor, biases=None, glo
         y = torch.empty((N,), dtype=torch.bfloat16, device=w.device)
     _check(lib().qmv(_p(x), _p(w), _p(scales), _p(biases), _p(global_scale_w), N, K, mode, 4, group_size, _p(y),
                      _s(stream)), "qmv")
+    return y
+
+
+def qqmv(x: torch.Tensor, w: torch.Tensor, scales: torch.Tensor, global_scale_x=None, global_scale_w=None,
+         mode: int = MODE_NVFP4, y=None, stream=None):
+    """One-row quantized-activation GEMV: x is quantized and dequantized (bf16)
+    inside the kernel, then multiplied by the 4-bit W."""
+    N, K = w.shape[0], w.shape[1] * 8
+    if y is None:
+        y = torch.empty((N,), dtype=torch.bfloat16, device=w.device)
+    _check(lib().qqmv(_p(x), _p(global_scale_x), _p(w), _p(scales), _p(global_scale_w), N, K, mode, _p(y),
+                      _s(stream)), "qqmv")
     return y
 
 

@@ -202,7 +202,26 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
   const DevInfo* d = nullptr;
   st = current(&d);
   if (st != FP4_OK) return st;
-  return from_cuda(launch_qmv(*d, x, w, scales, biases, global_scale_w, N, K, mode, group_size, y,
+  return from_cuda(launch_qmv(*d, x, nullptr, 0, w, scales, biases, global_scale_w, N, K, mode, group_size, y,
+                              g_inject_timeout.load(), stream));
+}
+
+fp4_status qqmv(const fp4_bf16* x, const float* global_scale_x, const uint32_t* w, const uint8_t* scales,
+                const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, fp4_bf16* y,
+                cudaStream_t stream) {
+  if (mode != FP4_MODE_NVFP4 && mode != FP4_MODE_MXFP4) return FP4_ERR_UNSUPPORTED;
+  const int group = mode == FP4_MODE_NVFP4 ? 16 : 32;
+  if (!x || !w || !scales || !y || N <= 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || N > INT32_MAX / 2) return FP4_ERR_INVALID_ARG;
+  if (K > 65536) return FP4_ERR_UNSUPPORTED;  // x is staged whole in shared memory
+  if ((global_scale_x || global_scale_w) && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 2) || (mode == FP4_MODE_NVFP4 && !aligned(scales, 2)) ||
+      (global_scale_x && !aligned(global_scale_x, 4)) || (global_scale_w && !aligned(global_scale_w, 4)))
+    return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_qmv(*d, x, global_scale_x, 1, w, scales, nullptr, global_scale_w, N, K, mode, group, y,
                               g_inject_timeout.load(), stream));
 }
 

@@ -104,6 +104,62 @@ __device__ __forceinline__ float exp2i_f32(int e) {
 // E8M0 byte -> fp32 (0xFF, NaN, is outside the contract).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t byte) { return exp2i_f32((int)(byte & 0xFFu) - 127); }
 
+// ------------------------------------------------- block quantization rule ----
+// The fp_quantize rule for one block from the bits of its largest |x| (bf16
+// magnitude bits, mb): the multiplier that maps x to e2m1 (q = e2m1_rn_sat(x *
+// mul)), the scale byte stored, and the scale's value.
+//   NVFP4 (MODE 2, E4M3 per 16): b = max|x|, s8 = E4M3_rn_sat(b / fl(6 gs)) (0 when
+//     b = 0), mul = 1 / fl(s8 gs) (0 when that product is 0).
+//   MXFP4 (MODE 1, E8M0 per 32): se = clamp(floor(log2 b) - 2, -127, 127) (-127 when
+//     b = 0), byte = se + 127, mul = 2^-se.
+template <int MODE>
+__device__ __forceinline__ void block_scale_rule(uint32_t mb, float gs, float& mul, uint32_t& sbyte,
+                                                 float& sval) {
+  if (MODE == 2) {
+    const float b = __uint_as_float(mb << 16);
+    const float p = __fmul_rn(6.0f, gs);
+    const float sc = (b == 0.0f) ? 0.0f : __fdiv_rn(b, p);
+    sbyte = e4m3_rn(sc);
+    sval = e4m3_to_f32(sbyte);
+    const float dd = __fmul_rn(sval, gs);
+    mul = (dd == 0.0f) ? 0.0f : __frcp_rn(dd);
+  } else {
+    int se = -127;
+    if (mb != 0) {
+      const int E = (int)(mb >> 7);
+      const int e = (E == 0) ? (-133 + (31 - __clz((int)(mb & 0x7Fu)))) : (E - 127);
+      se = min(max(e - 2, -127), 127);
+    }
+    sbyte = (uint32_t)(se + 127);
+    mul = exp2i_f32(-se);
+    sval = exp2i_f32(se);
+  }
+}
+
+// Largest bf16 magnitude (bits) of the eight values of a 16-byte piece.
+__device__ __forceinline__ uint32_t max_mag8(uint4 v) {
+  uint32_t m2 = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+  m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+  return max(m2 & 0xFFFFu, m2 >> 16);
+}
+
+// fp_quantize then fp_dequantize of eight bf16 values of one block: each
+// value becomes bf16_rn(fl(fl(e2m1(q) * sval) * gs)) with q = e2m1_rn_sat(x * mul)
+// (gs = 1 for MXFP4 or without a global scale; the multiply by 1 is exact).
+__device__ __forceinline__ uint4 quant_dequant8(uint4 v, float mul, float sval, float gs) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t code2 = e2m1x2_rn(__fmul_rn(bf16_lo(in[j]), mul), __fmul_rn(bf16_hi(in[j]), mul));
+    const uint32_t h2 = e2m1x2_to_f16x2(code2);
+    o[j] = pack_bf16x2_rn(__fmul_rn(__fmul_rn(f16_lo_to_f32(h2), sval), gs),
+                          __fmul_rn(__fmul_rn(f16_hi_to_f32(h2), sval), gs));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ---------------------------------------------------------- tiled scales ----
 __device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t c, int64_t padded_cols) {
   int64_t tile = (r >> 7) * (padded_cols >> 2) + (c >> 2);

@@ -34,18 +34,20 @@ cudaError_t launch_dequantize(const DevInfo& d, const uint32_t* wq, const void* 
                               int group, const float* gs, int tiled, uint16_t* out,
                               cudaStream_t s);
 
-// qmv.cu
-cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, const void* scales,
-                       const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode,
-                       int group, uint16_t* y, int inject_timeout, cudaStream_t s);
+// qmv.cu (qx != 0: the quantized-activation route -- x is replaced by
+// fp_dequantize(fp_quantize(x, gs_x)) before the GEMV; NVFP4 and MXFP4 only)
+cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const float* gs_x, int qx, const uint32_t* w,
+                       const void* scales, const uint16_t* biases, const float* gs_w, int64_t N, int64_t K,
+                       int mode, int group, uint16_t* y, int inject_timeout, cudaStream_t s);
 
 // qmv_tc.cu (NVFP4 = mode 2 and MXFP4 = mode 1 on tcgen05; launch_qmv dispatches to it when supported)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // driver's tensor-map encoder (nullptr if unavailable)
 // the NVFP4 plan: CTAs per cluster (K slices), row blocks, rows per CTA, weight ring slots
 bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nblk, int* R, int* nslots);
 bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K);
-cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject_timeout, cudaStream_t s);
+cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const float* gs_x, int qx,
+                          const uint32_t* w, const uint8_t* scales, const float* gs_w, int64_t N, int64_t K,
+                          uint16_t* y, int inject_timeout, cudaStream_t s);
 
 // qqmm.cu
 cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,

@@ -104,8 +104,10 @@ __device__ __forceinline__ void mma_f16_first(float (&d)[4], uint32_t a0, uint32
 }
 
 // MODE: 0 affine (group 32/64/128), 1 MXFP4 (group 32), 2 NVFP4 (group 16).
-template <int MODE>
+// QX (FP4 modes): x is first replaced by fp_dequantize(fp_quantize(x, gs_x)).
+template <int MODE, bool QX>
 __global__ void __launch_bounds__(kThreads, 1) qmv_kernel(const uint16_t* __restrict__ x,
+                                                           const float* __restrict__ gs_x,
                                                            const uint32_t* __restrict__ w,
                                                            const void* __restrict__ scales_v,
                                                            const uint16_t* __restrict__ biases,
@@ -213,6 +215,21 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_kernel(const uint16_t* __rest
     uint4 xv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) xv[i] = __ldg(src + i);
+    if (QX) {  // this chunk is two NVFP4 blocks or one MXFP4 block
+      const float gsx = (MODE == 2 && gs_x) ? __ldg(gs_x) : 1.0f;
+#pragma unroll
+      for (int b = 0; b < (MODE == 2 ? 2 : 1); ++b) {
+        constexpr int NB = (MODE == 2) ? 2 : 4;
+        uint32_t mb = 0;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) mb = max(mb, max_mag8(xv[b * NB + i]));
+        float mul, sval;
+        uint32_t sbyte;
+        block_scale_rule<(MODE == 2 ? 2 : 1)>(mb, gsx, mul, sbyte, sval);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) xv[b * NB + i] = quant_dequant8(xv[b * NB + i], mul, sval, gsx);
+      }
+    }
     uint32_t m2 = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -361,10 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_kernel(const uint16_t* __rest
   for (int r = tid; r < r1 - r0; r += kThreads) y[r0 + r] = (uint16_t)f32_to_bf16_rn(ypart[r] * unscale);
 }
 
-template <int MODE>
-cudaError_t launch_mode(const DevInfo& d, const uint16_t* x, const uint32_t* w, const void* scales,
-                        const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int group,
-                        uint16_t* y, cudaStream_t s) {
+template <int MODE, bool QX>
+cudaError_t launch_mode(const DevInfo& d, const uint16_t* x, const float* gs_x, const uint32_t* w,
+                        const void* scales, const uint16_t* biases, const float* gs_w, int64_t N, int64_t K,
+                        int group, uint16_t* y, cudaStream_t s) {
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(d.sm_count, (N + 7) / 8));
   const int64_t rows_max = (N + grid - 1) / grid;
   const int64_t rg_max = (rows_max + 15) / 16;
@@ -372,7 +389,7 @@ cudaError_t launch_mode(const DevInfo& d, const uint16_t* x, const uint32_t* w, 
                       (size_t)rg_max * 16 * 4;
   if (smem > d.smem_optin) return cudaErrorInvalidValue;
   {
-    cudaError_t e = cudaFuncSetAttribute(qmv_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(qmv_kernel<MODE, QX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -385,22 +402,25 @@ cudaError_t launch_mode(const DevInfo& d, const uint16_t* x, const uint32_t* w, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qmv_kernel<MODE>, x, w, scales, biases, gs_w, (int)N, (int)K, group, y);
+  return cudaLaunchKernelEx(&cfg, qmv_kernel<MODE, QX>, x, gs_x, w, scales, biases, gs_w, (int)N, (int)K, group, y);
 }
 
 }  // namespace
 
-cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const uint32_t* w, const void* scales,
-                       const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode,
-                       int group, uint16_t* y, int inject_timeout, cudaStream_t s) {
+cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const float* gs_x, int qx, const uint32_t* w,
+                       const void* scales, const uint16_t* biases, const float* gs_w, int64_t N, int64_t K,
+                       int mode, int group, uint16_t* y, int inject_timeout, cudaStream_t s) {
   // the tensor-core GEMV (NVFP4, MXFP4) needs K % 256 (NVFP4) or K % 512 (MXFP4) == 0,
   // 16-byte aligned scale rows and <= 256 rows per SM
   if ((mode == 2 || mode == 1) && (reinterpret_cast<uintptr_t>(scales) & 15) == 0 &&
       qmv_tc_supported(d, mode, N, K))
-    return launch_qmv_tc(d, mode, x, w, static_cast<const uint8_t*>(scales), gs_w, N, K, y, inject_timeout, s);
-  if (mode == 2) return launch_mode<2>(d, x, w, scales, biases, gs_w, N, K, group, y, s);
-  if (mode == 1) return launch_mode<1>(d, x, w, scales, biases, gs_w, N, K, group, y, s);
-  return launch_mode<0>(d, x, w, scales, biases, gs_w, N, K, group, y, s);
+    return launch_qmv_tc(d, mode, x, gs_x, qx, w, static_cast<const uint8_t*>(scales), gs_w, N, K, y,
+                         inject_timeout, s);
+  if (mode == 2 && qx) return launch_mode<2, true>(d, x, gs_x, w, scales, biases, gs_w, N, K, group, y, s);
+  if (mode == 1 && qx) return launch_mode<1, true>(d, x, gs_x, w, scales, biases, gs_w, N, K, group, y, s);
+  if (mode == 2) return launch_mode<2, false>(d, x, nullptr, w, scales, biases, gs_w, N, K, group, y, s);
+  if (mode == 1) return launch_mode<1, false>(d, x, nullptr, w, scales, biases, gs_w, N, K, group, y, s);
+  return launch_mode<0, false>(d, x, nullptr, w, scales, biases, gs_w, N, K, group, y, s);
 }
 
 }  // namespace fp4

@@ -163,10 +163,11 @@ __device__ __forceinline__ uint32_t map_rank(const void* p, int rank) {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-template <int MODE>
+template <int MODE, bool QX>
 __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmS,
                                                               const uint16_t* __restrict__ x,
+                                                              const float* __restrict__ gs_x,
                                                               const float* __restrict__ gs_w, int N, int K,
                                                               int R, int split, int nslots, uint32_t wslot,
                                                               uint32_t sslot, uint16_t* __restrict__ y,
@@ -350,6 +351,22 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
 #pragma unroll
     for (int u = 0; u < kXLoads; ++u)  // every load in flight before the first use
       xq[u] = pa + kPrep * u < nx ? __ldg(xg + pa + kPrep * u) : make_uint4(0, 0, 0, 0);
+    if (QX) {
+      // The quantized-activation route: x is replaced by fp_dequantize(fp_quantize(x))
+      // (bf16) before the GEMV.  A block (16 or 32 elements) is the 16-byte pieces of
+      // 2 or 4 neighbouring lanes (the slice starts on a block boundary).
+      const float gsx = (MODE == 2 && gs_x) ? __ldg(gs_x) : 1.0f;
+#pragma unroll
+      for (int u = 0; u < kXLoads; ++u) {
+        uint32_t mb = max_mag8(xq[u]);
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        if (MODE == 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        float mul, sval;
+        uint32_t sbyte;
+        block_scale_rule<MODE>(mb, gsx, mul, sbyte, sval);
+        xq[u] = quant_dequant8(xq[u], mul, sval, gsx);
+      }
+    }
     uint32_t m2 = 0;
 #pragma unroll
     for (int u = 0; u < kXLoads; ++u) {
@@ -554,7 +571,7 @@ int max_clusters(const DevInfo& d, int split) {
   std::lock_guard<std::mutex> lock(mu);
   if (have[d.device][split]) return cache[d.device][split];
   int n = 0;
-  if (cudaFuncSetAttribute(qmv_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
+  if (cudaFuncSetAttribute(qmv_tc_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
       cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(split * std::max(1, d.sm_count / split)));
@@ -567,7 +584,7 @@ int max_clusters(const DevInfo& d, int split) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, qmv_tc_kernel<MODE>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, qmv_tc_kernel<MODE, false>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();  // the failed query leaves no sticky error behind
     }
@@ -639,9 +656,10 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
   return best;
 }
 
-template <int MODE>
-cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                           const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject, cudaStream_t s) {
+template <int MODE, bool QX>
+cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const float* gs_x, const uint32_t* w,
+                           const uint8_t* scales, const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject,
+                           cudaStream_t s) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
   const TcPlan p = plan_qmv_tc<MODE>(d, N, K);
@@ -671,7 +689,7 @@ cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* 
       return cudaErrorInvalidValue;
   }
   cudaError_t e =
-      cudaFuncSetAttribute(qmv_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      cudaFuncSetAttribute(qmv_tc_kernel<MODE, QX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.nblk * p.split));
@@ -687,7 +705,7 @@ cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const uint32_t* 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel<MODE>, tmW, tmS, x, gs_w, (int)N, (int)K, p.R, p.split,
+  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel<MODE, QX>, tmW, tmS, x, gs_x, gs_w, (int)N, (int)K, p.R, p.split,
                             p.nslots, p.wslot, p.sslot, y, d.err, inject);
 }
 
@@ -725,10 +743,13 @@ bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nb
   return true;
 }
 
-cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const uint32_t* w, const uint8_t* scales,
-                          const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject_timeout, cudaStream_t s) {
-  if (mode == 2) return launch_mode_tc<2>(d, x, w, scales, gs_w, N, K, y, inject_timeout, s);
-  if (mode == 1) return launch_mode_tc<1>(d, x, w, scales, gs_w, N, K, y, inject_timeout, s);
+cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const float* gs_x, int qx,
+                          const uint32_t* w, const uint8_t* scales, const float* gs_w, int64_t N, int64_t K,
+                          uint16_t* y, int inject_timeout, cudaStream_t s) {
+  if (mode == 2 && qx) return launch_mode_tc<2, true>(d, x, gs_x, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 1 && qx) return launch_mode_tc<1, true>(d, x, gs_x, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 2) return launch_mode_tc<2, false>(d, x, nullptr, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 1) return launch_mode_tc<1, false>(d, x, nullptr, w, scales, gs_w, N, K, y, inject_timeout, s);
   return cudaErrorInvalidValue;
 }
 

@@ -100,25 +100,9 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
     m2 = __vmaxu2(m2, v[i].w & 0x7FFF7FFFu);
   }
   const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
-  float mul;
+  float mul, sval;
   uint32_t sbyte;
-  if (MODE == 2) {
-    const float b = __uint_as_float(mb << 16);
-    const float p = __fmul_rn(6.0f, gs);
-    const float s = (b == 0.0f) ? 0.0f : __fdiv_rn(b, p);
-    sbyte = e4m3_rn(s);
-    const float d = __fmul_rn(e4m3_to_f32(sbyte), gs);
-    mul = (d == 0.0f) ? 0.0f : __frcp_rn(d);
-  } else {
-    int se = -127;
-    if (mb != 0) {
-      const int E = (int)(mb >> 7);
-      const int e = (E == 0) ? (-133 + (31 - __clz((int)(mb & 0x7Fu)))) : (E - 127);
-      se = min(max(e - 2, -127), 127);
-    }
-    sbyte = (uint32_t)(se + 127);
-    mul = exp2i_f32(-se);
-  }
+  block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
   uint32_t out[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {

@@ -156,6 +156,22 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
                const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, int bits,
                int group_size, fp4_bf16* y, cudaStream_t stream);
 
+/* qqmv: the one-row route of the quantized-activation matmul [P3 qqmm.cpp,
+ * QQMatmul::eval_gpu: with quantized W and a single row of x, x goes through
+ * fp_quantize_dequantize into an array of x's dtype and then through fp_qmv].
+ *   y[n] = sum_k xhat[k] * deq(W)[n, k]   (fp32 accumulation, bf16 output)
+ *   xhat = fp4_dequantize(fp4_quantize(x)): per block of 16 (NVFP4, global scale
+ *          global_scale_x or 1) or 32 (MXFP4) the rule of fp4_quantize, then each
+ *          value bf16_rn(fl(fl(e2m1(q) * scale) * gs_x)) -- x's own dtype, as the
+ *          page's route stores it.  The quantization happens inside the GEMV
+ *          kernel (no extra launch, no scratch).
+ *   x, w, scales, global_scale_w, y, N, K: as for qmv (linear scales); mode is
+ *          NVFP4 or MXFP4; global_scale_x (device fp32 or NULL) is NVFP4 only.
+ * Requires K % 32 == 0 (hence whole blocks) and K <= 65536.  Launch order as qmv. */
+fp4_status qqmv(const fp4_bf16* x, const float* global_scale_x, const uint32_t* w, const uint8_t* scales,
+                const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, fp4_bf16* y,
+                cudaStream_t stream);
+
 /* a7-a9: qqmm, the FP4 x FP4 GEMM [P3 qqmm.cpp, qqmm_impl, qqmm_utils.cu].
  *   out[m, n] = bf16( alpha * sum_k deq(xq)[m, k] * deq(wq)[n, k] ),  beta = 0
  *   alpha = (*global_scale_x) * (*global_scale_w); a NULL pointer counts as 1.

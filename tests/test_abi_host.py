@@ -80,5 +80,10 @@ def test_validation_rejects_before_launch(B):
     assert L.qqmm(p, p, p, p, None, None, 0, 8, 256, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG
     assert L.gather_qmm(p, p, p, 0, p, p, None, 2, 32, 64, B.MODE_MXFP4, 4, 32, 1, p, None) == B.FP4_ERR_INVALID_ARG
     assert L.gather_qmm(p, p, p, 8, p, p, None, 0, 32, 64, B.MODE_MXFP4, 4, 32, 1, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.qqmv(p, None, p, p, None, 64, 64, B.MODE_AFFINE, p, None) == B.FP4_ERR_UNSUPPORTED
+    assert L.qqmv(p, p, p, p, None, 64, 64, B.MODE_MXFP4, p, None) == B.FP4_ERR_INVALID_ARG  # gs_x w/ MXFP4
+    assert L.qqmv(p, None, p, p, None, 64, 48, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG  # K % 32
+    assert L.qqmv(p, None, p, p, None, 0, 64, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.qqmv(odd, None, p, p, None, 64, 64, B.MODE_NVFP4, p, None) == B.FP4_ERR_ALIGNMENT
     assert L.fp4_debug_stream_weights(p, p, 64, 320, None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.fp4_debug_stream_weights(odd, p, 64, 256, None) == B.FP4_ERR_ALIGNMENT

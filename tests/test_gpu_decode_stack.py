@@ -8,14 +8,14 @@ For layers 0 and 63 every row of every projection is compared with the oracle,
 and the library's quantized weights are first compared bit for bit with the
 oracle's quantization of the same bf16 weights.  Every other layer is checked
 on a seeded sample of rows (the first, the last and 14 random ones per
-matrix)."""
+matrix), the samples judged together by the tolerance rule."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from block_scaled_fp4_fp_gb300 import synth
-from helpers import assert_close_to_oracle, bf16_u16, u8, u32
+from helpers import MAX_ABS_RMS, assert_close_to_oracle, bf16_f64, bf16_u16, u8, u32
 
 pytestmark = pytest.mark.gpu
 GROUP = {0: 64, 1: 32, 2: 16}
@@ -50,6 +50,7 @@ def test_decode_stack_every_layer(B, mode, layout):
     xs = {K: synth.decode_x(K, device="cuda") for K in (synth.HIDDEN, synth.MLP)}
     xh = {K: synth.to_u16(v) for K, v in xs.items()}
     rng = np.random.default_rng(1000 + 10 * mode + (layout == "fused"))
+    got, want = [], []  # sampled rows of every other layer, judged together by the tolerance rule
     for layer in range(synth.LAYERS):
         full = layer in FULL_LAYERS
         for N, K, grp in synth.layer_groups(layout):
@@ -75,7 +76,14 @@ def test_decode_stack_every_layer(B, mode, layout):
                 rd = torch.from_numpy(rows).cuda()
                 qh, sh, bh = host(mode, q[rd], s[rd], b[rd] if b is not None else None)
                 ref = oracle.qmv(xh[K], qh, sh, bh, mode, GROUP[mode], gsv)
-                assert_close_to_oracle(y[rd], ref, what)
+                yg = bf16_f64(y[rd])
+                rms = np.sqrt(np.mean(ref ** 2))
+                assert np.max(np.abs(yg - ref)) <= MAX_ABS_RMS * rms, f"{what}: max-abs"
+                got.append(y[rd].cpu())
+                want.append(ref)
             del q, s, b, w, y
+    # rel-L2 over the union of the samples (a 16-row sample alone is too small for it:
+    # one output rounding to the neighbouring bf16 moves its rel-L2 by ~1e-3)
+    assert_close_to_oracle(torch.cat(got), np.concatenate(want), f"sampled rows, mode {mode} {layout}")
     torch.cuda.synchronize()
     assert B.fp4_check_device_error() == B.FP4_OK
