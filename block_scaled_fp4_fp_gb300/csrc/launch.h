@@ -49,6 +49,13 @@ cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const f
                           const uint32_t* w, const uint8_t* scales, const float* gs_w, int64_t N, int64_t K,
                           uint16_t* y, int inject_timeout, cudaStream_t s);
 
+// qmv_affine.cu (affine-4 GEMV on a TMA ring; launch_qmv dispatches to it when the plan fits:
+// K a multiple of max(512, 8 group) and at most 32768, 16-byte aligned scales and biases)
+bool qmv_affine_supported(const DevInfo& d, int64_t N, int64_t K, int group);
+cudaError_t launch_qmv_affine(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+                              const uint16_t* biases, int64_t N, int64_t K, int group, uint16_t* y,
+                              cudaStream_t s);
+
 // qqmm.cu
 cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
                         const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,

@@ -416,6 +416,9 @@ cudaError_t launch_qmv(const DevInfo& d, const uint16_t* x, const float* gs_x, i
       qmv_tc_supported(d, mode, N, K))
     return launch_qmv_tc(d, mode, x, gs_x, qx, w, static_cast<const uint8_t*>(scales), gs_w, N, K, y,
                          inject_timeout, s);
+  if (mode == 0 && ((reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(biases)) & 15) == 0 &&
+      qmv_affine_supported(d, N, K, group))
+    return launch_qmv_affine(d, x, w, static_cast<const uint16_t*>(scales), biases, N, K, group, y, s);
   if (mode == 2 && qx) return launch_mode<2, true>(d, x, gs_x, w, scales, biases, gs_w, N, K, group, y, s);
   if (mode == 1 && qx) return launch_mode<1, true>(d, x, gs_x, w, scales, biases, gs_w, N, K, group, y, s);
   if (mode == 2) return launch_mode<2, false>(d, x, nullptr, w, scales, biases, gs_w, N, K, group, y, s);

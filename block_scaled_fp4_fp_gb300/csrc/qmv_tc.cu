@@ -354,10 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
     if (QX) {
       // The quantized-activation route: x is replaced by fp_dequantize(fp_quantize(x))
       // (bf16) before the GEMV.  A block (16 or 32 elements) is the 16-byte pieces of
-      // 2 or 4 neighbouring lanes (the slice starts on a block boundary).
+      // 2 or 4 neighbouring lanes (the slice starts on a block boundary); the slice is
+      // a multiple of 32 pieces, so the range test is uniform across each warp.
       const float gsx = (MODE == 2 && gs_x) ? __ldg(gs_x) : 1.0f;
 #pragma unroll
       for (int u = 0; u < kXLoads; ++u) {
+        if (pa + kPrep * u >= nx) break;
         uint32_t mb = max_mag8(xq[u]);
         mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
         if (MODE == 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
