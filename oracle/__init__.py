@@ -73,6 +73,11 @@ def lib():
                 "orc_nvfp4_quantize": (None, [P(u16), i64, i64, P(f32), P(u32), P(u8)]),
                 "orc_mxfp4_quantize": (None, [P(u16), i64, i64, P(u32), P(u8)]),
                 "orc_affine_quantize": (None, [P(u16), i64, i64, c.c_int, P(u32), P(u16), P(u16)]),
+                "orc_philox4x32_10": (None, [P(u32), P(u32), P(u32)]),
+                "orc_sr_word": (u32, [c.c_uint64, c.c_uint64, c.c_uint64]),
+                "orc_e2m1_encode_sr": (c.c_uint, [f32, u32]),
+                "orc_nvfp4_quantize_sr": (None, [P(u16), i64, i64, P(f32), c.c_uint64, c.c_uint64, P(u32), P(u8)]),
+                "orc_mxfp4_quantize_sr": (None, [P(u16), i64, i64, c.c_uint64, c.c_uint64, P(u32), P(u8)]),
                 "orc_padded_rows": (i64, [i64]),
                 "orc_padded_cols": (i64, [i64]),
                 "orc_tiled_offset": (i64, [i64, i64, i64]),
@@ -206,6 +211,45 @@ def quantize(x: np.ndarray, mode: int, gs=None):
     if mode == MODE_MXFP4:
         return mxfp4_quantize(x)
     raise ValueError("oracle quantize: mode must be NVFP4 or MXFP4")
+
+
+# ---- stochastic rounding ---------------------------------------------------
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 of a 4-word counter under a 2-word key -> 4 uint32 words."""
+    c = (ctypes.c_uint32 * 4)(*[int(v) & 0xFFFFFFFF for v in ctr])
+    k = (ctypes.c_uint32 * 2)(*[int(v) & 0xFFFFFFFF for v in key])
+    o = (ctypes.c_uint32 * 4)()
+    lib().orc_philox4x32_10(c, k, o)
+    return [int(v) for v in o]
+
+
+def sr_word(seed: int, offset: int, e: int) -> int:
+    return int(lib().orc_sr_word(int(seed), int(offset), int(e)))
+
+
+def e2m1_encode_sr(v: float, u: int) -> int:
+    return int(lib().orc_e2m1_encode_sr(float(v), int(u)))
+
+
+def quantize_sr(x: np.ndarray, mode: int, gs=None, seed: int = 0, offset: int = 0):
+    """Stochastic-rounding fp_quantize (rule and random numbers in fp4_oracle.c)."""
+    x = _c(x, np.uint16)
+    rows, cols = x.shape
+    g = 16 if mode == MODE_NVFP4 else 32
+    q = np.zeros((rows, cols // 8), np.uint32)
+    s = np.zeros((rows, cols // g), np.uint8)
+    if mode == MODE_NVFP4:
+        lib().orc_nvfp4_quantize_sr(_p(x, ctypes.c_uint16), rows, cols, _f32p(gs), int(seed), int(offset),
+                                    _p(q, ctypes.c_uint32), _p(s, ctypes.c_uint8))
+    elif mode == MODE_MXFP4:
+        if gs is not None:
+            raise ValueError("MXFP4 has no global scale")
+        lib().orc_mxfp4_quantize_sr(_p(x, ctypes.c_uint16), rows, cols, int(seed), int(offset),
+                                    _p(q, ctypes.c_uint32), _p(s, ctypes.c_uint8))
+    else:
+        raise ValueError("oracle quantize_sr: mode must be NVFP4 or MXFP4")
+    return q, s
 
 
 # ---- tiles -----------------------------------------------------------------

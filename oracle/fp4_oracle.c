@@ -256,6 +256,135 @@ void orc_mxfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols,
   }
 }
 
+/* ---- stochastic rounding ------------------------------------------------ */
+/* The pages name a stochastic-rounding variant of fp_quantize (P1, the
+ * USE_SR template parameter of the NVFP4/MXFP4 quantizer, which needs the
+ * Blackwell converters) without stating its rule or its random numbers.  The
+ * reading implemented here: block scales exactly as for round-to-nearest; each
+ * element v = x * mul is rounded to one of the two e2m1 values around |v|
+ * (lo <= |v| < hi), up with probability floor(2^24 (|v| - lo) / (hi - lo)) / 2^24,
+ * decided by the top 24 bits of one 32-bit random word; |v| >= 6 gives 6; the
+ * sign is kept.  The random word of element e (row-major index r*cols + c) is
+ * word e % 4 of Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random
+ * numbers: as easy as 1, 2, 3", SC 2011) at the 128-bit counter
+ * offset + floor(e / 4) (little-endian 32-bit words) under the key (low, high
+ * 32 bits of seed).  Pinned by tests/test_oracle_sr.py. */
+
+/* Philox4x32 with 10 rounds, written from the paper's definition: each round
+ * multiplies words 0 and 2 by the two round multipliers (64-bit products split
+ * into high and low halves), mixes the high halves with words 3 and 1 and the
+ * round key, and bumps the key by the two Weyl constants between rounds. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint64_t p0 = (uint64_t)M0 * c0, p1 = (uint64_t)M1 * c2;
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The random word of element e (see the contract above). */
+uint32_t orc_sr_word(uint64_t seed, uint64_t offset, uint64_t e) {
+  const uint64_t blk = offset + (e >> 2);
+  const uint32_t carry = blk < offset ? 1u : 0u;
+  const uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), carry, 0u};
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return out[e & 3];
+}
+
+/* Stochastic e2m1 rounding of v with random word u (rule above).  The two
+ * neighbours come from a scan of the value table; the probability fraction is
+ * exact in double. */
+unsigned orc_e2m1_encode_sr(float v, uint32_t u) {
+  const double a = fabs((double)v);
+  unsigned code;
+  if (a >= 6.0) {
+    code = 7;
+  } else {
+    unsigned lo = 0;
+    for (unsigned c = 0; c < 8; ++c)
+      if (orc_e2m1_decode(c) <= a) lo = c;  /* the table is increasing */
+    const double vlo = orc_e2m1_decode(lo), vhi = orc_e2m1_decode(lo + 1);
+    const double t = floor(ldexp((a - vlo) / (vhi - vlo), 24));
+    code = ((double)(u >> 8) < t) ? lo + 1 : lo;
+  }
+  return code | (signbit(v) ? 8u : 0u);
+}
+
+void orc_nvfp4_quantize_sr(const uint16_t* x, int64_t rows, int64_t cols, const float* global_scale,
+                           uint64_t seed, uint64_t offset, uint32_t* q, uint8_t* scales) {
+  const float gs = global_scale ? *global_scale : 1.0f;
+  const int64_t ng = cols / 16;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    uint32_t* qrow = q + r * (cols / 8);
+    memset(qrow, 0, (size_t)(cols / 8) * 4);
+    for (int64_t g = 0; g < ng; ++g) {
+      float xf[16];
+      float b = 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        xf[i] = bf16_to_float(x[r * cols + g * 16 + i]);
+        if (fabsf(xf[i]) > b) b = fabsf(xf[i]);
+      }
+      float p = 6.0f * gs;
+      float s = (b == 0.0f) ? 0.0f : b / p;
+      unsigned s8 = orc_e4m3_encode(s);
+      float d = (float)orc_e4m3_decode(s8) * gs;
+      float rcp = (d == 0.0f) ? 0.0f : 1.0f / d;
+      for (int i = 0; i < 16; ++i) {
+        const uint64_t e = (uint64_t)(r * cols + g * 16 + i);
+        put_code(qrow, g * 16 + i, orc_e2m1_encode_sr(xf[i] * rcp, orc_sr_word(seed, offset, e)));
+      }
+      scales[r * ng + g] = (uint8_t)s8;
+    }
+  }
+}
+
+void orc_mxfp4_quantize_sr(const uint16_t* x, int64_t rows, int64_t cols, uint64_t seed, uint64_t offset,
+                           uint32_t* q, uint8_t* scales) {
+  const int64_t ng = cols / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    uint32_t* qrow = q + r * (cols / 8);
+    memset(qrow, 0, (size_t)(cols / 8) * 4);
+    for (int64_t g = 0; g < ng; ++g) {
+      float xf[32];
+      float b = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        xf[i] = bf16_to_float(x[r * cols + g * 32 + i]);
+        if (fabsf(xf[i]) > b) b = fabsf(xf[i]);
+      }
+      int se;
+      if (b == 0.0f) {
+        se = -127;
+      } else {
+        int e;
+        (void)frexpf(b, &e);
+        se = (e - 1) - 2;
+        if (se < -127) se = -127;
+        if (se > 127) se = 127;
+      }
+      float mul = ldexpf(1.0f, -se);
+      for (int i = 0; i < 32; ++i) {
+        const uint64_t el = (uint64_t)(r * cols + g * 32 + i);
+        put_code(qrow, g * 32 + i, orc_e2m1_encode_sr(xf[i] * mul, orc_sr_word(seed, offset, el)));
+      }
+      scales[r * ng + g] = (uint8_t)(se + 127);
+    }
+  }
+}
+
 /* Affine 4-bit (test-data generator only; the pages give no rule):
  * per group lo = min, hi = max, scale = bf16(fl((hi-lo)/15)), bias = bf16(lo),
  * q = clamp(rint((w - bias)/scale), 0, 15), q = 0 when scale is 0. */

@@ -52,6 +52,15 @@ void orc_mxfp4_quantize(const uint16_t* x, int64_t rows, int64_t cols,
 void orc_affine_quantize(const uint16_t* w, int64_t rows, int64_t cols, int group,
                          uint32_t* q, uint16_t* scales, uint16_t* biases);
 
+/* ---- stochastic-rounding quantizers (see fp4_oracle.c for the contract) -- */
+void     orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+uint32_t orc_sr_word(uint64_t seed, uint64_t offset, uint64_t e);
+unsigned orc_e2m1_encode_sr(float v, uint32_t u);
+void orc_nvfp4_quantize_sr(const uint16_t* x, int64_t rows, int64_t cols, const float* global_scale,
+                           uint64_t seed, uint64_t offset, uint32_t* q, uint8_t* scales);
+void orc_mxfp4_quantize_sr(const uint16_t* x, int64_t rows, int64_t cols, uint64_t seed, uint64_t offset,
+                           uint32_t* q, uint8_t* scales);
+
 /* ---- scale tile layout ------------------------------------------------ */
 int64_t orc_padded_rows(int64_t rows);
 int64_t orc_padded_cols(int64_t cols);
