@@ -282,17 +282,27 @@ def bench_quantize(B, device, reps=50):
     """Activation quantize 4096x5120 (0.1 % outliers x50), tiled scales; 4 rotating inputs."""
     xs = [synth.activations_with_outliers(4096, 5120, seed=i, outlier_seed=100 + i, device=device) for i in range(4)]
     res = {}
-    for mode, name in ((B.MODE_NVFP4, "nvfp4"), (B.MODE_MXFP4, "mxfp4")):
+    for mode, name, sr in ((B.MODE_NVFP4, "nvfp4", False), (B.MODE_MXFP4, "mxfp4", False),
+                           (B.MODE_NVFP4, "nvfp4_stochastic", True), (B.MODE_MXFP4, "mxfp4_stochastic", True)):
         gss = [B.fp4_amax_global_scale(x) if mode == B.MODE_NVFP4 else None for x in xs]
         outs = [B.fp4_quantize(x, mode, global_scale=g, layout=B.SCALES_TILED) for x, g in zip(xs, gss)]
+
+        def call(r):
+            i = r % 4
+            if sr:  # a fresh offset per call: no random word is reused
+                B.fp4_quantize_sr(xs[i], mode, 1234, r * (4096 * 5120 // 4), global_scale=gss[i],
+                                  layout=B.SCALES_TILED, xq=outs[i][0], scales=outs[i][1])
+            else:
+                B.fp4_quantize(xs[i], mode, global_scale=gss[i], layout=B.SCALES_TILED, xq=outs[i][0],
+                               scales=outs[i][1])
+
         for i in range(4):  # warm-up
-            B.fp4_quantize(xs[i], mode, global_scale=gss[i], layout=B.SCALES_TILED, xq=outs[i][0], scales=outs[i][1])
+            call(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for r in range(reps):  # back-to-back launches over 4 rotating inputs (4 x 84 MB > L2)
-            i = r % 4
-            B.fp4_quantize(xs[i], mode, global_scale=gss[i], layout=B.SCALES_TILED, xq=outs[i][0], scales=outs[i][1])
+            call(r)
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps if reps else float("nan")
@@ -336,6 +346,40 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
         res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops,
                         "ms_with_x_quantize": ms_q, "TFLOP/s_with_x_quantize": flops / ms_q / 1e9}
         del x, xq, xs, out
+    return res
+
+
+def bench_qmm(B, device, Ms=(1024, 2048, 8192), reps=20):
+    """Dense W4A16 prefill GEMM M x 17408 x 5120: bf16 activations against NVFP4
+    (group 16, global scale) and affine-4 group-64 weights."""
+    N, K = 17408, 5120
+    res = {}
+    for name, mode in (("nvfp4", B.MODE_NVFP4), ("affine_g64", B.MODE_AFFINE)):
+        if mode == B.MODE_AFFINE:
+            wq, ws, wb = synth.affine_synthetic(N, K, seed=1, device=device)
+            gw = None
+        else:
+            w = synth.bf16_normal((N, K), 0.02, seed=1, device=device)
+            gw = B.fp4_amax_global_scale(w)
+            wq, ws = B.fp4_quantize(w, mode, global_scale=gw)
+            wb = None
+            del w
+        for M in Ms:
+            x = synth.bf16_normal((M, K), 1.0, seed=2, device=device)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+            for _ in range(3):  # warm-up
+                B.qmm(x, wq, ws, wb, gw, mode=mode, out=out)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                B.qmm(x, wq, ws, wb, gw, mode=mode, out=out)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps if reps else float("nan")
+            flops = 2.0 * M * N * K
+            res.setdefault(name, {})[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}
+            del x, out
     return res
 
 
@@ -469,6 +513,8 @@ def run_case(args):
         bench_quantize(B, dev, reps=2)
     elif c == "gather":
         bench_gather(B, dev, reps=1)
+    elif c.startswith("qmm_m"):
+        bench_qmm(B, dev, Ms=(int(c[len("qmm_m"):]),), reps=1)
     torch.cuda.synchronize()
     st = B.fp4_check_device_error()
     print(json.dumps({"case": c, "status": B.status_string(st)}))
@@ -586,6 +632,10 @@ def run_ours(args):
         comps["quantize_4096x5120"] = bench_quantize(B, device)
         comps["qqmm_nvfp4_Mx17408x5120"] = bench_qqmm(B, device)
         comps["gather_qmm_mxfp4_moe"] = bench_gather(B, device)
+        comps["qmm_w4a16_Mx17408x5120"] = bench_qmm(B, device)
+        for fmt in comps["qmm_w4a16_Mx17408x5120"].values():
+            for v in fmt.values():
+                v["frac_of_bf16_peak"] = v["TFLOP/s"] / peaks["bf16_tflops"]
         fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
         for k, v in comps["qqmm_nvfp4_Mx17408x5120"].items():
             v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak

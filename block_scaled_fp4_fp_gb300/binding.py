@@ -38,12 +38,15 @@ SIGNATURES = {
     "fp4_amax_workspace_bytes": (c.c_size_t, [_I64]),
     "fp4_amax_global_scale": (_INT, [_VP, _I64, _VP, _VP, _VP, c.c_size_t, _VP]),
     "fp4_quantize": (_INT, [_VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP, _VP, _INT, _VP]),
+    "fp4_quantize_sr": (_INT, [_VP, _I64, _I64, _INT, _INT, _INT, _VP, c.c_uint64, c.c_uint64, _VP, _VP, _INT,
+                               _VP]),
     "fp4_dequantize": (_INT, [_VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _INT, _VP, _VP]),
     "qmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
     "qqmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP, _VP]),
     "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
+    "qmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
     "fp4_debug_inject_wait_timeout": (_INT, [_INT]),
     "fp4_debug_stream_weights": (_INT, [_VP, _VP, _I64, _I64, _VP]),
     "fp4_amax_global_scale_noalloc": (_INT, [_VP, _I64, _VP, _VP, _VP]),
@@ -146,6 +149,21 @@ def fp4_quantize(x: torch.Tensor, mode: int, group_size: int = None, global_scal
     return xq, scales
 
 
+def fp4_quantize_sr(x: torch.Tensor, mode: int, seed: int, offset: int = 0, group_size: int = None,
+                    global_scale=None, layout: int = SCALES_LINEAR, xq=None, scales=None, stream=None):
+    """fp_quantize with stochastic rounding of the elements (Philox4x32-10 words
+    from seed and offset); block scales as fp4_quantize."""
+    group_size = group_size or GROUP[mode]
+    rows, cols = x.shape
+    if xq is None:
+        xq = torch.empty((rows, cols // 8), dtype=torch.int32, device=x.device)
+    if scales is None:
+        scales = torch.empty(scales_shape(rows, cols, group_size, layout), dtype=torch.uint8, device=x.device)
+    _check(lib().fp4_quantize_sr(_p(x), rows, cols, mode, 4, group_size, _p(global_scale), int(seed), int(offset),
+                                 _p(xq), _p(scales), layout, _s(stream)), "fp4_quantize_sr")
+    return xq, scales
+
+
 def fp4_dequantize(wq: torch.Tensor, scales: torch.Tensor, biases=None, mode: int = MODE_NVFP4,
                    group_size: int = None, global_scale=None, layout: int = SCALES_LINEAR, out=None,
                    stream=None, rows: int = None):
@@ -203,6 +221,19 @@ def gather_qmm(x: torch.Tensor, lhs_idx: torch.Tensor, rhs_idx: torch.Tensor, w:
         out = torch.empty((R, N), dtype=torch.bfloat16, device=w.device)
     _check(lib().gather_qmm(_p(x), _p(lhs_idx), _p(rhs_idx), R, _p(w), _p(scales), _p(biases), E, N, K, mode, 4,
                             group_size, 1 if sorted_indices else 0, _p(out), _s(stream)), "gather_qmm")
+    return out
+
+
+def qmm(x: torch.Tensor, w: torch.Tensor, scales: torch.Tensor, biases=None, global_scale_w=None,
+        mode: int = MODE_NVFP4, group_size: int = None, out=None, stream=None):
+    """Dense W4A16 GEMM: out = x . deq(W)^T with x bf16 [M, K] and 4-bit W [N, K]."""
+    group_size = group_size or GROUP[mode]
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=w.device)
+    _check(lib().qmm(_p(x), _p(w), _p(scales), _p(biases), _p(global_scale_w), M, N, K, mode, 4, group_size, _p(out),
+                     _s(stream)), "qmm")
     return out
 
 

@@ -139,9 +139,10 @@ fp4_status fp4_amax_global_scale(const fp4_bf16* x, int64_t n, float* gs_out, fl
                                max_partials > 1024 ? 1024 : max_partials, stream));
 }
 
-fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits,
-                        int group_size, const float* global_scale, uint32_t* xq, uint8_t* scales,
-                        fp4_scale_layout layout, cudaStream_t stream) {
+namespace {
+fp4_status quantize_common(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits, int group_size,
+                           const float* global_scale, uint32_t* xq, uint8_t* scales, fp4_scale_layout layout,
+                           int sr, uint64_t seed, uint64_t offset, cudaStream_t stream) {
   fp4_status st = check_format(mode, bits, group_size);
   if (st != FP4_OK) return st;
   if (mode == FP4_MODE_AFFINE) return FP4_ERR_UNSUPPORTED;
@@ -157,7 +158,21 @@ fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode 
   st = current(&d);
   if (st != FP4_OK) return st;
   return from_cuda(launch_quantize(*d, x, rows, cols, mode, group_size, global_scale, xq, scales,
-                                   layout == FP4_SCALES_TILED_128x4, stream));
+                                   layout == FP4_SCALES_TILED_128x4, sr, seed, offset, stream));
+}
+}  // namespace
+
+fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits,
+                        int group_size, const float* global_scale, uint32_t* xq, uint8_t* scales,
+                        fp4_scale_layout layout, cudaStream_t stream) {
+  return quantize_common(x, rows, cols, mode, bits, group_size, global_scale, xq, scales, layout, 0, 0, 0, stream);
+}
+
+fp4_status fp4_quantize_sr(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits,
+                           int group_size, const float* global_scale, uint64_t seed, uint64_t offset, uint32_t* xq,
+                           uint8_t* scales, fp4_scale_layout layout, cudaStream_t stream) {
+  return quantize_common(x, rows, cols, mode, bits, group_size, global_scale, xq, scales, layout, 1, seed, offset,
+                         stream);
 }
 
 fp4_status fp4_dequantize(const uint32_t* wq, const void* scales, const fp4_bf16* biases, int64_t rows,
@@ -243,24 +258,52 @@ fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const
                                g_inject_timeout.load(), stream));
 }
 
+namespace {
+// Shared checks of the W4A16 GEMMs: format, weight scales/biases by mode, alignment.
+fp4_status check_w4a16(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
+                       const float* gs_w, fp4_mode mode, int bits, int group_size, int64_t N, int64_t K,
+                       const fp4_bf16* out) {
+  fp4_status st = check_format(mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  if (!x || !w || !scales || !out) return FP4_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % 64 != 0 || N % 16 != 0 || N > INT32_MAX / 2 || K > (1 << 20)) return FP4_ERR_INVALID_ARG;
+  if ((mode == FP4_MODE_AFFINE) != (biases != nullptr)) return FP4_ERR_INVALID_ARG;
+  if (gs_w && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(scales, 2) ||
+      (biases && !aligned(biases, 2)) || (gs_w && !aligned(gs_w, 4)))
+    return FP4_ERR_ALIGNMENT;
+  return FP4_OK;
+}
+}  // namespace
+
 fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* rhs_idx, int64_t R,
                       const uint32_t* w, const void* scales, const fp4_bf16* biases, int64_t E, int64_t N,
                       int64_t K, fp4_mode mode, int bits, int group_size, int sorted, fp4_bf16* out,
                       cudaStream_t stream) {
-  fp4_status st = check_format(mode, bits, group_size);
+  fp4_status st = check_w4a16(x, w, scales, biases, nullptr, mode, bits, group_size, N, K, out);
   if (st != FP4_OK) return st;
-  if (mode != FP4_MODE_MXFP4) return FP4_ERR_UNSUPPORTED;
   if (!sorted) return FP4_ERR_UNSUPPORTED;
-  if (!x || !lhs_idx || !rhs_idx || !w || !scales || !out || biases) return FP4_ERR_INVALID_ARG;
-  if (R <= 0 || E <= 0 || N <= 0 || K <= 0 || K % 64 != 0 || N % 16 != 0) return FP4_ERR_INVALID_ARG;
-  if (R > INT32_MAX / 2 || E > 4096 || N > INT32_MAX / 2 || K > (1 << 20)) return FP4_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(lhs_idx, 4) || !aligned(rhs_idx, 4))
-    return FP4_ERR_ALIGNMENT;
+  if (!lhs_idx || !rhs_idx) return FP4_ERR_INVALID_ARG;
+  if (R <= 0 || E <= 0 || R > INT32_MAX / 2 || E > 4096) return FP4_ERR_INVALID_ARG;
+  if (!aligned(lhs_idx, 4) || !aligned(rhs_idx, 4)) return FP4_ERR_ALIGNMENT;
   const DevInfo* d = nullptr;
   st = current(&d);
   if (st != FP4_OK) return st;
-  return from_cuda(launch_gather_qmm(*d, x, lhs_idx, rhs_idx, R, w, static_cast<const uint8_t*>(scales), E, N,
-                                     K, mode, out, g_inject_timeout.load(), stream));
+  return from_cuda(launch_gather_qmm(*d, x, lhs_idx, rhs_idx, R, w, scales, biases, nullptr, E, N, K, mode,
+                                     group_size, out, g_inject_timeout.load(), stream));
+}
+
+fp4_status qmm(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
+               const float* global_scale_w, int64_t M, int64_t N, int64_t K, fp4_mode mode, int bits, int group_size,
+               fp4_bf16* out, cudaStream_t stream) {
+  fp4_status st = check_w4a16(x, w, scales, biases, global_scale_w, mode, bits, group_size, N, K, out);
+  if (st != FP4_OK) return st;
+  if (M <= 0 || M > INT32_MAX / 2) return FP4_ERR_INVALID_ARG;
+  const DevInfo* d = nullptr;
+  st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_qmm(*d, x, M, w, scales, biases, global_scale_w, N, K, mode, group_size, out,
+                              g_inject_timeout.load(), stream));
 }
 
 fp4_status fp4_debug_stream_weights(const uint32_t* w, const uint8_t* scales, int64_t N, int64_t K,

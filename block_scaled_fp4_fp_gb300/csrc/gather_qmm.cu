@@ -1,30 +1,42 @@
-// gather_qmm.cu -- MoE grouped GEMM: bf16 activations x MXFP4 expert weights
-// (W4A16) on the tensor cores.
+// gather_qmm.cu -- 4-bit-weight x bf16-activation GEMMs on the tensor cores
+// (W4A16): the MoE grouped GEMM gather_qmm and the dense prefill GEMM qmm, for
+// MXFP4, NVFP4 and affine-4 weights.
 //
 // Pages: "epic: NVIDIA Volta (sm_70) inference acceleration program #1536"
 // (Diagnosis 1: gather_gemm; Diagnosis 5: the MoE grouped GEMM); "mlx: opt-in
 // dense GEMM for nvfp4 prefill ... - #287" (the mixed-input GEMM whose weights
 // are dequantized by producer warps in shared memory before bf16 tensor-core
-// MMAs).
+// MMAs, measured at 55-73 TFLOP/s for MLX's qmm and 285-324 TFLOP/s for the
+// hand-written kernel on an RTX PRO 6000); "perf(cuda): enable hardware
+// NVFP4/MXFP4 conversion on Blackwell builds" (qmm_sm80, the prefill qmm).
 //
-// Design: rows arrive sorted by expert.  Each CTA owns one tile of up to 256
-// rows of one expert's segment (tiles never straddle experts; the tile ->
-// expert map is rebuilt in every CTA by binary searches over the sorted expert
-// ids, so no workspace is needed) and one 256-column slice of N.  Per K = 64
-// stage:
-//   * 16 producer warps gather the tile's activation rows with cp.async (16
-//     bytes per copy, written in the 128-byte-swizzled K-major layout) and
-//     dequantize the 256 x 64 weight slice exactly to bf16 (e2m1 *
-//     2^(byte-127)) into the same layout, once for both 128-row halves of the
-//     tile; each thread's weight codes and scales are loaded kPD stages ahead
-//     into registers;
+// Design.  A CTA owns one tile of up to 256 rows and one 256-column slice of N.
+// gather_qmm: rows arrive sorted by expert; tiles never straddle experts (the
+// tile -> expert map is rebuilt in every CTA by binary searches over the sorted
+// expert ids, so no workspace is needed).  qmm: the identity routing, one
+// "expert", tile t = rows 256 t ...  Per K = 64 stage:
+//   * 16 producer warps dequantize the 256 x 64 weight slice exactly to bf16
+//     into the 128-byte-swizzled K-major layout the MMA reads, once for both
+//     128-row halves of the tile; each thread's codes and scales are loaded kPD
+//     stages ahead into registers.  MXFP4: e2m1 * 2^(byte - 127); NVFP4: e2m1 *
+//     E4M3 (both exact in bf16; the NVFP4 global scale is applied in fp32 in the
+//     epilogue); affine: w = q * scale + bias in fp32 split into two bf16 terms
+//     hi = bf16(w), lo = bf16(w - hi) (a single bf16 rounding of w would cost
+//     ~2.5e-3 relative error), each its own B operand;
+//   * gather_qmm: the producers gather the tile's activation rows with cp.async
+//     (16 bytes per copy, written in the same swizzled layout); qmm: one TMA
+//     box of 256 rows x 128 bytes per stage (rows past M read as zeros);
 //   * one thread issues tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulators
-//     in tensor memory, M 128, N 256, K 16 per instruction): one MMA per half
-//     that holds rows, each into its own 256-column accumulator;
+//     in tensor memory, M 128, N 256, K 16 per instruction): per half that holds
+//     rows one MMA (two for affine: hi then lo), each half into its own
+//     256-column accumulator;
 //   * after the last stage warps 0-7 (lane quadrant warp % 4, half warp / 4)
-//     read the accumulators (tcgen05.ld) and store bf16 rows of `out` in
-//     routed-row order.
+//     read the accumulators (tcgen05.ld) and store bf16 rows of `out`.
+// Every mbarrier wait is bounded (an expired wait records FP4_ERR_TIMEOUT).
 #include <algorithm>
+#include <cstring>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -37,20 +49,28 @@ constexpr int BM = 128;                // rows per MMA (one accumulator)
 constexpr int TM = 2 * BM;             // rows per tile: two MMA halves share each weight slice
 constexpr int BN = 256;
 constexpr int BK = 64;                 // bf16 elements per stage row: 128 bytes
-constexpr int STAGES = 3;
 constexpr int kProducerWarps = 16;
 constexpr int kPD = 2;                 // weight prefetch distance (stages) in the producers' registers
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;  // + MMA warp
 constexpr uint32_t A_HALF = BM * BK * 2;   // 16 KB: one 128-row half of the activations
 constexpr uint32_t A_BYTES = 2 * A_HALF;   // 32 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 2048;
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB per weight term
 constexpr uint32_t TMEM_COLS = 512;        // accumulator of half h at column 256 h
+constexpr int kItems = (BN * 2) / kProducers;  // (row, 32-code half) items per producer thread per stage
+static_assert(kItems == 1, "one weight item per producer thread per stage");
 // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, K-major, N>>3, M>>4
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(BM >> 4) << 24);
+
+// MODE 0 (affine) carries two weight terms per stage and fits two stages; the
+// FP4 formats one term and three stages.
+template <int MODE> struct Cfg {
+  static constexpr int kTerms = MODE == 0 ? 2 : 1;
+  static constexpr int kStages = MODE == 0 ? 2 : 3;
+  static constexpr uint32_t kStageBytes = A_BYTES + kTerms * B_BYTES;
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 2048;
+};
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
@@ -64,15 +84,64 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
-    const uint16_t* __restrict__ x, const int32_t* __restrict__ lhs, const int32_t* __restrict__ rhs,
-    int R, const uint32_t* __restrict__ w, const uint8_t* __restrict__ scales, int E, int N, int K,
+// The weight scale data of one (row, 32-code) item: MXFP4 one E8M0 byte, NVFP4
+// two E4M3 bytes (16 codes each), affine the bf16 scale and bias packed.
+template <int MODE>
+__device__ __forceinline__ uint32_t load_item_scale(const void* scales, const uint16_t* biases, int64_t row,
+                                                    int64_t K, int group, int64_t k0) {
+  if (MODE == 1) return __ldg(static_cast<const uint8_t*>(scales) + row * (K / 32) + k0 / 32);
+  if (MODE == 2) return __ldg(reinterpret_cast<const uint16_t*>(static_cast<const uint8_t*>(scales) + row * (K / 16) + k0 / 16));
+  const int64_t gi = row * (K / group) + k0 / group;
+  return (uint32_t)__ldg(static_cast<const uint16_t*>(scales) + gi) | ((uint32_t)__ldg(biases + gi) << 16);
+}
+
+// Dequantize one item (32 codes) into its 4 swizzled 16-byte chunks of each term.
+template <int MODE>
+__device__ __forceinline__ void dequant_item(uint4 q, uint32_t sc, uint8_t* b_hi, uint8_t* b_lo, int n, int g) {
+  const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t hi[4], lo[4];
+    if (MODE == 0) {
+      const float s = bf16_lo(sc), b = bf16_hi(sc);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const uint32_t byte = (wv[j] >> (8 * bb)) & 0xFFu;
+        // q via the 2^23 magic: exact small integers
+        const float q0 = __fsub_rn(__uint_as_float(0x4B000000u | (byte & 15u)), 8388608.0f);
+        const float q1 = __fsub_rn(__uint_as_float(0x4B000000u | (byte >> 4)), 8388608.0f);
+        const float w0 = __fmaf_rn(q0, s, b), w1 = __fmaf_rn(q1, s, b);
+        const uint32_t h = pack_bf16x2_rn(w0, w1);
+        hi[bb] = h;
+        lo[bb] = pack_bf16x2_rn(__fsub_rn(w0, bf16_lo(h)), __fsub_rn(w1, bf16_hi(h)));
+      }
+    } else {
+      // NVFP4: word j holds codes 8j .. 8j + 7, scale byte (8j) / 16 = j / 2
+      const float scale = (MODE == 1) ? e8m0_to_f32(sc) : e4m3_to_f32((sc >> (8 * (j >> 1))) & 0xFFu);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const uint32_t h2 = e2m1x2_to_f16x2((wv[j] >> (8 * bb)) & 0xFFu);
+        hi[bb] = pack_bf16x2_rn(__fmul_rn(f16_lo_to_f32(h2), scale), __fmul_rn(f16_hi_to_f32(h2), scale));
+      }
+    }
+    *reinterpret_cast<uint4*>(b_hi + sw128(n, g * 4 + j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    if (MODE == 0) *reinterpret_cast<uint4*>(b_lo + sw128(n, g * 4 + j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+template <int MODE, bool DENSE>
+__global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
+    const __grid_constant__ CUtensorMap tmX, const uint16_t* __restrict__ x, const int32_t* __restrict__ lhs,
+    const int32_t* __restrict__ rhs, int R, const uint32_t* __restrict__ w, const void* __restrict__ scales,
+    const uint16_t* __restrict__ biases, const float* __restrict__ gs_w, int E, int N, int K, int group,
     uint16_t* __restrict__ out, unsigned* __restrict__ err, int inject_timeout) {
+  using C = Cfg<MODE>;
+  constexpr int STAGES = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* accum_full = bars + 2 * STAGES;
@@ -87,7 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   const int tile_id = blockIdx.y;
 
   // ---- tile -> (expert, first routed row, row count) --------------------
-  if (warp == 0) {
+  if (DENSE) {
+    if (threadIdx.x == 0) {
+      tile_info[0] = 0;
+      tile_info[1] = tile_id * TM;
+      tile_info[2] = min(TM, R - tile_id * TM);
+    }
+  } else if (warp == 0) {
     int prefix = 0, found = 0, fe = 0, frow = 0, frows = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
@@ -129,17 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], kProducers);
+      mbar_init(&full[s], kProducers + (DENSE ? 1 : 0));  // + the activation tile's byte count
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum_full, 1);
     mbar_init(never, 1);
     fence_barrier_init();
   }
-  // The first CTA checks the routing contract once: every expert id in [0, E)
-  // and non-decreasing.  A row outside it gets no tile (its output row is not
-  // written); the error word reports it as an invalid argument.
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
+  // gather_qmm: the first CTA checks the routing contract once: every expert id
+  // in [0, E) and non-decreasing.  A row outside it gets no tile (its output row
+  // is not written); the error word reports it as an invalid argument.
+  if (!DENSE && blockIdx.x == 0 && blockIdx.y == 0) {
     bool bad = false;
     for (int i = threadIdx.x; i < R; i += blockDim.x) {
       const int e = __ldg(rhs + i);
@@ -151,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   const int expert = tile_info[0];
   if (expert < 0) return;  // uniform: this grid slot has no tile
   const int row0 = tile_info[1], rows = tile_info[2];
-  for (int r = threadIdx.x; r < TM; r += blockDim.x) row_src[r] = (r < rows) ? __ldg(lhs + row0 + r) : 0;
+  if (!DENSE)
+    for (int r = threadIdx.x; r < TM; r += blockDim.x) row_src[r] = (r < rows) ? __ldg(lhs + row0 + r) : 0;
   const int halves = rows > BM ? 2 : 1;  // 128-row halves holding rows (uniform)
   if (warp == kProducerWarps) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -169,27 +245,20 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
     // ---------------------------------------------------------- producers --
     const int t = threadIdx.x;
     const int64_t words_per_row = K / 8;
-    const int64_t groups_per_row = K / 32;
-    const uint32_t* we = w + (int64_t)expert * N * words_per_row;
-    const uint8_t* se = scales + (int64_t)expert * N * groups_per_row;
-    // Each thread dequantizes kItems (row, 32-code group) items per stage.  Their
-    // codes and scales are loaded kPD stages ahead into a register ring, so the
-    // global-memory latency overlaps the dequantization of the stages between.
-    constexpr int kItems = (BN * 2) / kProducers;
-    uint4 qr[kPD + 1][kItems];
-    uint32_t sr[kPD + 1][kItems];
-    auto load_w = [&](int kb, uint4 (&q)[kItems], uint32_t (&sc)[kItems]) {
-#pragma unroll
-      for (int i = 0; i < kItems; ++i) {
-        const int item = t + kProducers * i;
-        const int n = item >> 1, g = item & 1;
-        if (n0 + n < N) {
-          q[i] = ld_stream_v4(we + (int64_t)(n0 + n) * words_per_row + (kb * BK + g * 32) / 8);
-          sc[i] = __ldg(se + (int64_t)(n0 + n) * groups_per_row + kb * 2 + g);
-        } else {
-          q[i] = make_uint4(0, 0, 0, 0);
-          sc[i] = 0;
-        }
+    const int64_t erow0 = (int64_t)expert * N;  // first weight row of this expert
+    const int n = t >> 1, g = t & 1;            // this thread's item: row n, codes 32 g .. 32 g + 31 of a stage
+    const bool nrow_ok = n0 + n < N;
+    const uint32_t* wrow = w + (erow0 + n0 + n) * words_per_row;
+    // codes and scales of the item, kPD stages ahead in a register ring
+    uint4 qr[kPD + 1];
+    uint32_t sr[kPD + 1];
+    auto load_w = [&](int kb, uint4& q, uint32_t& sc) {
+      if (nrow_ok) {
+        q = ld_stream_v4(wrow + (kb * BK + g * 32) / 8);
+        sc = load_item_scale<MODE>(scales, biases, erow0 + n0 + n, K, group, (int64_t)kb * BK + g * 32);
+      } else {
+        q = make_uint4(0, 0, 0, 0);
+        sc = 0;
       }
     };
 #pragma unroll
@@ -204,40 +273,35 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
           const int s = kb % STAGES;
           const int round = kb / STAGES;
           if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
-          const uint32_t a_s = base + s * STAGE_BYTES;
-          uint8_t* b_s = smem + s * STAGE_BYTES + A_BYTES;
-          // activations: up to 256 rows x 8 chunks of 16 bytes (half h at A_HALF h;
-          // a second half with no rows is not copied, its MMA is not issued)
-#pragma unroll
-          for (int i = 0; i < (TM * 8) / kProducers; ++i) {
-            const int idx = t + kProducers * i;
-            const int r = idx >> 3, c = idx & 7;
-            if (r < BM * halves) {
-              const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
-              cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
+          const uint32_t a_s = base + s * C::kStageBytes;
+          uint8_t* b_s = smem + s * C::kStageBytes + A_BYTES;
+          if (DENSE) {
+            // activations: one TMA box of 256 rows x 128 bytes (rows past the matrix read as zeros)
+            if (t == 0) {
+              mbar_arrive_expect_tx(&full[s], (uint32_t)A_BYTES);
+              tma_load_2d(smem + s * C::kStageBytes, &tmX, &full[s], kb * BK, row0);
             }
-          }
-          asm volatile("cp.async.commit_group;" ::: "memory");
-          // weights: 256 rows x 2 groups of 32 codes, dequantized to bf16 (exact)
+          } else {
+            // activations: up to 256 rows x 8 chunks of 16 bytes (half h at A_HALF h;
+            // a second half with no rows is not copied, its MMA is not issued)
 #pragma unroll
-          for (int i = 0; i < kItems; ++i) {
-            const int item = t + kProducers * i;
-            const int n = item >> 1, g = item & 1;
-            const float sc = e8m0_to_f32(sr[u][i]);
-            const uint32_t wv[4] = {qr[u][i].x, qr[u][i].y, qr[u][i].z, qr[u][i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int bb = 0; bb < 4; ++bb) {
-                const uint32_t h2 = e2m1x2_to_f16x2((wv[j] >> (8 * bb)) & 0xFFu);
-                pk[bb] = pack_bf16x2_rn(__fmul_rn(f16_lo_to_f32(h2), sc), __fmul_rn(f16_hi_to_f32(h2), sc));
+            for (int i = 0; i < (TM * 8) / kProducers; ++i) {
+              const int idx = t + kProducers * i;
+              const int r = idx >> 3, c = idx & 7;
+              if (r < BM * halves) {
+                const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
+                cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
               }
-              *reinterpret_cast<uint4*>(b_s + sw128(n, g * 4 + j)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            asm volatile("cp.async.commit_group;" ::: "memory");
           }
-          // stage kb-1 is complete once its copies landed: publish it
-          if (kb > 0) {
+          // weights: 256 rows x 2 items of 32 codes, dequantized to bf16 (one or two terms)
+          dequant_item<MODE>(qr[u], sr[u], b_s, b_s + B_BYTES, n, g);
+          if (DENSE) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&full[s]);
+          } else if (kb > 0) {
+            // stage kb-1 is complete once its copies landed: publish it
             asm volatile("cp.async.wait_group 1;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(&full[(kb - 1) % STAGES]);
@@ -245,9 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
         }
       }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive(&full[(num_kb - 1) % STAGES]);
+    if (!DENSE) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&full[(num_kb - 1) % STAGES]);
+    }
   } else {
     // ------------------------------------------------------------ MMA warp --
     if (elect_one_sync()) {
@@ -259,18 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
         const int s = kb % STAGES;
         mbar_wait(&full[s], (kb / STAGES) & 1, err, failed);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t adesc = desc_sw128(base + s * STAGE_BYTES);
-        const uint64_t bdesc = desc_sw128(base + s * STAGE_BYTES + A_BYTES);
+        const uint64_t adesc = desc_sw128(base + s * C::kStageBytes);
+        const uint64_t bdesc = desc_sw128(base + s * C::kStageBytes + A_BYTES);
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
-          const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-          for (int hh = 0; hh < halves; ++hh)  // half hh: its 128 rows (16 KB further), its accumulator
-            asm volatile(
-                "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                :: "r"(tmem + 256u * hh), "l"(adesc + (uint64_t)(2 * k + (A_HALF >> 4) * hh)),
-                   "l"(bdesc + (uint64_t)(2 * k)), "r"(IDESC), "r"(acc)
-                : "memory");
+#pragma unroll
+          for (int tt = 0; tt < C::kTerms; ++tt) {
+            const uint32_t acc = (kb > 0 || k > 0 || tt > 0) ? 1u : 0u;
+            for (int hh = 0; hh < halves; ++hh)  // half hh: its 128 rows (16 KB further), its accumulator
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                  :: "r"(tmem + 256u * hh), "l"(adesc + (uint64_t)(2 * k + (A_HALF >> 4) * hh)),
+                     "l"(bdesc + (uint64_t)(2 * k + (B_BYTES >> 4) * tt)), "r"(IDESC), "r"(acc)
+                  : "memory");
+          }
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(smem_u32(&empty[s])) : "memory");
@@ -284,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   if (warp < 4 * halves) {
     mbar_wait(accum_full, 0, err, failed);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const float gsw = (MODE == 2 && gs_w) ? __ldg(gs_w) : 1.0f;
     const int q = warp & 3, hh = warp >> 2;  // lane quadrant, half
     const int r = BM * hh + 32 * q + lane;
     uint16_t* orow = out + (int64_t)(row0 + r) * N;
@@ -298,17 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       const int col = n0 + c;
       if (r < rows) {
-        uint4 o0, o1;
-        o0.x = pack_bf16x2_rn(__uint_as_float(v[0]), __uint_as_float(v[1]));
-        o0.y = pack_bf16x2_rn(__uint_as_float(v[2]), __uint_as_float(v[3]));
-        o0.z = pack_bf16x2_rn(__uint_as_float(v[4]), __uint_as_float(v[5]));
-        o0.w = pack_bf16x2_rn(__uint_as_float(v[6]), __uint_as_float(v[7]));
-        o1.x = pack_bf16x2_rn(__uint_as_float(v[8]), __uint_as_float(v[9]));
-        o1.y = pack_bf16x2_rn(__uint_as_float(v[10]), __uint_as_float(v[11]));
-        o1.z = pack_bf16x2_rn(__uint_as_float(v[12]), __uint_as_float(v[13]));
-        o1.w = pack_bf16x2_rn(__uint_as_float(v[14]), __uint_as_float(v[15]));
-        if (col < N) *reinterpret_cast<uint4*>(orow + col) = o0;
-        if (col + 8 < N) *reinterpret_cast<uint4*>(orow + col + 8) = o1;
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          o[e] = pack_bf16x2_rn(__fmul_rn(__uint_as_float(v[2 * e]), gsw), __fmul_rn(__uint_as_float(v[2 * e + 1]), gsw));
+        if (col < N) *reinterpret_cast<uint4*>(orow + col) = make_uint4(o[0], o[1], o[2], o[3]);
+        if (col + 8 < N) *reinterpret_cast<uint4*>(orow + col + 8) = make_uint4(o[4], o[5], o[6], o[7]);
       }
     }
   }
@@ -320,22 +385,61 @@ __global__ void __launch_bounds__(kThreads, 1) gather_qmm_kernel(
   }
 }
 
+template <int MODE, bool DENSE>
+cudaError_t launch_w4a16(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
+                         const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w, int64_t E,
+                         int64_t N, int64_t K, int group, uint16_t* out, int inject, cudaStream_t s) {
+  using C = Cfg<MODE>;
+  if (C::kSmemBytes > d.smem_optin) return cudaErrorInvalidValue;
+  CUtensorMap tmX;
+  memset(&tmX, 0, sizeof(tmX));
+  if (DENSE) {
+    // activations [R, K] bf16: boxes of 256 rows x 64 elements (128 bytes), 128-byte swizzle
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)TM};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(w4a16_kernel<MODE, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t m_tiles = DENSE ? (R + TM - 1) / TM : (R + TM - 1) / TM + E;  // gather: upper bound on per-expert tiles
+  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)m_tiles);
+  w4a16_kernel<MODE, DENSE><<<grid, kThreads, C::kSmemBytes, s>>>(tmX, x, lhs, rhs, (int)R, w, scales, biases, gs_w,
+                                                                   (int)E, (int)N, (int)K, group, out, d.err, inject);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs,
-                              const int32_t* rhs, int64_t R, const uint32_t* w,
-                              const uint8_t* scales, int64_t E, int64_t N, int64_t K, int mode,
-                              uint16_t* out, int inject_timeout, cudaStream_t s) {
-  (void)mode;
-  if (SMEM_BYTES > d.smem_optin) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gather_qmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const int64_t m_tiles = (R + TM - 1) / TM + E;  // upper bound on per-expert tiles
-  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)m_tiles);
-  gather_qmm_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(x, lhs, rhs, (int)R, w, scales, (int)E, (int)N,
-                                                       (int)K, out, d.err, inject_timeout);
-  return cudaGetLastError();
+cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
+                              const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w,
+                              int64_t E, int64_t N, int64_t K, int mode, int group, uint16_t* out, int inject_timeout,
+                              cudaStream_t s) {
+  if (mode == 1)
+    return launch_w4a16<1, false>(d, x, lhs, rhs, R, w, scales, biases, gs_w, E, N, K, group, out, inject_timeout, s);
+  if (mode == 2)
+    return launch_w4a16<2, false>(d, x, lhs, rhs, R, w, scales, biases, gs_w, E, N, K, group, out, inject_timeout, s);
+  return launch_w4a16<0, false>(d, x, lhs, rhs, R, w, scales, biases, gs_w, E, N, K, group, out, inject_timeout, s);
+}
+
+cudaError_t launch_qmm(const DevInfo& d, const uint16_t* x, int64_t M, const uint32_t* w, const void* scales,
+                       const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode, int group,
+                       uint16_t* out, int inject_timeout, cudaStream_t s) {
+  if (mode == 1)
+    return launch_w4a16<1, true>(d, x, nullptr, nullptr, M, w, scales, biases, gs_w, 1, N, K, group, out,
+                                 inject_timeout, s);
+  if (mode == 2)
+    return launch_w4a16<2, true>(d, x, nullptr, nullptr, M, w, scales, biases, gs_w, 1, N, K, group, out,
+                                 inject_timeout, s);
+  return launch_w4a16<0, true>(d, x, nullptr, nullptr, M, w, scales, biases, gs_w, 1, N, K, group, out,
+                               inject_timeout, s);
 }
 
 }  // namespace fp4

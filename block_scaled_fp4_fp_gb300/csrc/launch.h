@@ -26,9 +26,10 @@ int current_device_info(const DevInfo** out);
 size_t amax_workspace_bytes(int64_t n);
 cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* gs_out,
                         float* amax_out, uint32_t* partials, int max_partials, cudaStream_t s);
+// sr != 0: stochastic rounding of the elements (Philox4x32-10 words from seed and offset)
 cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, int64_t cols,
                             int mode, int group, const float* gs, uint32_t* xq, uint8_t* scales,
-                            int tiled, cudaStream_t s);
+                            int tiled, int sr, uint64_t seed, uint64_t offset, cudaStream_t s);
 cudaError_t launch_dequantize(const DevInfo& d, const uint32_t* wq, const void* scales,
                               const uint16_t* biases, int64_t rows, int64_t cols, int mode,
                               int group, const float* gs, int tiled, uint16_t* out,
@@ -66,10 +67,15 @@ cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
 cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint8_t* scales, int64_t N,
                                  int64_t K, cudaStream_t s);
 
-// gather_qmm.cu
-cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs,
-                              const int32_t* rhs, int64_t R, const uint32_t* w,
-                              const uint8_t* scales, int64_t E, int64_t N, int64_t K, int mode,
-                              uint16_t* out, int inject_timeout, cudaStream_t s);
+// gather_qmm.cu: W4A16 GEMMs (MXFP4 = 1, NVFP4 = 2, affine = 0 weights) -- the MoE
+// gather_qmm (rows sorted by expert) and the dense qmm (gs_w: NVFP4 weight global
+// scale or nullptr; biases: affine only)
+cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
+                              const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w,
+                              int64_t E, int64_t N, int64_t K, int mode, int group, uint16_t* out, int inject_timeout,
+                              cudaStream_t s);
+cudaError_t launch_qmm(const DevInfo& d, const uint16_t* x, int64_t M, const uint32_t* w, const void* scales,
+                       const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode, int group,
+                       uint16_t* out, int inject_timeout, cudaStream_t s);
 
 }  // namespace fp4

@@ -86,10 +86,65 @@ __global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __
 // within a row, blockIdx.y strides over rows (two rows per thread in flight);
 // no index needs a division.  Codes leave as 8/16 contiguous bytes per thread.
 // Blocks with blockIdx.x >= main_bx zero the padding of a tiled scale buffer.
-template <int MODE>
+// ------------------------------------------------- stochastic rounding --
+// Random words: element e (row-major index) takes word e % 4 of Philox4x32-10
+// (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3") at the 128-bit
+// counter offset + e / 4 under the key (seed low, seed high).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t offset, uint64_t block) {
+  const uint64_t b = offset + block;
+  return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), b < offset ? 1u : 0u, 0u), (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+
+// Stochastic e2m1 rounding: |v| goes to one of its two grid neighbours lo < hi,
+// up iff the top 24 bits of u are below floor(2^24 (|v| - lo) / (hi - lo));
+// |v| >= 6 gives 6; the sign bit is kept.  Every step is exact in fp32.
+__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
+  const float a = fabsf(v);
+  uint32_t idx;
+  if (!(a < 6.0f)) {
+    idx = 7;
+  } else {
+    uint32_t li;
+    float lo, inv_step;
+    if (a < 2.0f) {
+      li = __float2uint_rz(__fmul_rn(a, 2.0f));  // 0..3, steps of 0.5
+      lo = __fmul_rn((float)li, 0.5f);
+      inv_step = 2.0f;
+    } else if (a < 4.0f) {
+      const uint32_t f = __float2uint_rz(a);     // 2 or 3, steps of 1
+      li = f + 2u;
+      lo = (float)f;
+      inv_step = 1.0f;
+    } else {
+      li = 6u;                                   // 4, step of 2 to 6
+      lo = 4.0f;
+      inv_step = 0.5f;
+    }
+    const float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);
+    const uint32_t t = __float2uint_rz(__fmul_rn(frac, 16777216.0f));
+    idx = li + (((u >> 8) < t) ? 1u : 0u);
+  }
+  return idx | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+template <int MODE, bool SR>
 __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 4], float gs,
                                                uint32_t* __restrict__ xq_words,
-                                               uint8_t* __restrict__ scale_byte) {
+                                               uint8_t* __restrict__ scale_byte, uint64_t e0,
+                                               uint64_t seed, uint64_t offset) {
   constexpr int NV = (MODE == 2) ? 2 : 4;
   uint32_t m2 = 0;
 #pragma unroll
@@ -108,9 +163,18 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
   for (int i = 0; i < NV; ++i) {
     const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t word = 0;
+    if (SR) {  // 8 elements e0 + 8 i .. : two Philox blocks of four words
+      const uint4 r0 = sr_words(seed, offset, (e0 >> 2) + 2 * i), r1 = sr_words(seed, offset, (e0 >> 2) + 2 * i + 1);
+      const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
+      for (int j = 0; j < 4; ++j)
+        word |= (e2m1_sr(__fmul_rn(bf16_lo(wv[j]), mul), u[2 * j]) |
+                 (e2m1_sr(__fmul_rn(bf16_hi(wv[j]), mul), u[2 * j + 1]) << 4)) << (8 * j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
+    }
     out[i] = word;
   }
   if (MODE == 2) {
@@ -121,11 +185,11 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
   *scale_byte = (uint8_t)sbyte;
 }
 
-template <int MODE>
+template <int MODE, bool SR>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(
     const uint16_t* __restrict__ x, int rows, int cols, const float* __restrict__ gs_ptr,
     uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, int tiled, int padded_rows,
-    int padded_cols, int main_bx) {
+    int padded_cols, int main_bx, uint64_t seed, uint64_t offset) {
   constexpr int G = (MODE == 2) ? 16 : 32;
   constexpr int NV = G / 8;
   constexpr int RT = (MODE == 2) ? 4 : 2;  // rows in flight per thread (64 or 128 bytes... 128 bytes)
@@ -166,8 +230,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(
     for (int k = 0; k < RT; ++k) {
       const int rk = r + k * gy;
       if (rk < rows)
-        quantize_group<MODE>(a[k], gs, xq + (int64_t)rk * wpr + gi * NV,
-                             scales + (tiled ? tiled_scale_offset(rk, gi, padded_cols) : (int64_t)rk * scols + gi));
+        quantize_group<MODE, SR>(a[k], gs, xq + (int64_t)rk * wpr + gi * NV,
+                                 scales + (tiled ? tiled_scale_offset(rk, gi, padded_cols) : (int64_t)rk * scols + gi),
+                                 (uint64_t)rk * (uint64_t)cols + (uint64_t)gi * G, seed, offset);
     }
   }
 }
@@ -235,7 +300,7 @@ cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* g
 
 cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, int64_t cols,
                             int mode, int group, const float* gs, uint32_t* xq, uint8_t* scales,
-                            int tiled, cudaStream_t s) {
+                            int tiled, int sr, uint64_t seed, uint64_t offset, cudaStream_t s) {
   const int64_t scols = cols / group;
   const int64_t main_bx = (scols + kQThreads - 1) / kQThreads;
   const int64_t prow = ((rows + 127) / 128) * 128, pcol = ((scols + 3) / 4) * 4;
@@ -251,12 +316,18 @@ cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, i
     pad_bx = std::min<int64_t>(std::max<int64_t>((pad + kQThreads * gy - 1) / (kQThreads * gy), 1), 64);
   }
   dim3 grid((unsigned)(main_bx + pad_bx), (unsigned)gy);
-  if (mode == 2)
-    quantize_kernel<2><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, gs, xq, scales, tiled, (int)prow,
-                                                  (int)pcol, (int)main_bx);
+  if (mode == 2 && sr)
+    quantize_kernel<2, true><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, gs, xq, scales, tiled, (int)prow,
+                                                        (int)pcol, (int)main_bx, seed, offset);
+  else if (mode == 2)
+    quantize_kernel<2, false><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, gs, xq, scales, tiled, (int)prow,
+                                                         (int)pcol, (int)main_bx, 0, 0);
+  else if (sr)
+    quantize_kernel<1, true><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, nullptr, xq, scales, tiled,
+                                                        (int)prow, (int)pcol, (int)main_bx, seed, offset);
   else
-    quantize_kernel<1><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, nullptr, xq, scales, tiled,
-                                                  (int)prow, (int)pcol, (int)main_bx);
+    quantize_kernel<1, false><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, nullptr, xq, scales, tiled,
+                                                         (int)prow, (int)pcol, (int)main_bx, 0, 0);
   return cudaGetLastError();
 }
 

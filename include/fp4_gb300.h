@@ -122,6 +122,24 @@ fp4_status fp4_quantize(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode 
                         int group_size, const float* global_scale, uint32_t* xq, uint8_t* scales,
                         fp4_scale_layout layout, cudaStream_t stream);
 
+/* fp_quantize with stochastic rounding [P1: the NVFP4/MXFP4 quantizer's USE_SR
+ * template parameter, which needs the Blackwell converters; the pages state
+ * neither the rule nor the random numbers, so both are fixed here].
+ * Arguments as fp4_quantize, plus seed and offset.  Block scales are exactly
+ * fp4_quantize's.  Each element v = x * mul (mul as fp4_quantize) is rounded to
+ * one of its two e2m1 neighbours lo <= |v| < hi: up when the top 24 bits of its
+ * random word are below floor(2^24 (|v| - lo) / (hi - lo)), so the expected
+ * value is v (to 2^-24 of the step); |v| >= 6 gives 6 and the sign is kept.
+ * The random word of element e = r * cols + c is word e % 4 of Philox4x32-10
+ * (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3", SC 2011) at
+ * the 128-bit counter offset + floor(e / 4) (32-bit words little-endian) under
+ * the key (low 32 bits of seed, high 32 bits): independent of the launch
+ * configuration, so a call is reproducible, and successive calls that advance
+ * offset by ceil(rows * cols / 4) never reuse a word. */
+fp4_status fp4_quantize_sr(const fp4_bf16* x, int64_t rows, int64_t cols, fp4_mode mode, int bits,
+                           int group_size, const float* global_scale, uint64_t seed, uint64_t offset, uint32_t* xq,
+                           uint8_t* scales, fp4_scale_layout layout, cudaStream_t stream);
+
 /* a5: fp_dequantize / affine_dequantize [P3 quantized.cpp].
  *   wq      uint32[rows, cols/8]
  *   scales  NVFP4/MXFP4: uint8 block scales in `layout`; affine: bf16[rows, cols/group]
@@ -195,19 +213,39 @@ fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const
  *   lhs_idx  int32[R] activation row of each routed row
  *   rhs_idx  int32[R] expert of each routed row, in [0, E)
  *   w        uint32[E, N, K/8], 16-byte aligned
- *   scales   uint8[E, N, K/group] linear block scales
- *   biases   must be NULL
+ *   scales   MXFP4 uint8[E, N, K/32] E8M0, NVFP4 uint8[E, N, K/16] E4M3 (no global
+ *            scale), affine bf16[E, N, K/group]; linear layout, 2-byte aligned
+ *   biases   affine: bf16[E, N, K/group]; NULL otherwise
  *   out      bf16[R, N], 16-byte aligned
- * mode MXFP4 (group 32).  sorted != 0 promises rhs_idx is non-decreasing (rows
- * grouped by expert), which this version requires.  Requires K % 64 == 0 and
- * N % 16 == 0.  The expert ids live in device memory, so the kernel checks them:
- * an id outside [0, E) or a decrease leaves the affected output rows unwritten
- * and makes the next fp4_check_device_error return FP4_ERR_INVALID_ARG.
- * lhs_idx values must lie in [0, T); they are not checked. */
+ * sorted != 0 promises rhs_idx is non-decreasing (rows grouped by expert), which
+ * this version requires.  Requires K % 64 == 0 and N % 16 == 0.  The expert ids
+ * live in device memory, so the kernel checks them: an id outside [0, E) or a
+ * decrease leaves the affected output rows unwritten and makes the next
+ * fp4_check_device_error return FP4_ERR_INVALID_ARG.  lhs_idx values must lie in
+ * [0, T); they are not checked. */
 fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* rhs_idx, int64_t R,
                       const uint32_t* w, const void* scales, const fp4_bf16* biases, int64_t E,
                       int64_t N, int64_t K, fp4_mode mode, int bits, int group_size, int sorted,
                       fp4_bf16* out, cudaStream_t stream);
+
+/* qmm: the dense prefill GEMM with 4-bit weights and bf16 activations (W4A16)
+ * ["mlx: opt-in dense GEMM for nvfp4 prefill ... - #287": the mixed-input GEMM
+ * of bf16 activations against NVFP4 weights at M > 1; "perf(cuda): enable
+ * hardware NVFP4/MXFP4 conversion on Blackwell builds": qmm_sm80].
+ *   out[m, n] = sum_k x[m, k] * deq(W)[n, k]   (fp32 accumulation, bf16 output)
+ *   x        bf16[M, K], 16-byte aligned
+ *   w        uint32[N, K/8] (W stored [N, K]), 16-byte aligned
+ *   scales   linear block scales: NVFP4 uint8[N, K/16], MXFP4 uint8[N, K/32], affine
+ *            bf16[N, K/group]; 2-byte aligned
+ *   biases   affine: bf16[N, K/group]; NULL otherwise
+ *   global_scale_w NVFP4 only: device fp32 gs of W (applied to the fp32 sums), or NULL
+ *   out      bf16[M, N], 16-byte aligned
+ * The weights are dequantized exactly (FP4: e2m1 * block scale is exact in bf16;
+ * affine: q * scale + bias in fp32 carried as two bf16 terms).  Requires
+ * K % 64 == 0 and N % 16 == 0. */
+fp4_status qmm(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
+               const float* global_scale_w, int64_t M, int64_t N, int64_t K, fp4_mode mode, int bits, int group_size,
+               fp4_bf16* out, cudaStream_t stream);
 
 /* Maximum element count accepted by fp4_amax_global_scale_noalloc (2^36). */
 #define FP4_AMAX_NOALLOC_MAX_ELEMS ((int64_t)1 << 36)

@@ -91,6 +91,8 @@ def lib():
                                    c.c_int, P(i64), i64, P(f64)]),
                 "orc_qqmm": (None, [P(u32), P(u8), P(u32), P(u8), f32, i64, i64, i64, c.c_int,
                                     P(i64), i64, P(i64), i64, P(f64)]),
+                "orc_qmm": (None, [P(u16), i64, P(u32), c.c_void_p, P(u16), P(f32), i64, i64, c.c_int, c.c_int,
+                                   P(i64), i64, P(f64)]),
                 "orc_gather_qmm": (None, [P(u16), P(i32), P(i32), i64, P(u32), c.c_void_p, P(u16),
                                           i64, i64, i64, c.c_int, c.c_int, P(i64), i64, P(f64)]),
                 "orc_num_threads": (c.c_int, []),
@@ -345,6 +347,23 @@ def qqmm(xq, sx, wq, sw, mode, alpha=1.0, mrows=None, ncols=None):
     lib().orc_qqmm(_p(xq, ctypes.c_uint32), _p(sx, ctypes.c_uint8), _p(wq, ctypes.c_uint32),
                    _p(sw, ctypes.c_uint8), float(alpha), M, N, K, mode, _p(mr, ctypes.c_int64), om,
                    _p(nc, ctypes.c_int64), on, _p(out, ctypes.c_double))
+    return out
+
+
+def qmm(x, w, scales, biases, mode, group, gs_w=None, rows=None):
+    """out[i] = x[rows[i]] . deq(W)^T in fp64 (all rows of x when ``rows`` is None);
+    x is [M, K] bf16 bits, W [N, K/8] packed."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint32)
+    M, K = x.shape
+    N = w.shape[0]
+    s, sp = _scales_arg(mode, scales)
+    b = _c(biases, np.uint16) if biases is not None else None
+    r = _c(rows, np.int64) if rows is not None else None
+    om = len(r) if r is not None else M
+    out = np.zeros((om, N), np.float64)
+    lib().orc_qmm(_p(x, ctypes.c_uint16), M, _p(w, ctypes.c_uint32), sp, _p(b, ctypes.c_uint16), _f32p(gs_w), N, K,
+                  mode, group, _p(r, ctypes.c_int64), om, _p(out, ctypes.c_double))
     return out
 
 

@@ -544,6 +544,28 @@ void orc_qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const u
   }
 }
 
+/* qmm, the dense W4A16 GEMM ["mlx: opt-in dense GEMM for nvfp4 prefill ..." and
+ * qmm_sm80 in "perf(cuda): enable hardware NVFP4/MXFP4 conversion on Blackwell
+ * builds"]: out[i, n] = sum_k x[m_i, k] * deq(W)[n, k] in fp64 over the listed
+ * rows m_i of x (NULL means all M rows), every column n; deq includes the NVFP4
+ * weight global scale.  x is [M, K] bf16, W [N, K] packed. */
+void orc_qmm(const uint16_t* x, int64_t M, const uint32_t* w, const void* scales, const uint16_t* biases,
+             const float* global_scale_w, int64_t N, int64_t K, int mode, int group,
+             const int64_t* rows, int64_t nrows, double* out) {
+  const double gs = global_scale_w ? (double)*global_scale_w : 1.0;
+  const int64_t om = rows ? nrows : M;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < om; ++i) {
+    const uint16_t* xr = x + (rows ? rows[i] : i) * K;
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += orc_bf16_to_double(xr[k]) * deq_exact(w, scales, biases, n, k, K, mode, group, gs);
+      out[i * N + n] = acc;
+    }
+  }
+}
+
 /* gather_qmm [P2 Diagnosis 1 and 5: gather_gemm / grouped GEMM for MoE]: each
  * routed row r multiplies activation row lhs[r] by expert rhs[r]'s weights. */
 void orc_gather_qmm(const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,

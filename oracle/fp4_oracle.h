@@ -88,6 +88,11 @@ void orc_qmv(const uint16_t* x, const uint32_t* w, const void* scales, const uin
 void orc_qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
               float alpha, int64_t M, int64_t N, int64_t K, int mode,
               const int64_t* mrows, int64_t nm, const int64_t* ncols, int64_t nn, double* out);
+/* out[i, n] = sum_k x[m_i, k] * deq(W)[n, k] (with the NVFP4 weight global scale) over
+ * the listed rows m_i of x [M, K] (NULL means all), every column n. */
+void orc_qmm(const uint16_t* x, int64_t M, const uint32_t* w, const void* scales, const uint16_t* biases,
+             const float* global_scale_w, int64_t N, int64_t K, int mode, int group,
+             const int64_t* rows, int64_t nrows, double* out);
 /* out[i, n] = sum_k x[lhs[r_i], k] * deq(W[rhs[r_i]])[n, k] for the listed routed
  * rows r_i (NULL means all R), all N columns.  W is [E, N, K] packed. */
 void orc_gather_qmm(const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,

@@ -85,5 +85,15 @@ def test_validation_rejects_before_launch(B):
     assert L.qqmv(p, None, p, p, None, 64, 48, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG  # K % 32
     assert L.qqmv(p, None, p, p, None, 0, 64, B.MODE_NVFP4, p, None) == B.FP4_ERR_INVALID_ARG
     assert L.qqmv(odd, None, p, p, None, 64, 64, B.MODE_NVFP4, p, None) == B.FP4_ERR_ALIGNMENT
+    assert L.fp4_quantize_sr(p, 4, 64, B.MODE_AFFINE, 4, 64, None, 1, 0, p, p, 0, None) == B.FP4_ERR_UNSUPPORTED
+    assert L.fp4_quantize_sr(p, 4, 40, B.MODE_NVFP4, 4, 16, None, 1, 0, p, p, 0, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize_sr(p, 4, 64, B.MODE_MXFP4, 4, 32, p, 1, 0, p, p, 0, None) == B.FP4_ERR_INVALID_ARG
+    assert L.fp4_quantize_sr(odd, 4, 64, B.MODE_NVFP4, 4, 16, None, 1, 0, p, p, 0, None) == B.FP4_ERR_ALIGNMENT
+    assert L.qmm(p, p, p, None, None, 4, 16, 96, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_INVALID_ARG  # K % 64
+    assert L.qmm(p, p, p, None, None, 4, 24, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_INVALID_ARG  # N % 16
+    assert L.qmm(p, p, p, None, None, 0, 16, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_INVALID_ARG  # M = 0
+    assert L.qmm(p, p, p, None, None, 4, 16, 64, B.MODE_AFFINE, 4, 64, p, None) == B.FP4_ERR_INVALID_ARG  # no biases
+    assert L.qmm(p, p, p, None, p, 4, 16, 64, B.MODE_MXFP4, 4, 32, p, None) == B.FP4_ERR_INVALID_ARG  # gs w/ MXFP4
+    assert L.qmm(odd, p, p, None, None, 4, 16, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_ALIGNMENT
     assert L.fp4_debug_stream_weights(p, p, 64, 320, None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.fp4_debug_stream_weights(odd, p, 64, 256, None) == B.FP4_ERR_ALIGNMENT
