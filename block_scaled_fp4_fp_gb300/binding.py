@@ -46,6 +46,8 @@ SIGNATURES = {
     "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
+    "qqmm_batched": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                            _INT, _VP, _VP]),
     "qmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
     "fp4_debug_inject_wait_timeout": (_INT, [_INT]),
     "fp4_debug_stream_weights": (_INT, [_VP, _VP, _I64, _I64, _VP]),
@@ -208,6 +210,22 @@ def qqmm(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor,
         out = torch.empty((M, N), dtype=torch.bfloat16, device=wq.device)
     _check(lib().qqmm(_p(xq), _p(sx), _p(wq), _p(sw), _p(global_scale_x), _p(global_scale_w), M, N, K, mode,
                       _p(out), _s(stream)), "qqmm")
+    return out
+
+
+def qqmm_batched(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor, global_scale_x=None,
+                 global_scale_w=None, mode: int = MODE_NVFP4, out=None, stream=None):
+    """Batched FP4 x FP4 GEMM: xq [B, M, K/8] and its tiled scales [B, Mp, Cp];
+    wq [B, N, K/8] (or [N, K/8], shared) and scales; out [B, M, N]; global
+    scales as [B] arrays or None."""
+    Bt, M, K = xq.shape[0], xq.shape[1], xq.shape[2] * 8
+    shared = wq.dim() == 2
+    N = wq.shape[-2]
+    if out is None:
+        out = torch.empty((Bt, M, N), dtype=torch.bfloat16, device=wq.device)
+    _check(lib().qqmm_batched(_p(xq), _p(sx), _p(wq), _p(sw), _p(global_scale_x), _p(global_scale_w), Bt, M, N, K,
+                              xq.stride(0), sx.stride(0), 0 if shared else wq.stride(0), 0 if shared else sw.stride(0),
+                              out.stride(0), mode, _p(out), _s(stream)), "qqmm_batched")
     return out
 
 

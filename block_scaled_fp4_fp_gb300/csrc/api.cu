@@ -240,13 +240,27 @@ fp4_status qqmv(const fp4_bf16* x, const float* global_scale_x, const uint32_t* 
                               g_inject_timeout.load(), stream));
 }
 
-fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
-                const float* global_scale_x, const float* global_scale_w, int64_t M, int64_t N, int64_t K,
-                fp4_mode mode, fp4_bf16* out, cudaStream_t stream) {
+namespace {
+fp4_status qqmm_common(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
+                       const float* global_scale_x, const float* global_scale_w, int64_t M, int64_t N, int64_t K,
+                       const BatchArgs& ba, fp4_mode mode, fp4_bf16* out, cudaStream_t stream) {
   if (mode != FP4_MODE_NVFP4 && mode != FP4_MODE_MXFP4) return FP4_ERR_UNSUPPORTED;
   if (!xq || !sx || !wq || !sw || !out || M <= 0 || N <= 0 || K <= 0) return FP4_ERR_INVALID_ARG;
   if (K % 256 != 0 || N % 8 != 0 || M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > (1 << 24))
     return FP4_ERR_INVALID_ARG;
+  if (ba.batch < 1 || ba.batch > 65535) return FP4_ERR_INVALID_ARG;
+  if (ba.batch > 1) {
+    const int group = mode == FP4_MODE_NVFP4 ? 16 : 32;
+    int64_t prm = 0, pcm = 0, prn = 0, pcn = 0;
+    fp4_padded_scale_dims(M, K / group, &prm, &pcm);
+    fp4_padded_scale_dims(N, K / group, &prn, &pcn);
+    // every batch's operands lie apart (W and its scales may be shared: stride 0)
+    if (ba.stride_xq < M * (K / 8) || ba.stride_sx < prm * pcm || ba.stride_out < M * N) return FP4_ERR_INVALID_ARG;
+    if ((ba.stride_wq != 0 && ba.stride_wq < N * (K / 8)) || (ba.stride_sw != 0 && ba.stride_sw < prn * pcn))
+      return FP4_ERR_INVALID_ARG;
+    if (ba.stride_xq % 4 || ba.stride_wq % 4 || ba.stride_sx % 16 || ba.stride_sw % 16 || ba.stride_out % 8)
+      return FP4_ERR_ALIGNMENT;
+  }
   if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(sx, 16) || !aligned(sw, 16) || !aligned(out, 16))
     return FP4_ERR_ALIGNMENT;
   if ((global_scale_x && !aligned(global_scale_x, 4)) || (global_scale_w && !aligned(global_scale_w, 4)))
@@ -254,8 +268,29 @@ fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const
   const DevInfo* d = nullptr;
   fp4_status st = current(&d);
   if (st != FP4_OK) return st;
-  return from_cuda(launch_qqmm(*d, xq, sx, wq, sw, global_scale_x, global_scale_w, M, N, K, mode, out,
+  return from_cuda(launch_qqmm(*d, xq, sx, wq, sw, global_scale_x, global_scale_w, M, N, K, ba, mode, out,
                                g_inject_timeout.load(), stream));
+}
+}  // namespace
+
+fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
+                const float* global_scale_x, const float* global_scale_w, int64_t M, int64_t N, int64_t K,
+                fp4_mode mode, fp4_bf16* out, cudaStream_t stream) {
+  return qqmm_common(xq, sx, wq, sw, global_scale_x, global_scale_w, M, N, K, BatchArgs{}, mode, out, stream);
+}
+
+fp4_status qqmm_batched(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
+                        const float* global_scale_x, const float* global_scale_w, int64_t batch, int64_t M,
+                        int64_t N, int64_t K, int64_t stride_xq, int64_t stride_sx, int64_t stride_wq,
+                        int64_t stride_sw, int64_t stride_out, fp4_mode mode, fp4_bf16* out, cudaStream_t stream) {
+  BatchArgs ba;
+  ba.batch = batch;
+  ba.stride_xq = stride_xq;
+  ba.stride_sx = stride_sx;
+  ba.stride_wq = stride_wq;
+  ba.stride_sw = stride_sw;
+  ba.stride_out = stride_out;
+  return qqmm_common(xq, sx, wq, sw, global_scale_x, global_scale_w, M, N, K, ba, mode, out, stream);
 }
 
 namespace {

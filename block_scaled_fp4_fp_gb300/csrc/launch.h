@@ -57,10 +57,16 @@ cudaError_t launch_qmv_affine(const DevInfo& d, const uint16_t* x, const uint32_
                               const uint16_t* biases, int64_t N, int64_t K, int group, uint16_t* y,
                               cudaStream_t s);
 
-// qqmm.cu
+// qqmm.cu: batch b reads xq + b stride_xq (uint32 words), sx + b stride_sx (bytes),
+// wq + b stride_wq (0: one W for every batch), sw + b stride_sw, gs_x[b], gs_w[b],
+// and writes out + b stride_out (elements); a plain call is batch 1.
+struct BatchArgs {
+  int64_t batch = 1;
+  int64_t stride_xq = 0, stride_sx = 0, stride_wq = 0, stride_sw = 0, stride_out = 0;
+};
 cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
                         const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
-                        int64_t N, int64_t K, int mode, uint16_t* out, int inject_timeout,
+                        int64_t N, int64_t K, const BatchArgs& ba, int mode, uint16_t* out, int inject_timeout,
                         cudaStream_t s);
 
 // weight_stream.cu (measurement aid: the GEMV's weight stream without the GEMV)

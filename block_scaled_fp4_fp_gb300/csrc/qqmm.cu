@@ -118,11 +118,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Batch b of a batched call reads its x codes at z = b (x) and z = b * wz (W:
+// wz = 0 when every batch shares W), its scale tiles at b * stride_sx and
+// b * stride_sw bytes, its global scales gs_x[b], gs_w[b], and writes out + b *
+// stride_out.
+struct Batch {
+  int count = 1;
+  int wz = 1;
+  int64_t stride_sx = 0, stride_sw = 0, stride_out = 0;
+};
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const uint8_t* __restrict__ sx, const uint8_t* __restrict__ sw, const float* __restrict__ gs_x,
-    const float* __restrict__ gs_w, int M, int N, int K, uint16_t* __restrict__ out,
+    const float* __restrict__ gs_w, int M, int N, int K, Batch bt, uint16_t* __restrict__ out,
     unsigned* __restrict__ err, int inject_timeout) {
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
@@ -142,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
   const int lane = threadIdx.x & 31;
   const int num_kb = K / BK;
   const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
+  const int tiles_per_batch = num_m * num_n;
+  const int num_tiles = tiles_per_batch * bt.count;
   const int64_t tiles_per_rowtile = (K / C::GROUP) / 4;  // 128x4 scale tiles along K
   const int n_rowtiles = (N + 127) / 128;
 
@@ -174,7 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
       prefetch_tmap(&tmB);
       int g = 0;  // k-blocks issued by this CTA so far (ring position)
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        const int m_blk = tile % num_m, n_blk = tile / num_m;
+        const int b = tile / tiles_per_batch, rem = tile - b * tiles_per_batch;
+        const int m_blk = rem % num_m, n_blk = rem / num_m;
+        const uint8_t* sxb = sx + (int64_t)b * bt.stride_sx;
+        const uint8_t* swb = sw + (int64_t)b * bt.stride_sw;
         const bool second_b_tile = (n_blk * 2 + 1) < n_rowtiles;
         const uint32_t tx = A_BYTES + B_BYTES + C::SFA_BYTES + (second_b_tile ? 2u : 1u) * C::SFA_BYTES;
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
@@ -183,16 +197,16 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
           if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
           uint8_t* st = smem + s * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_2d(st, &tmA, &full[s], kb * BK_BYTES, m_blk * BM);
-          tma_load_2d(st + A_BYTES, &tmB, &full[s], kb * BK_BYTES, n_blk * BN);
+          tma_load_3d(st, &tmA, &full[s], kb * BK_BYTES, m_blk * BM, b);
+          tma_load_3d(st + A_BYTES, &tmB, &full[s], kb * BK_BYTES, n_blk * BN, b * bt.wz);
           const int64_t tcol = (int64_t)kb * C::TILES_PER_STAGE;
-          bulk_load(st + A_BYTES + B_BYTES, sx + ((int64_t)m_blk * tiles_per_rowtile + tcol) * 512,
+          bulk_load(st + A_BYTES + B_BYTES, sxb + ((int64_t)m_blk * tiles_per_rowtile + tcol) * 512,
                     C::SFA_BYTES, &full[s]);
           bulk_load(st + A_BYTES + B_BYTES + C::SFA_BYTES,
-                    sw + ((int64_t)(2 * n_blk) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES, &full[s]);
+                    swb + ((int64_t)(2 * n_blk) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES, &full[s]);
           if (second_b_tile)
             bulk_load(st + A_BYTES + B_BYTES + 2 * C::SFA_BYTES,
-                      sw + ((int64_t)(2 * n_blk + 1) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES,
+                      swb + ((int64_t)(2 * n_blk + 1) * tiles_per_rowtile + tcol) * 512, C::SFA_BYTES,
                       &full[s]);
         }
       }
@@ -248,10 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
     // 8 warps: lane quadrant q = warp % 4 (tensor-memory access rule), column half h.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
-    const float alpha = __fmul_rn(gs_x ? __ldg(gs_x) : 1.0f, gs_w ? __ldg(gs_w) : 1.0f);
     int it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int m_blk = tile % num_m, n_blk = tile / num_m;
+      const int b = tile / tiles_per_batch, rem = tile - b * tiles_per_batch;
+      const int m_blk = rem % num_m, n_blk = rem / num_m;
+      const float alpha = __fmul_rn(gs_x ? __ldg(gs_x + b) : 1.0f, gs_w ? __ldg(gs_w + b) : 1.0f);
       mbar_wait(acc_full, it & 1, err, failed);
       tc_fence_after();
       // drain this warp's 32 rows x 128 columns into registers as packed bf16
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
       if (lane == 0) mbar_arrive(acc_empty);
       const int row = m_blk * BM + 32 * q + lane;
       if (row < M) {
-        uint16_t* orow = out + (int64_t)row * N + n_blk * BN + h * 128;
+        uint16_t* orow = out + (int64_t)b * bt.stride_out + (int64_t)row * N + n_blk * BN + h * 128;
         const int cols_left = N - (n_blk * BN + h * 128);
 #pragma unroll
         for (int v = 0; v < 16; ++v)
@@ -306,15 +321,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D map over packed codes viewed as bytes: [rows, K/2], box 128 bytes x box_rows.
-bool make_code_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows) {
+// 3-D map over packed codes viewed as bytes: [batch, rows, K/2] with the batch
+// pitch in bytes, box 128 bytes x box_rows x 1.
+bool make_code_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows, int64_t batch,
+                   int64_t batch_pitch) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)rows, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(batch > 1 ? batch_pitch : rows * (K / 2))};
+  cuuint32_t box[3] = {(cuuint32_t)BK_BYTES, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -323,16 +340,25 @@ bool make_code_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uin
 template <int MODE>
 cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
                         const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M, int64_t N,
-                        int64_t K, uint16_t* out, int inject, cudaStream_t s) {
+                        int64_t K, const BatchArgs& ba, uint16_t* out, int inject, cudaStream_t s) {
   CUtensorMap ta, tb;
-  if (!make_code_map(&ta, xq, M, K, BM) || !make_code_map(&tb, wq, N, K, BN)) return cudaErrorInvalidValue;
+  const bool shared_w = ba.stride_wq == 0;
+  if (!make_code_map(&ta, xq, M, K, BM, ba.batch, ba.stride_xq * 4) ||
+      !make_code_map(&tb, wq, N, K, BN, shared_w ? 1 : ba.batch, ba.stride_wq * 4))
+    return cudaErrorInvalidValue;
   const size_t smem = Cfg<MODE>::SMEM_BYTES;
   if (smem > d.smem_optin) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(qqmm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  Batch bt;
+  bt.count = (int)ba.batch;
+  bt.wz = shared_w ? 0 : 1;
+  bt.stride_sx = ba.stride_sx;
+  bt.stride_sw = ba.stride_sw;
+  bt.stride_out = ba.stride_out;
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM) * ba.batch;
   dim3 grid((unsigned)std::min<int64_t>(tiles, d.sm_count));
-  qqmm_kernel<MODE><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, out,
+  qqmm_kernel<MODE><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, bt, out,
                                                   d.err, inject);
   return cudaGetLastError();
 }
@@ -341,10 +367,10 @@ cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
 
 cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx, const uint32_t* wq,
                         const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
-                        int64_t N, int64_t K, int mode, uint16_t* out, int inject_timeout,
+                        int64_t N, int64_t K, const BatchArgs& ba, int mode, uint16_t* out, int inject_timeout,
                         cudaStream_t s) {
-  if (mode == 2) return launch_mode<2>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, out, inject_timeout, s);
-  return launch_mode<1>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, out, inject_timeout, s);
+  if (mode == 2) return launch_mode<2>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
+  return launch_mode<1>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
 }
 
 }  // namespace fp4

@@ -228,6 +228,23 @@ fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* 
                       int64_t N, int64_t K, fp4_mode mode, int bits, int group_size, int sorted,
                       fp4_bf16* out, cudaStream_t stream);
 
+/* qqmm_batched: batch_count independent FP4 x FP4 GEMMs in one launch [P3
+ * qqmm_impl: the page's cuBLASLt call fixes the batch count at 1; this is the
+ * strided-batch generalization].
+ *   out_b = bf16( gs_x[b] * gs_w[b] * Xq_b . Wq_b^T ),  b = 0 .. batch - 1
+ *   Xq_b = xq + b * stride_xq (uint32 words), its tiled scales sx + b * stride_sx (bytes);
+ *   Wq_b = wq + b * stride_wq, scales sw + b * stride_sw; a stride of 0 shares one W
+ *   (and its scales) across the batch; out_b = out + b * stride_out (elements).
+ *   global_scale_x / global_scale_w: device fp32 arrays of `batch` values, or NULL (1).
+ * Each batch follows qqmm's rules (M, N, K, layouts, alignment).  The strides
+ * must keep the batches apart (stride_xq >= M K / 8, stride_sx >= the padded
+ * scale bytes, stride_out >= M N, and likewise for W unless 0) and aligned
+ * (16 bytes for codes and scales, 8 elements for out); batch <= 65535. */
+fp4_status qqmm_batched(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const uint8_t* sw,
+                        const float* global_scale_x, const float* global_scale_w, int64_t batch, int64_t M,
+                        int64_t N, int64_t K, int64_t stride_xq, int64_t stride_sx, int64_t stride_wq,
+                        int64_t stride_sw, int64_t stride_out, fp4_mode mode, fp4_bf16* out, cudaStream_t stream);
+
 /* qmm: the dense prefill GEMM with 4-bit weights and bf16 activations (W4A16)
  * ["mlx: opt-in dense GEMM for nvfp4 prefill ... - #287": the mixed-input GEMM
  * of bf16 activations against NVFP4 weights at M > 1; "perf(cuda): enable

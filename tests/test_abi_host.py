@@ -95,5 +95,14 @@ def test_validation_rejects_before_launch(B):
     assert L.qmm(p, p, p, None, None, 4, 16, 64, B.MODE_AFFINE, 4, 64, p, None) == B.FP4_ERR_INVALID_ARG  # no biases
     assert L.qmm(p, p, p, None, p, 4, 16, 64, B.MODE_MXFP4, 4, 32, p, None) == B.FP4_ERR_INVALID_ARG  # gs w/ MXFP4
     assert L.qmm(odd, p, p, None, None, 4, 16, 64, B.MODE_NVFP4, 4, 16, p, None) == B.FP4_ERR_ALIGNMENT
+    # batched qqmm: overlapping or misaligned batch strides
+    assert L.qqmm_batched(p, p, p, p, None, None, 2, 128, 256, 256, 100, 16384, 0, 0, 128 * 256, B.MODE_NVFP4,
+                          p, None) == B.FP4_ERR_INVALID_ARG  # stride_xq < M K / 8
+    assert L.qqmm_batched(p, p, p, p, None, None, 2, 128, 256, 256, 4096, 1024, 0, 0, 128 * 256, B.MODE_NVFP4,
+                          p, None) == B.FP4_ERR_INVALID_ARG  # stride_sx < the 2048 padded scale bytes
+    assert L.qqmm_batched(p, p, p, p, None, None, 2, 128, 256, 256, 4098, 16400, 0, 0, 128 * 256, B.MODE_NVFP4,
+                          p, None) == B.FP4_ERR_ALIGNMENT  # stride_xq not 16-byte
+    assert L.qqmm_batched(p, p, p, p, None, None, 0, 128, 256, 256, 4096, 16384, 0, 0, 128 * 256, B.MODE_NVFP4,
+                          p, None) == B.FP4_ERR_INVALID_ARG  # batch 0
     assert L.fp4_debug_stream_weights(p, p, 64, 320, None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.fp4_debug_stream_weights(odd, p, 64, 256, None) == B.FP4_ERR_ALIGNMENT

@@ -90,3 +90,35 @@ def test_qqmm_timeout_injection_reports_and_recovers(B):
     out, ref = run(B, 2, 128, 256, 256, seed=9)
     assert B.fp4_check_device_error() == B.FP4_OK
     assert_close_to_oracle(out, ref, "qqmm after recovery")
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("shared_w", [False, True])
+def test_qqmm_batched_matches_each_gemm(B, mode, shared_w):
+    """qqmm_batched: every batch's output is the single FP4 x FP4 GEMM of its own
+    operands and global scales (per-batch x, W either per batch or shared)."""
+    Bt, M, N, K = 3, 200, 264, 512
+    g = 16 if mode == 2 else 32
+    xs, ws = [], []
+    for b in range(Bt):
+        xs.append(quantized(mode, synth.bf16_normal((M, K), 1.0 + b, seed=60 + b)))
+        if b == 0 or not shared_w:
+            ws.append(quantized(mode, synth.bf16_normal((N, K), 0.02, seed=70 + b)))
+    dev = lambda a: torch.from_numpy(a).cuda()
+    xq = dev(np.stack([x[0] for x in xs]).view(np.int32))
+    sx = dev(np.stack([oracle.tile_scales(x[1]) for x in xs]))
+    wq = dev(np.stack([w[0] for w in ws]).view(np.int32))
+    sw = dev(np.stack([oracle.tile_scales(w[1]) for w in ws]))
+    if shared_w:
+        wq, sw = wq[0], sw[0]
+    gx = gw = None
+    if mode == 2:
+        gx = torch.tensor([x[2] for x in xs], dtype=torch.float32, device="cuda")
+        gw = torch.tensor([ws[0 if shared_w else b][2] for b in range(Bt)], dtype=torch.float32, device="cuda")
+    out = B.qqmm_batched(xq, sx, wq, sw, gx, gw, mode=mode)
+    for b in range(Bt):
+        xq_b, xs_b, gx_b = xs[b]
+        wq_b, ws_b, gw_b = ws[0 if shared_w else b]
+        alpha = np.float32(gx_b) * np.float32(gw_b) if mode == 2 else 1.0
+        ref = oracle.qqmm(xq_b, xs_b, wq_b, ws_b, mode, alpha=alpha)
+        assert_close_to_oracle(out[b], ref, f"batched qqmm mode {mode} batch {b}")
