@@ -315,7 +315,7 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
     N, K = 17408, 5120
     w = synth.bf16_normal((N, K), 0.02, seed=1, device=device)
     gw = B.fp4_amax_global_scale(w)
-    wq, ws = B.fp4_quantize(w, B.MODE_NVFP4, global_scale=gw, layout=B.SCALES_TILED)
+    wq, ws_w = B.fp4_quantize(w, B.MODE_NVFP4, global_scale=gw, layout=B.SCALES_TILED)
     del w
     res = {}
     for M in Ms:
@@ -324,12 +324,12 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
         xq, xs = B.fp4_quantize(x, B.MODE_NVFP4, global_scale=gx, layout=B.SCALES_TILED)
         out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         for _ in range(3):  # warm-up
-            B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
+            B.qqmm(xq, xs, wq, ws_w, gx, gw, mode=B.MODE_NVFP4, out=out)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
-            B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
+            B.qqmm(xq, xs, wq, ws_w, gx, gw, mode=B.MODE_NVFP4, out=out)
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps if reps else float("nan")
@@ -338,13 +338,25 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
         for _ in range(reps):
             B.fp4_amax_global_scale_noalloc(x, gs_out=gx)
             B.fp4_quantize(x, B.MODE_NVFP4, global_scale=gx, layout=B.SCALES_TILED, xq=xq, scales=xs)
-            B.qqmm(xq, xs, wq, ws, gx, gw, mode=B.MODE_NVFP4, out=out)
+            B.qqmm(xq, xs, wq, ws_w, gx, gw, mode=B.MODE_NVFP4, out=out)
         e1.record()
         torch.cuda.synchronize()
         ms_q = e0.elapsed_time(e1) / reps if reps else float("nan")
+        # the same three steps fused into one cooperative launch (qqmm_quantize_x)
+        ws = B.qqmm_quantize_x_workspace(M, K, B.MODE_NVFP4)
+        for _ in range(3):
+            B.qqmm_quantize_x(x, wq, ws_w, ws, None, gw, mode=B.MODE_NVFP4, out=out)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            B.qqmm_quantize_x(x, wq, ws_w, ws, None, gw, mode=B.MODE_NVFP4, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms_f = e0.elapsed_time(e1) / reps if reps else float("nan")
         flops = 2.0 * M * N * K
         res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops,
-                        "ms_with_x_quantize": ms_q, "TFLOP/s_with_x_quantize": flops / ms_q / 1e9}
+                        "ms_with_x_quantize": ms_q, "TFLOP/s_with_x_quantize": flops / ms_q / 1e9,
+                        "ms_fused_x_quantize": ms_f, "TFLOP/s_fused_x_quantize": flops / ms_f / 1e9}
         del x, xq, xs, out
     return res
 

@@ -48,6 +48,8 @@ SIGNATURES = {
                           _VP, _VP]),
     "qqmm_batched": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
                             _INT, _VP, _VP]),
+    "qqmm_quantize_x_workspace_bytes": (c.c_size_t, [_I64, _I64, _INT]),
+    "qqmm_quantize_x": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, c.c_size_t, _VP, _VP, _VP]),
     "qmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
     "fp4_debug_inject_wait_timeout": (_INT, [_INT]),
     "fp4_debug_stream_weights": (_INT, [_VP, _VP, _I64, _I64, _VP]),
@@ -226,6 +228,24 @@ def qqmm_batched(xq: torch.Tensor, sx: torch.Tensor, wq: torch.Tensor, sw: torch
     _check(lib().qqmm_batched(_p(xq), _p(sx), _p(wq), _p(sw), _p(global_scale_x), _p(global_scale_w), Bt, M, N, K,
                               xq.stride(0), sx.stride(0), 0 if shared else wq.stride(0), 0 if shared else sw.stride(0),
                               out.stride(0), mode, _p(out), _s(stream)), "qqmm_batched")
+    return out
+
+
+def qqmm_quantize_x_workspace(M: int, K: int, mode: int = MODE_NVFP4, device="cuda"):
+    """A zero-filled workspace for qqmm_quantize_x (allocate once, reuse)."""
+    n = lib().qqmm_quantize_x_workspace_bytes(M, K, mode)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def qqmm_quantize_x(x: torch.Tensor, wq: torch.Tensor, sw: torch.Tensor, ws: torch.Tensor, global_scale_x=None,
+                    global_scale_w=None, mode: int = MODE_NVFP4, global_scale_x_out=None, out=None, stream=None):
+    """Quantize bf16 x [M, K] and multiply by FP4 W in one launch."""
+    M, K = x.shape
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=wq.device)
+    _check(lib().qqmm_quantize_x(_p(x), _p(global_scale_x), _p(wq), _p(sw), _p(global_scale_w), M, N, K, mode,
+                                 _p(ws), ws.numel(), _p(global_scale_x_out), _p(out), _s(stream)), "qqmm_quantize_x")
     return out
 
 

@@ -293,6 +293,31 @@ fp4_status qqmm_batched(const uint32_t* xq, const uint8_t* sx, const uint32_t* w
   return qqmm_common(xq, sx, wq, sw, global_scale_x, global_scale_w, M, N, K, ba, mode, out, stream);
 }
 
+size_t qqmm_quantize_x_workspace_bytes(int64_t M, int64_t K, fp4_mode mode) {
+  if (M <= 0 || K <= 0) return 0;
+  return qqmm_fused_workspace_bytes(M, K, mode == FP4_MODE_NVFP4 ? 2 : 1);
+}
+
+fp4_status qqmm_quantize_x(const fp4_bf16* x, const float* global_scale_x, const uint32_t* wq, const uint8_t* sw,
+                           const float* global_scale_w, int64_t M, int64_t N, int64_t K, fp4_mode mode, void* ws,
+                           size_t ws_bytes, float* global_scale_x_out, fp4_bf16* out, cudaStream_t stream) {
+  if (mode != FP4_MODE_NVFP4 && mode != FP4_MODE_MXFP4) return FP4_ERR_UNSUPPORTED;
+  if (!x || !wq || !sw || !out || !ws || M <= 0 || N <= 0 || K <= 0) return FP4_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 8 != 0 || M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > (1 << 24))
+    return FP4_ERR_INVALID_ARG;
+  if (mode == FP4_MODE_MXFP4 && (global_scale_x || global_scale_w || global_scale_x_out)) return FP4_ERR_INVALID_ARG;
+  if (ws_bytes < qqmm_fused_workspace_bytes(M, K, mode == FP4_MODE_NVFP4 ? 2 : 1)) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(sw, 16) || !aligned(out, 16) || !aligned(ws, 128) ||
+      (global_scale_x && !aligned(global_scale_x, 4)) || (global_scale_w && !aligned(global_scale_w, 4)) ||
+      (global_scale_x_out && !aligned(global_scale_x_out, 4)))
+    return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_qqmm_fused(*d, x, global_scale_x, global_scale_x_out, wq, sw, global_scale_w, M, N, K,
+                                     mode == FP4_MODE_NVFP4 ? 2 : 1, ws, out, g_inject_timeout.load(), stream));
+}
+
 namespace {
 // Shared checks of the W4A16 GEMMs: format, weight scales/biases by mode, alignment.
 fp4_status check_w4a16(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,

@@ -69,6 +69,14 @@ cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
                         int64_t N, int64_t K, const BatchArgs& ba, int mode, uint16_t* out, int inject_timeout,
                         cudaStream_t s);
 
+// qqmm.cu: the fused call -- bf16 x quantized by the same (cooperative) launch
+// into the workspace, then the GEMM (gs_in: the NVFP4 activation global scale,
+// or nullptr to take amax(x) / 2688; gs_out: where the scale used goes, nullable)
+size_t qqmm_fused_workspace_bytes(int64_t M, int64_t K, int mode);
+cudaError_t launch_qqmm_fused(const DevInfo& d, const uint16_t* x, const float* gs_in, float* gs_out,
+                              const uint32_t* wq, const uint8_t* sw, const float* gs_w, int64_t M, int64_t N,
+                              int64_t K, int mode, void* ws, uint16_t* out, int inject_timeout, cudaStream_t s);
+
 // weight_stream.cu (measurement aid: the GEMV's weight stream without the GEMV)
 cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint8_t* scales, int64_t N,
                                  int64_t K, cudaStream_t s);

@@ -128,12 +128,146 @@ struct Batch {
   int64_t stride_sx = 0, stride_sw = 0, stride_out = 0;
 };
 
+// The quantized-activation prologue of a fused call: bf16 x [M, K] is
+// quantized by every CTA of the (co-resident, cooperative) grid into the
+// caller's workspace -- codes xq and the 128x4-tiled scales sx the GEMM then
+// reads -- after, when no activation global scale is given (NVFP4), the tensor
+// amax reduced across the grid.  Grid barriers count arrivals in bar[0] and
+// release through the generation word bar[1] (both zero before the first call,
+// and left so); their waits are bounded.
+struct FusedX {
+  const uint16_t* x = nullptr;
+  const float* gs_in = nullptr;  // NVFP4 activation global scale, or nullptr: amax / 2688 from x
+  float* gs_out = nullptr;       // the global scale used, for the epilogue (workspace)
+  float* gs_user = nullptr;      // and a copy for the caller (nullable)
+  uint32_t* xq = nullptr;
+  uint8_t* sx = nullptr;
+  uint32_t* partials = nullptr;  // one per CTA
+  unsigned* bar = nullptr;
+  int padded_rows = 0, padded_cols = 0;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// All CTAs of the grid meet: bar[0] counts arrivals, the last one resets it and
+// bumps the generation bar[1]; the others wait (bounded) for the bump.
+__device__ void grid_barrier(unsigned* bar, unsigned* err, bool& failed) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned gen = ld_acquire_gpu(bar + 1);
+    __threadfence();
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else if (!failed) {
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(bar + 1) == gen) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          record_error(err, kErrTimeout);
+          failed = true;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
 template <int MODE>
+__device__ void quantize_prologue(const FusedX& fx, int M, int K, unsigned* err, bool& failed) {
+  constexpr int G = (MODE == 2) ? 16 : 32;
+  constexpr int NV = G / 8;
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ float gs_sh;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  float gs = 1.0f;
+  if (MODE == 2 && fx.gs_in) {
+    gs = __ldg(fx.gs_in);
+  } else if (MODE == 2) {
+    // tensor amax over bf16 magnitude bits (their unsigned order is |x|'s order)
+    const int64_t nvec = (int64_t)M * K / 8;
+    uint32_t m = 0;
+    for (int64_t i = tid; i < nvec; i += nthreads) m = max(m, max_mag8(ld_stream_v4(reinterpret_cast<const uint4*>(fx.x) + i)));
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kThreads / 32; ++w) m = max(m, red[w]);
+      fx.partials[blockIdx.x] = m;
+    }
+    grid_barrier(fx.bar, err, failed);
+    if (threadIdx.x == 0) {
+      uint32_t a = 0;
+      for (unsigned b = 0; b < gridDim.x; ++b) a = max(a, __ldcg(fx.partials + b));
+      gs_sh = __fdiv_rn(__uint_as_float(a << 16), 2688.0f);
+      if (blockIdx.x == 0) {
+        *fx.gs_out = gs_sh;
+        if (fx.gs_user) *fx.gs_user = gs_sh;
+      }
+    }
+    __syncthreads();
+    gs = gs_sh;
+  }
+  if (MODE == 2 && fx.gs_in && tid == 0) {
+    *fx.gs_out = gs;
+    if (fx.gs_user) *fx.gs_user = gs;
+  }
+  // quantize: one thread per block-scale group, scales straight into their tiles
+  const int scols = K / G;
+  const int64_t ngroups = (int64_t)M * scols;
+  for (int64_t gi = tid; gi < ngroups; gi += nthreads) {
+    const int r = (int)(gi / scols), c = (int)(gi - (int64_t)r * scols);
+    const uint4* src = reinterpret_cast<const uint4*>(fx.x + (int64_t)r * K + (int64_t)c * G);
+    uint4 v[NV];
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      v[i] = ld_stream_v4(src + i);
+      mb = max(mb, max_mag8(v[i]));
+    }
+    float mul, sval;
+    uint32_t sbyte;
+    block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
+    uint32_t words[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
+      words[i] = word;
+    }
+    uint32_t* dst = fx.xq + (int64_t)r * (K / 8) + (int64_t)c * NV;
+    if (NV == 2) *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+    fx.sx[tiled_scale_offset(r, c, fx.padded_cols)] = (uint8_t)sbyte;
+  }
+  // the padding rows of the scale tiles are zero
+  const int64_t pad = (int64_t)(fx.padded_rows - M) * fx.padded_cols;
+  for (int64_t i = tid; i < pad; i += nthreads) {
+    const int r = M + (int)(i / fx.padded_cols), c = (int)(i % fx.padded_cols);
+    fx.sx[tiled_scale_offset(r, c, fx.padded_cols)] = 0;
+  }
+  // generic-proxy writes, read next by TMA and bulk copies (async proxy) in other CTAs
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  grid_barrier(fx.bar, err, failed);
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <int MODE, bool FQ>
 __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const uint8_t* __restrict__ sx, const uint8_t* __restrict__ sw, const float* __restrict__ gs_x,
     const float* __restrict__ gs_w, int M, int N, int K, Batch bt, uint16_t* __restrict__ out,
-    unsigned* __restrict__ err, int inject_timeout) {
+    unsigned* __restrict__ err, int inject_timeout, FusedX fx) {
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -177,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;  // this thread gave up a wait (see mbar_wait)
+  if (FQ) quantize_prologue<MODE>(fx, M, K, err, failed);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -266,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       const int b = tile / tiles_per_batch, rem = tile - b * tiles_per_batch;
       const int m_blk = rem % num_m, n_blk = rem / num_m;
-      const float alpha = __fmul_rn(gs_x ? __ldg(gs_x + b) : 1.0f, gs_w ? __ldg(gs_w + b) : 1.0f);
+      // (a fused call's activation scale was written by this grid: read it coherently)
+      const float gx = gs_x ? (FQ ? __ldcg(gs_x + b) : __ldg(gs_x + b)) : 1.0f;
+      const float alpha = __fmul_rn(gx, gs_w ? __ldg(gs_w + b) : 1.0f);
       mbar_wait(acc_full, it & 1, err, failed);
       tc_fence_after();
       // drain this warp's 32 rows x 128 columns into registers as packed bf16
@@ -348,7 +485,8 @@ cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
     return cudaErrorInvalidValue;
   const size_t smem = Cfg<MODE>::SMEM_BYTES;
   if (smem > d.smem_optin) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(qqmm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(qqmm_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   Batch bt;
   bt.count = (int)ba.batch;
@@ -358,9 +496,72 @@ cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
   bt.stride_out = ba.stride_out;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM) * ba.batch;
   dim3 grid((unsigned)std::min<int64_t>(tiles, d.sm_count));
-  qqmm_kernel<MODE><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, bt, out,
-                                                  d.err, inject);
+  qqmm_kernel<MODE, false><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, bt,
+                                                         out, d.err, inject, FusedX{});
   return cudaGetLastError();
+}
+
+// Workspace of a fused call: [codes | tiled scales | per-CTA partial maxima |
+// global scale | barrier words], each part 128-byte aligned.
+struct FusedWs {
+  size_t xq = 0, sx = 0, partials = 0, gs = 0, bar = 0, total = 0;
+  int64_t padded_rows = 0, padded_cols = 0;
+};
+
+FusedWs fused_ws_layout(int64_t M, int64_t K, int mode) {
+  FusedWs w;
+  const int group = mode == 2 ? 16 : 32;
+  w.padded_rows = (M + 127) / 128 * 128;
+  w.padded_cols = ((K / group) + 3) / 4 * 4;
+  auto up = [](size_t v) { return (v + 127) / 128 * 128; };
+  w.xq = 0;
+  w.sx = up((size_t)M * (size_t)K / 2);
+  w.partials = w.sx + up((size_t)(w.padded_rows * w.padded_cols));
+  w.gs = w.partials + 1024 * 4;
+  w.bar = w.gs + 128;
+  w.total = w.bar + 128;
+  return w;
+}
+
+template <int MODE>
+cudaError_t launch_fused_mode(const DevInfo& d, const uint16_t* x, const float* gs_in, float* gs_out,
+                              const uint32_t* wq, const uint8_t* sw, const float* gs_w, int64_t M, int64_t N,
+                              int64_t K, uint8_t* ws, uint16_t* out, int inject, cudaStream_t s) {
+  const FusedWs L = fused_ws_layout(M, K, MODE);
+  FusedX fx;
+  fx.x = x;
+  fx.gs_in = gs_in;
+  fx.gs_out = MODE == 2 ? reinterpret_cast<float*>(ws + L.gs) : nullptr;
+  fx.gs_user = MODE == 2 ? gs_out : nullptr;
+  fx.xq = reinterpret_cast<uint32_t*>(ws + L.xq);
+  fx.sx = ws + L.sx;
+  fx.partials = reinterpret_cast<uint32_t*>(ws + L.partials);
+  fx.bar = reinterpret_cast<unsigned*>(ws + L.bar);
+  fx.padded_rows = (int)L.padded_rows;
+  fx.padded_cols = (int)L.padded_cols;
+  CUtensorMap ta, tb;
+  if (!make_code_map(&ta, fx.xq, M, K, BM, 1, 0) || !make_code_map(&tb, wq, N, K, BN, 1, 0))
+    return cudaErrorInvalidValue;
+  const size_t smem = Cfg<MODE>::SMEM_BYTES;
+  if (smem > d.smem_optin) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(qqmm_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(std::min<int64_t>(tiles, d.sm_count), 1024));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barriers need every CTA resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, qqmm_kernel<MODE, true>, ta, tb, (const uint8_t*)fx.sx, sw,
+                         (const float*)(MODE == 2 ? fx.gs_out : nullptr), gs_w, (int)M, (int)N, (int)K, Batch{}, out,
+                         d.err, inject, fx);
+  return e;
 }
 
 }  // namespace
@@ -371,6 +572,18 @@ cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
                         cudaStream_t s) {
   if (mode == 2) return launch_mode<2>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
   return launch_mode<1>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
+}
+
+size_t qqmm_fused_workspace_bytes(int64_t M, int64_t K, int mode) { return fused_ws_layout(M, K, mode).total; }
+
+cudaError_t launch_qqmm_fused(const DevInfo& d, const uint16_t* x, const float* gs_in, float* gs_out,
+                              const uint32_t* wq, const uint8_t* sw, const float* gs_w, int64_t M, int64_t N,
+                              int64_t K, int mode, void* ws, uint16_t* out, int inject_timeout, cudaStream_t s) {
+  if (mode == 2)
+    return launch_fused_mode<2>(d, x, gs_in, gs_out, wq, sw, gs_w, M, N, K, static_cast<uint8_t*>(ws), out,
+                                inject_timeout, s);
+  return launch_fused_mode<1>(d, x, nullptr, nullptr, wq, sw, nullptr, M, N, K, static_cast<uint8_t*>(ws), out,
+                              inject_timeout, s);
 }
 
 }  // namespace fp4

@@ -245,6 +245,35 @@ fp4_status qqmm_batched(const uint32_t* xq, const uint8_t* sx, const uint32_t* w
                         int64_t N, int64_t K, int64_t stride_xq, int64_t stride_sx, int64_t stride_wq,
                         int64_t stride_sw, int64_t stride_out, fp4_mode mode, fp4_bf16* out, cudaStream_t stream);
 
+/* Workspace bytes qqmm_quantize_x needs for an M x K activation. */
+size_t qqmm_quantize_x_workspace_bytes(int64_t M, int64_t K, fp4_mode mode);
+
+/* qqmm_quantize_x: the quantized-activation GEMM with the activation's
+ * quantization fused into the same launch [P3 qqmm.cpp: QQMatmul::eval_gpu
+ * quantizes x with quantize_input (fp_quantize, optional global scale) and then
+ * calls the block-scaled GEMM -- separate launches there].
+ *   out = bf16( gs_x * gs_w * fp4_quantize(x, gs_x) . Wq^T ), bit for bit what
+ *   fp4_amax_global_scale (when global_scale_x is NULL) + fp4_quantize (tiled
+ *   scales) + qqmm compute.
+ *   x        bf16[M, K], 16-byte aligned
+ *   global_scale_x  NVFP4: device fp32 activation global scale (a calibrated value),
+ *            or NULL to take fl(amax(x) / 2688) from x; MXFP4: must be NULL
+ *   global_scale_x_out  NVFP4 only, nullable: receives the activation scale used
+ *   wq, sw, global_scale_w, M, N, K, mode, out: as for qqmm
+ *   ws       device workspace of ws_bytes >= qqmm_quantize_x_workspace_bytes(M, K, mode)
+ *            bytes, 128-byte aligned.  It must be zero-filled once when allocated;
+ *            each call leaves its grid-barrier words ready for the next.  The
+ *            quantized x (codes, then 128x4-tiled scales) sits at its start.
+ *            Calls that overlap on the GPU must not share a workspace.
+ * One persistent cooperative launch: every CTA quantizes a share of x (after a
+ * grid-wide amax when NVFP4 has no activation scale), a grid barrier, then the
+ * GEMM reads the quantized x from the workspace (still in L2).  The launch needs
+ * every CTA resident (at most one per SM); a device that cannot co-schedule it
+ * returns FP4_ERR_CUDA. */
+fp4_status qqmm_quantize_x(const fp4_bf16* x, const float* global_scale_x, const uint32_t* wq, const uint8_t* sw,
+                           const float* global_scale_w, int64_t M, int64_t N, int64_t K, fp4_mode mode, void* ws,
+                           size_t ws_bytes, float* global_scale_x_out, fp4_bf16* out, cudaStream_t stream);
+
 /* qmm: the dense prefill GEMM with 4-bit weights and bf16 activations (W4A16)
  * ["mlx: opt-in dense GEMM for nvfp4 prefill ... - #287": the mixed-input GEMM
  * of bf16 activations against NVFP4 weights at M > 1; "perf(cuda): enable

@@ -104,5 +104,15 @@ def test_validation_rejects_before_launch(B):
                           p, None) == B.FP4_ERR_ALIGNMENT  # stride_xq not 16-byte
     assert L.qqmm_batched(p, p, p, p, None, None, 0, 128, 256, 256, 4096, 16384, 0, 0, 128 * 256, B.MODE_NVFP4,
                           p, None) == B.FP4_ERR_INVALID_ARG  # batch 0
+    wsb = L.qqmm_quantize_x_workspace_bytes(128, 256, B.MODE_NVFP4)
+    assert wsb >= 128 * 128 + 128 * 16
+    assert L.qqmm_quantize_x(p, None, p, p, None, 128, 256, 256, B.MODE_NVFP4, p, wsb - 1, None, p,
+                             None) == B.FP4_ERR_INVALID_ARG  # workspace too small
+    assert L.qqmm_quantize_x(p, p, p, p, None, 128, 256, 256, B.MODE_MXFP4, p, wsb, None, p,
+                             None) == B.FP4_ERR_INVALID_ARG  # global scale with MXFP4
+    assert L.qqmm_quantize_x(p, None, p, p, None, 128, 256, 320, B.MODE_NVFP4, p, 1 << 20, None, p,
+                             None) == B.FP4_ERR_INVALID_ARG  # K % 256
+    assert L.qqmm_quantize_x(p, None, p, p, None, 128, 256, 256, B.MODE_NVFP4, ctypes.c_void_p(256 + 64), wsb, None,
+                             p, None) == B.FP4_ERR_ALIGNMENT  # workspace not 128-byte aligned
     assert L.fp4_debug_stream_weights(p, p, 64, 320, None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.fp4_debug_stream_weights(odd, p, 64, 256, None) == B.FP4_ERR_ALIGNMENT
