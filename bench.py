@@ -513,16 +513,27 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     B.fp4_init(0)
     c = args.case
-    if c.startswith("qmv_"):
+    if c.startswith("qmv_") or c.startswith("qqmv_"):
         layout = "fused" if c.endswith("_fused") else "split"
-        mode = {"qmv_nvfp4": B.MODE_NVFP4, "qmv_mxfp4": B.MODE_MXFP4, "qmv_affine": B.MODE_AFFINE}[c.replace("_fused", "")]
-        stack = DecodeStack(B, mode, 4, dev, layout=layout)  # 4 layers: 0.84 GB of weights, well above L2
+        base = c.replace("_fused", "").replace("qqmv_", "qmv_")
+        mode = {"qmv_nvfp4": B.MODE_NVFP4, "qmv_mxfp4": B.MODE_MXFP4, "qmv_affine": B.MODE_AFFINE}[base]
+        # 4 layers: 0.84 GB of weights, well above L2
+        stack = DecodeStack(B, mode, 4, dev, layout=layout, qx=c.startswith("qqmv_"))
         for _ in range(3):
             stack.step()
     elif c.startswith("qqmm_m"):
         bench_qqmm(B, dev, Ms=(int(c[len("qqmm_m"):]),), reps=1)
     elif c == "quantize":
         bench_quantize(B, dev, reps=2)
+    elif c.startswith("qqmm_fused_m"):
+        M, N, K = int(c[len("qqmm_fused_m"):]), 17408, 5120
+        w = synth.bf16_normal((N, K), 0.02, seed=1, device=dev)
+        gw = B.fp4_amax_global_scale(w)
+        wq, sw = B.fp4_quantize(w, B.MODE_NVFP4, global_scale=gw, layout=B.SCALES_TILED)
+        x = synth.bf16_normal((M, K), 1.0, seed=2, device=dev)
+        ws = B.qqmm_quantize_x_workspace(M, K, B.MODE_NVFP4)
+        for _ in range(2):
+            B.qqmm_quantize_x(x, wq, sw, ws, None, gw, mode=B.MODE_NVFP4)
     elif c == "gather":
         bench_gather(B, dev, reps=1)
     elif c.startswith("qmm_m"):
@@ -713,7 +724,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no other formats/components)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
-                    help="profiling case: qmv_nvfp4[_fused]|qmv_mxfp4[_fused]|qmv_affine|qqmm_m<M>|quantize|gather")
+                    help="profiling case: qmv_nvfp4[_fused]|qmv_mxfp4[_fused]|qmv_affine[_fused]|qqmv_nvfp4_fused|"
+                         "qqmm_m<M>|qqmm_fused_m<M>|qmm_m<M>|quantize|gather")
     args = ap.parse_args()
     if args.case:
         run_case(args)

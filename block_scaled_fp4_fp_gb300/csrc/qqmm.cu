@@ -193,8 +193,15 @@ __device__ void quantize_prologue(const FusedX& fx, int M, int K, unsigned* err,
   } else if (MODE == 2) {
     // tensor amax over bf16 magnitude bits (their unsigned order is |x|'s order)
     const int64_t nvec = (int64_t)M * K / 8;
+    const uint4* xv = reinterpret_cast<const uint4*>(fx.x);
     uint32_t m = 0;
-    for (int64_t i = tid; i < nvec; i += nthreads) m = max(m, max_mag8(ld_stream_v4(reinterpret_cast<const uint4*>(fx.x) + i)));
+    int64_t i = tid;
+    for (; i + 3 * nthreads < nvec; i += 4 * nthreads) {  // four 16-byte loads in flight per thread
+      const uint4 a = ld_stream_v4(xv + i), b = ld_stream_v4(xv + i + nthreads);
+      const uint4 c = ld_stream_v4(xv + i + 2 * nthreads), e = ld_stream_v4(xv + i + 3 * nthreads);
+      m = max(max(m, max(max_mag8(a), max_mag8(b))), max(max_mag8(c), max_mag8(e)));
+    }
+    for (; i < nvec; i += nthreads) m = max(m, max_mag8(ld_stream_v4(xv + i)));
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -222,33 +229,45 @@ __device__ void quantize_prologue(const FusedX& fx, int M, int K, unsigned* err,
   // quantize: one thread per block-scale group, scales straight into their tiles
   const int scols = K / G;
   const int64_t ngroups = (int64_t)M * scols;
-  for (int64_t gi = tid; gi < ngroups; gi += nthreads) {
-    const int r = (int)(gi / scols), c = (int)(gi - (int64_t)r * scols);
-    const uint4* src = reinterpret_cast<const uint4*>(fx.x + (int64_t)r * K + (int64_t)c * G);
-    uint4 v[NV];
-    uint32_t mb = 0;
+  constexpr int U = (MODE == 2) ? 4 : 2;  // groups per thread per round: 8 loads in flight
+  for (int64_t g0 = tid; g0 < ngroups; g0 += U * nthreads) {
+    uint4 v[U][NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      v[i] = ld_stream_v4(src + i);
-      mb = max(mb, max_mag8(v[i]));
+    for (int u = 0; u < U; ++u) {
+      const int64_t gi = g0 + u * nthreads;
+      if (gi < ngroups) {
+        const int r = (int)(gi / scols), c = (int)(gi - (int64_t)r * scols);
+        const uint4* src = reinterpret_cast<const uint4*>(fx.x + (int64_t)r * K + (int64_t)c * G);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[u][i] = ld_stream_v4(src + i);
+      }
     }
-    float mul, sval;
-    uint32_t sbyte;
-    block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
-    uint32_t words[NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-      uint32_t word = 0;
+    for (int u = 0; u < U; ++u) {
+      const int64_t gi = g0 + u * nthreads;
+      if (gi >= ngroups) break;
+      const int r = (int)(gi / scols), c = (int)(gi - (int64_t)r * scols);
+      uint32_t mb = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
-      words[i] = word;
+      for (int i = 0; i < NV; ++i) mb = max(mb, max_mag8(v[u][i]));
+      float mul, sval;
+      uint32_t sbyte;
+      block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
+      uint32_t words[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const uint32_t wv[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
+        words[i] = word;
+      }
+      uint32_t* dst = fx.xq + (int64_t)r * (K / 8) + (int64_t)c * NV;
+      if (NV == 2) *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+      fx.sx[tiled_scale_offset(r, c, fx.padded_cols)] = (uint8_t)sbyte;
     }
-    uint32_t* dst = fx.xq + (int64_t)r * (K / 8) + (int64_t)c * NV;
-    if (NV == 2) *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
-    else *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
-    fx.sx[tiled_scale_offset(r, c, fx.padded_cols)] = (uint8_t)sbyte;
   }
   // the padding rows of the scale tiles are zero
   const int64_t pad = (int64_t)(fx.padded_rows - M) * fx.padded_cols;
