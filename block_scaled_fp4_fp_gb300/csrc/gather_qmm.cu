@@ -24,8 +24,9 @@
 //     hi = bf16(w), lo = bf16(w - hi) (a single bf16 rounding of w would cost
 //     ~2.5e-3 relative error), each its own B operand;
 //   * gather_qmm: the producers gather the tile's activation rows with cp.async
-//     (16 bytes per copy, written in the same swizzled layout); qmm: one TMA
-//     box of 256 rows x 128 bytes per stage (rows past M read as zeros);
+//     (16 bytes per copy, written in the same swizzled layout), and the copies
+//     arrive on the stage barrier by themselves when they land; qmm: one TMA box
+//     of 256 rows x 128 bytes per stage (rows past M read as zeros);
 //   * one thread issues tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulators
 //     in tensor memory, M 128, N 256, K 16 per instruction): per half that holds
 //     rows one MMA (two for affine: hi then lo), each half into its own
@@ -77,12 +78,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+
+// byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
 // The weight scale data of one (row, 32-code) item: MXFP4 one E8M0 byte, NVFP4
 // two E4M3 bytes (16 codes each), affine the bf16 scale and bias packed.
@@ -204,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], kProducers + (DENSE ? 1 : 0));  // + the activation tile's byte count
+      // qmm: the producers' arrivals + the activation box's byte count; gather_qmm: the
+      // producers' arrivals + one arrival per producer when its activation copies land
+      mbar_init(&full[s], DENSE ? kProducers + 1 : 2 * kProducers);
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum_full, 1);
@@ -282,8 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
               tma_load_2d(smem + s * C::kStageBytes, &tmX, &full[s], kb * BK, row0);
             }
           } else {
-            // activations: up to 256 rows x 8 chunks of 16 bytes (half h at A_HALF h;
-            // a second half with no rows is not copied, its MMA is not issued)
+            // activations: up to 256 rows x 8 chunks of 16 bytes by cp.async (half h at
+            // A_HALF h; a second half with no rows is not copied, its MMA is not issued);
+            // each thread's copies arrive on the stage barrier by themselves when they
+            // land (cp.async.mbarrier.arrive.noinc), so no producer waits for them
 #pragma unroll
             for (int i = 0; i < (TM * 8) / kProducers; ++i) {
               const int idx = t + kProducers * i;
@@ -293,27 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
                 cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
               }
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
           }
           // weights: 256 rows x 2 items of 32 codes, dequantized to bf16 (one or two terms)
           dequant_item<MODE>(qr[u], sr[u], b_s, b_s + B_BYTES, n, g);
-          if (DENSE) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&full[s]);
-          } else if (kb > 0) {
-            // stage kb-1 is complete once its copies landed: publish it
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&full[(kb - 1) % STAGES]);
-          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&full[s]);
         }
       }
     }
-    if (!DENSE) {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&full[(num_kb - 1) % STAGES]);
-    }
+    // no copy may still be in flight when the block retires (the MMA thread may have given up)
+    if (!DENSE) asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ------------------------------------------------------------ MMA warp --
     if (elect_one_sync()) {
@@ -324,6 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % STAGES;
         mbar_wait(&full[s], (kb / STAGES) & 1, err, failed);
+        // the activation rows were written by cp.async (generic proxy) and observed
+        // through the barrier: make them visible to the tensor core's async proxy
+        if (!DENSE) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint64_t adesc = desc_sw128(base + s * C::kStageBytes);
         const uint64_t bdesc = desc_sw128(base + s * C::kStageBytes + A_BYTES);
