@@ -354,7 +354,10 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
         torch.cuda.synchronize()
         ms_f = e0.elapsed_time(e1) / reps if reps else float("nan")
         flops = 2.0 * M * N * K
-        res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops,
+        # algorithmic bytes: both operands' codes and E4M3 scales once, the bf16 output once
+        nbytes = (M + N) * K // 2 + (M + N) * (K // 16) + 2 * M * N
+        res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops, "bytes": nbytes,
+                        "GB/s": nbytes / ms / 1e6,
                         "ms_with_x_quantize": ms_q, "TFLOP/s_with_x_quantize": flops / ms_q / 1e9,
                         "ms_fused_x_quantize": ms_f, "TFLOP/s_fused_x_quantize": flops / ms_f / 1e9}
         del x, xq, xs, out
@@ -662,6 +665,7 @@ def run_ours(args):
         fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
         for k, v in comps["qqmm_nvfp4_Mx17408x5120"].items():
             v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
+            v["frac_of_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
         for k, v in comps["gather_qmm_mxfp4_moe"].items():
             v["frac_of_bf16_peak"] = v["TFLOP/s"] / peaks["bf16_tflops"]
         for k, v in comps["quantize_4096x5120"].items():

@@ -6,26 +6,29 @@
 // qqmm_utils.cu (alpha = amax_x*amax_w/(448*6)^2, beta = 0) and qqmm_utils.h
 // (scales in 128-row x 4-column tiles, zero padded).
 //
-// Design (GB300-native, not the pages' cuBLASLt call):
-//   * persistent: one CTA per SM loops over 128 x 256 output tiles, 320 threads:
-//       warp 0  -- TMA producer: codes of x and W by 2-D tensor maps with the
-//                  128-byte swizzle, scale tiles by 1-D bulk copies, into a
-//                  4-stage shared-memory ring (K = 256 per stage);
-//       warp 1  -- allocates tensor memory; one elected thread copies each
-//                  stage's scale tiles into tensor memory (tcgen05.cp 32x128b,
-//                  replicated to the four lane quadrants -- the 128x4 tile is
-//                  exactly that copy's source layout) and issues
-//                  tcgen05.mma.kind::mxf4nvf4.block_scale (4X with E4M3 scales
-//                  for NVFP4, 2X with E8M0 for MXFP4), fp32 accumulation in
-//                  tensor memory, K = 64 per instruction;
-//       warps 2-9 -- epilogue: tcgen05.ld of the accumulator (lane quadrant
-//                  warp%4, one 128-column half each), times alpha, round to
-//                  bf16 into registers, release the accumulator, then store --
-//                  so the next tile's MMAs overlap the stores, and the producer
-//                  runs ahead into the next tile while the accumulator drains.
+// Design (GB300-native, not the pages' cuBLASLt call).  Two persistent,
+// warp-specialised kernels of 320 threads (warp 0 TMA producer, warp 1 tensor
+// memory and MMA issue, warps 2-9 epilogue):
+//   * qqmm_pair_kernel (every plain and batched call): a cluster of two CTAs
+//     on two SMs owns 256 x 256 output tiles and one thread issues
+//     tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale (M 256, N 256, K 64;
+//     4X with E4M3 scales for NVFP4, 2X with E8M0 for MXFP4), each CTA holding
+//     its 128 x rows and half of the 256 W rows of every K = 256 stage, so an
+//     SM moves 32 KB of codes per stage instead of 48 KB; a 5-stage ring; the
+//     scale tiles go to tensor memory by tcgen05.cp (32x128b, replicated to
+//     the four lane quadrants -- the 128x4 tile is exactly that copy's source
+//     layout); the epilogue drains the fp32 accumulator (tcgen05.ld), scales
+//     by alpha, rounds to bf16, releases the accumulator to the next tile's
+//     MMAs and writes through a swizzled shared-memory stage with TMA tensor
+//     stores.
+//   * qqmm_kernel (the fused quantized-activation call, which needs a
+//     cooperative grid, and the fallback when no CTA pair can be resident):
+//     one CTA per SM, 128 x 256 tiles, tcgen05 cta_group::1, a 4-stage ring,
+//     scale tiles by 1-D bulk copies, per-thread row stores.
 //   * every mbarrier wait is bounded; an expired wait records an error word
-//     and the protocol continues, so the kernel always terminates.
+//     and the protocol continues, so the kernels always terminate.
 #include <algorithm>
+#include <mutex>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -464,6 +467,315 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (tcgen05 cta_group::2).  A cluster of two CTAs on two SMs
+// owns a 256 x 256 output tile: CTA r holds rows [128 r, 128 r + 128) of the
+// x tile and rows [128 r, 128 r + 128) of the W tile in its shared memory, and
+// one thread of CTA 0 issues M = 256 MMAs that read both CTAs' operands and
+// accumulate each CTA's 128 rows x 256 columns in that CTA's tensor memory.
+// Each SM so loads and reads 32 KB of codes per K = 256 stage instead of 48 KB
+// for the same 128 x 256 x 256 products.
+//   * both CTAs' loads complete on CTA 0's `full` barrier (TMA .cta_group::2,
+//     the barrier addressed in CTA 0 through mapa); CTA 0's producer expects
+//     both CTAs' bytes;
+//   * CTA 0's MMA thread releases a stage in both CTAs (commit multicast to
+//     their `empty` barriers) and publishes the accumulator to both epilogues;
+//   * the epilogue warps of both CTAs arrive on CTA 0's `acc_empty`;
+//   * scale tiles arrive by TMA too (a 4-D view of the 128x4-tiled bytes) so
+//     that they can complete on CTA 0's barrier; tcgen05.cp.cta_group::2
+//     moves each CTA's scale tiles into its own tensor memory.  Each CTA
+//     holds the scales of its own x rows and of all 256 W rows.
+constexpr int kPairStages = 5;
+
+template <int MODE>
+struct PairCfg {
+  static constexpr int TPS = Cfg<MODE>::TILES_PER_STAGE;
+  static constexpr uint32_t SF_BYTES = TPS * 512;       // one 128-row scale tile slice
+  static constexpr uint32_t AB_BYTES = 2 * A_BYTES;      // x rows + half the W rows: 32 KB
+  static constexpr uint32_t STAGE_BYTES = AB_BYTES + 3 * SF_BYTES;  // + SFA + two SFB slices
+  static constexpr uint32_t TX_CTA = STAGE_BYTES;        // bytes one CTA loads per stage
+  static constexpr uint32_t SMEM_BYTES = kPairStages * STAGE_BYTES + kEpiWarps * 4096 + 1024 + 256;
+  static constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                    ((MODE == 2 ? 0u : 1u) << 23) | ((uint32_t)(256 >> 4) << 24);
+  static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(caddr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar_addr), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait (as mbar_wait) on a barrier that other CTAs of the cluster arrive at.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, unsigned* err, bool& failed) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  if (failed) return false;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      record_error(err, kErrTimeout);
+      failed = true;
+      return false;
+    }
+  }
+}
+// TMA loads into this CTA's shared memory that complete on a barrier of either
+// CTA of the pair (`bar`: shared::cluster address).
+__device__ __forceinline__ void tma2_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void tma2_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z,
+                                             int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+      :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void tc2_commit_both(uint64_t* bar) {
+  const uint16_t mask = 0x3;
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(smem_u32(bar)), "h"(mask) : "memory");
+}
+__device__ __forceinline__ void tc2_cp_sf(uint32_t tmem, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(tmem), "l"(sdesc) : "memory");
+}
+template <int MODE>
+__device__ __forceinline__ void tc2_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t accumulate) {
+  if (MODE == 2) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate) : "memory");
+  }
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) qqmm_pair_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+    const __grid_constant__ CUtensorMap tmO, const float* __restrict__ gs_x, const float* __restrict__ gs_w, int M,
+    int N, int K, Batch bt, unsigned* __restrict__ err, int inject_timeout) {
+  using P = PairCfg<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  // per stage: [x rows | W rows | SFA | SFB rows 0-127 | SFB rows 128-255]; then
+  // the epilogue warps' output staging (4 KB each); then the barriers
+  uint8_t* stage_out = smem + kPairStages * P::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_out + kEpiWarps * 4096);
+  uint64_t* full = bars;                       // CTA 0's are used
+  uint64_t* empty = bars + kPairStages;
+  uint64_t* acc_full = bars + 2 * kPairStages;
+  uint64_t* acc_empty = bars + 2 * kPairStages + 1;  // CTA 0's is used
+  uint64_t* never = bars + 2 * kPairStages + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 3);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  const int num_kb = K / BK;
+  const int num_mp = (M + 255) / 256, num_n = (N + BN - 1) / BN;
+  const int tiles_per_batch = num_mp * num_n;
+  const int num_tiles = tiles_per_batch * bt.count;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * kEpiWarps);
+    mbar_init(never, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers initialised and tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (elect_one_sync()) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmSA);
+      prefetch_tmap(&tmSB);
+      int g = 0;
+      for (int tile = pair; tile < num_tiles; tile += npairs) {
+        const int b = tile / tiles_per_batch, rem = tile - b * tiles_per_batch;
+        const int mp = rem % num_mp, n_blk = rem / num_mp;
+        const int arow = mp * 256 + 128 * (int)rank;     // this CTA's x rows
+        const int brow = n_blk * BN + 128 * (int)rank;   // this CTA's half of the W rows
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int s = g % kPairStages;
+          const int round = g / kPairStages;
+          if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
+          const uint32_t st = base + s * P::STAGE_BYTES;
+          const uint32_t fb = mapa_u32(smem_u32(&full[s]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * P::TX_CTA);
+          tma2_load_3d(st, &tmA, fb, kb * BK_BYTES, arow, b);
+          tma2_load_3d(st + A_BYTES, &tmB, fb, kb * BK_BYTES, brow, b * bt.wz);
+          const int ty = kb * 2 * P::TPS;  // 256-byte rows of the scale view
+          tma2_load_4d(st + P::AB_BYTES, &tmSA, fb, 0, ty, mp * 2 + (int)rank, b);
+          tma2_load_4d(st + P::AB_BYTES + P::SF_BYTES, &tmSB, fb, 0, ty, n_blk * 2, b * bt.wz);
+          tma2_load_4d(st + P::AB_BYTES + 2 * P::SF_BYTES, &tmSB, fb, 0, ty, n_blk * 2 + 1, b * bt.wz);
+        }
+      }
+      // drain (CTA 0 sees both CTAs' fills): nothing may land after the pair retires
+      if (rank == 0)
+        for (int k = (g > kPairStages ? g - kPairStages : 0); k < g; ++k)
+          mbar_wait_cluster(&full[k % kPairStages], (k / kPairStages) & 1, err, failed);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer (CTA 0) --
+    if (rank == 0 && elect_one_sync()) {
+      if (inject_timeout) {
+        bool injected = false;
+        mbar_wait(never, 0, err, injected, 2000000LL);
+      }
+      int g = 0, it = 0;
+      for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
+        if (it > 0) mbar_wait_cluster(acc_empty, (it - 1) & 1, err, failed);
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int s = g % kPairStages;
+          mbar_wait_cluster(&full[s], (g / kPairStages) & 1, err, failed);
+          tc_fence_after();
+          const uint32_t st = base + s * P::STAGE_BYTES;
+          const uint32_t sfa_smem = st + P::AB_BYTES;
+          const uint32_t sfb_smem = sfa_smem + P::SF_BYTES;
+          const uint32_t sfa_t = tmem + SF_COL + s * 48;
+          const uint32_t sfb_t = sfa_t + 16;
+#pragma unroll
+          for (int j = 0; j < P::TPS; ++j) {
+            tc2_cp_sf(sfa_t + 4 * j, desc_sf(sfa_smem + 512 * j));
+            tc2_cp_sf(sfb_t + 8 * j, desc_sf(sfb_smem + 512 * j));
+            tc2_cp_sf(sfb_t + 8 * j + 4, desc_sf(sfb_smem + P::SF_BYTES + 512 * j));
+          }
+          const uint64_t adesc = desc_sw128(st);
+          const uint64_t bdesc = desc_sw128(st + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 64; ++k) {
+            const int tl = (MODE == 2) ? k : (k >> 1);
+            const uint32_t sf_id = (MODE == 2) ? 0u : (uint32_t)((k & 1) * 2);
+            const uint32_t idesc = P::IDESC | (sf_id << 29) | (sf_id << 4);
+            tc2_mma<MODE>(tmem + ACC_COL, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                          sfa_t + 4 * tl, sfb_t + 8 * tl, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc2_commit_both(&empty[s]);
+        }
+        tc2_commit_both(acc_full);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    // Warp (q, h) drains lane quadrant q, columns [128 h, 128 h + 128), of this
+    // CTA's accumulator, releases it, then writes the 32 x 128 bf16 result as
+    // two 32 x 64 boxes through a 4 KB shared-memory stage (128-byte swizzled,
+    // so the row-per-lane writes hit every bank) and TMA tensor stores, which
+    // clip rows >= M and columns >= N.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const uint32_t acc_empty0 = mapa_u32(smem_u32(acc_empty), 0);
+    uint8_t* my_out = stage_out + (warp - 2) * 4096;
+    const uint32_t my_out_s = smem_u32(my_out);
+    int it = 0;
+    for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
+      const int b = tile / tiles_per_batch, rem = tile - b * tiles_per_batch;
+      const int mp = rem % num_mp, n_blk = rem / num_mp;
+      const float gx = gs_x ? __ldg(gs_x + b) : 1.0f;
+      const float alpha = __fmul_rn(gx, gs_w ? __ldg(gs_w + b) : 1.0f);
+      mbar_wait(acc_full, it & 1, err, failed);
+      tc_fence_after();
+      uint32_t o[64];
+#pragma unroll
+      for (int c4 = 0; c4 < 2; ++c4) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + ACC_COL + h * 128 + (c4 * 4 + j) * 16, r[j]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o[(c4 * 4 + j) * 8 + e] = pack_bf16x2_rn(__fmul_rn(__uint_as_float(r[j][2 * e]), alpha),
+                                                     __fmul_rn(__uint_as_float(r[j][2 * e + 1]), alpha));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty0);
+      const int row0 = mp * 256 + 128 * (int)rank + 32 * q;
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        // the previous box's store has finished reading the stage
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(my_out + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+              make_uint4(o[c2 * 32 + 4 * c], o[c2 * 32 + 4 * c + 1], o[c2 * 32 + 4 * c + 2], o[c2 * 32 + 4 * c + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        const int col0 = n_blk * BN + h * 128 + c2 * 64;
+        if (lane == 0 && row0 < M && col0 < N) {  // (a box wholly outside the output is not issued)
+          asm volatile(
+              "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+              :: "l"(&tmO), "r"(col0), "r"(row0), "r"(b), "r"(my_out_s) : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+  // no CTA of the pair retires while the other may still arrive on its barriers
+  // or (CTA 0's MMAs) write its tensor memory
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -517,6 +829,95 @@ cudaError_t launch_mode(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
   dim3 grid((unsigned)std::min<int64_t>(tiles, d.sm_count));
   qqmm_kernel<MODE, false><<<grid, kThreads, smem, s>>>(ta, tb, sx, sw, gs_x, gs_w, (int)M, (int)N, (int)K, bt,
                                                          out, d.err, inject, FusedX{});
+  return cudaGetLastError();
+}
+
+// 4-D view of 128x4-tiled scale bytes [batch][row tiles][K tiles * 2][256 bytes]:
+// one box is the TILES_PER_STAGE consecutive 512-byte tiles of one stage.
+bool make_scale_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int group, int tps, int64_t batch,
+                    int64_t batch_pitch) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int64_t rowtiles = (rows + 127) / 128;
+  const int64_t ktiles = (K / group) / 4;  // 128x4 tiles along K per row tile
+  cuuint64_t dims[4] = {256, (cuuint64_t)(ktiles * 2), (cuuint64_t)rowtiles, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {256, (cuuint64_t)(ktiles * 512),
+                           (cuuint64_t)(batch > 1 ? batch_pitch : rowtiles * ktiles * 512)};
+  cuuint32_t box[4] = {256, (cuuint32_t)(2 * tps), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// bf16 output [batch][M][N] (batch pitch in elements) for TMA stores of 32-row x
+// 64-column boxes, 128-byte swizzled in shared memory.
+bool make_out_map(CUtensorMap* m, void* ptr, int64_t M, int64_t N, int64_t batch, int64_t batch_pitch) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)(batch > 1 ? batch_pitch : M * N) * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Pairs of the pair kernel that can be resident at once (cached per device and
+// format; 0 if the query fails).
+template <int MODE>
+int pair_clusters(const DevInfo& d) {
+  static std::mutex mu;
+  static int cache[64];
+  static bool have[64];
+  if (d.device < 0 || d.device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (have[d.device]) return cache[d.device];
+  int n = 0;
+  const int smem = (int)PairCfg<MODE>::SMEM_BYTES;
+  if (cudaFuncSetAttribute(qqmm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * std::max(1, d.sm_count / 2)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    if (cudaOccupancyMaxActiveClusters(&n, qqmm_pair_kernel<MODE>, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();
+    }
+  } else {
+    cudaGetLastError();
+  }
+  cache[d.device] = n;
+  have[d.device] = true;
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_pair_mode(const DevInfo& d, int npairs_max, const uint32_t* xq, const uint8_t* sx,
+                             const uint32_t* wq, const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
+                             int64_t N, int64_t K, const BatchArgs& ba, uint16_t* out, int inject, cudaStream_t s) {
+  using P = PairCfg<MODE>;
+  constexpr int group = MODE == 2 ? 16 : 32;
+  CUtensorMap ta, tb, tsa, tsb, to;
+  const bool shared_w = ba.stride_wq == 0;
+  const int64_t wb = shared_w ? 1 : ba.batch;
+  if (!make_code_map(&ta, xq, M, K, 128, ba.batch, ba.stride_xq * 4) ||
+      !make_code_map(&tb, wq, N, K, 128, wb, ba.stride_wq * 4) ||
+      !make_scale_map(&tsa, sx, M, K, group, P::TPS, ba.batch, ba.stride_sx) ||
+      !make_scale_map(&tsb, sw, N, K, group, P::TPS, (shared_w || ba.stride_sw == 0) ? 1 : ba.batch, ba.stride_sw) ||
+      !make_out_map(&to, out, M, N, ba.batch, ba.stride_out))
+    return cudaErrorInvalidValue;
+  Batch bt;
+  bt.count = (int)ba.batch;
+  bt.wz = shared_w ? 0 : 1;
+  bt.stride_out = ba.stride_out;
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + 255) / 256) * ba.batch;
+  const int npairs = (int)std::min<int64_t>(tiles, npairs_max);
+  qqmm_pair_kernel<MODE><<<dim3((unsigned)(2 * npairs)), kThreads, P::SMEM_BYTES, s>>>(
+      ta, tb, tsa, tsb, to, gs_x, gs_w, (int)M, (int)N, (int)K, bt, d.err, inject);
   return cudaGetLastError();
 }
 
@@ -589,6 +990,12 @@ cudaError_t launch_qqmm(const DevInfo& d, const uint32_t* xq, const uint8_t* sx,
                         const uint8_t* sw, const float* gs_x, const float* gs_w, int64_t M,
                         int64_t N, int64_t K, const BatchArgs& ba, int mode, uint16_t* out, int inject_timeout,
                         cudaStream_t s) {
+  // the CTA-pair kernel whenever pairs of it can be resident; the one-SM kernel otherwise
+  const int np = mode == 2 ? pair_clusters<2>(d) : pair_clusters<1>(d);
+  if (np > 0) {
+    if (mode == 2) return launch_pair_mode<2>(d, np, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
+    return launch_pair_mode<1>(d, np, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
+  }
   if (mode == 2) return launch_mode<2>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
   return launch_mode<1>(d, xq, sx, wq, sw, gs_x, gs_w, M, N, K, ba, out, inject_timeout, s);
 }
