@@ -112,31 +112,19 @@ __device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t offset, uint64
 // up iff the top 24 bits of u are below floor(2^24 (|v| - lo) / (hi - lo));
 // |v| >= 6 gives 6; the sign bit is kept.  Every step is exact in fp32.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
+  // branch-free (the three grid spacings are selected, not branched on, so a
+  // warp's lanes never diverge): s = |v| / step is exact (step a power of 2),
+  // lo = floor(s) step, frac = s - floor(s) = (|v| - lo) / step exactly
   const float a = fabsf(v);
-  uint32_t idx;
-  if (!(a < 6.0f)) {
-    idx = 7;
-  } else {
-    uint32_t li;
-    float lo, inv_step;
-    if (a < 2.0f) {
-      li = __float2uint_rz(__fmul_rn(a, 2.0f));  // 0..3, steps of 0.5
-      lo = __fmul_rn((float)li, 0.5f);
-      inv_step = 2.0f;
-    } else if (a < 4.0f) {
-      const uint32_t f = __float2uint_rz(a);     // 2 or 3, steps of 1
-      li = f + 2u;
-      lo = (float)f;
-      inv_step = 1.0f;
-    } else {
-      li = 6u;                                   // 4, step of 2 to 6
-      lo = 4.0f;
-      inv_step = 0.5f;
-    }
-    const float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);
-    const uint32_t t = __float2uint_rz(__fmul_rn(frac, 16777216.0f));
-    idx = li + (((u >> 8) < t) ? 1u : 0u);
-  }
+  const bool r0 = a < 2.0f, r1 = a < 4.0f;
+  const float inv = r0 ? 2.0f : (r1 ? 1.0f : 0.5f);
+  const float s = __fmul_rn(a, inv);
+  const float fl = floorf(s);
+  const uint32_t f = __float2uint_rz(fl);
+  const uint32_t li = r0 ? f : (r1 ? f + 2u : 6u);
+  const float frac = __fsub_rn(s, fl);
+  const uint32_t t = __float2uint_rz(__fmul_rn(frac, 16777216.0f));
+  const uint32_t idx = (a < 6.0f) ? li + (((u >> 8) < t) ? 1u : 0u) : 7u;  // |v| >= 6 (or NaN): 6
   return idx | ((__float_as_uint(v) >> 28) & 8u);
 }
 
@@ -195,6 +183,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(
   constexpr int RT = (MODE == 2) ? 4 : 2;  // rows in flight per thread (64 or 128 bytes... 128 bytes)
   const int scols = cols / G;
   if ((int)blockIdx.x >= main_bx) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel may still use the buffer
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // zero the padding bytes of the tiled scale buffer
     const int64_t total = (int64_t)padded_rows * padded_cols;
     const int64_t nthreads = (int64_t)(gridDim.x - main_bx) * gridDim.y * blockDim.x;
@@ -210,6 +200,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(
     }
     return;
   }
+  // programmatic dependent launch: this grid may start while the previous
+  // kernel drains; x and the global scale are read only after it completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int gi = blockIdx.x * blockDim.x + threadIdx.x;  // group within the row
   if (gi >= scols) return;
   const float gs = (MODE == 2 && gs_ptr) ? __ldg(gs_ptr) : 1.0f;
@@ -301,35 +295,43 @@ cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* g
 cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, int64_t cols,
                             int mode, int group, const float* gs, uint32_t* xq, uint8_t* scales,
                             int tiled, int sr, uint64_t seed, uint64_t offset, cudaStream_t s) {
+  (void)d;
   const int64_t scols = cols / group;
   const int64_t main_bx = (scols + kQThreads - 1) / kQThreads;
   const int64_t prow = ((rows + 127) / 128) * 128, pcol = ((scols + 3) / 4) * 4;
-  // enough (x, y) blocks for ~16 resident 64-thread blocks per SM; each thread
-  // keeps 2-4 rows of loads in flight and strides over the rest
+  // one batch of rows per thread (4 NVFP4 rows, 2 MXFP4 rows: 128 bytes of
+  // loads in flight) and as many short-lived blocks as that takes -- measured
+  // faster on this stream than fewer, longer-lived threads with software
+  // pipelining; the loop strides over the rest only past 65535 row batches
   const int64_t rt = (mode == 2) ? 4 : 2;
-  int64_t gy = std::max<int64_t>(1, ((int64_t)d.sm_count * 16) / main_bx);
-  gy = std::min<int64_t>(gy, std::min<int64_t>((rows + rt - 1) / rt, 65535));
-  gy = std::max<int64_t>(gy, 1);
+  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>((rows + rt - 1) / rt, 65535));
   int64_t pad_bx = 0;
   if (tiled && (prow != rows || pcol != scols)) {
     const int64_t pad = prow * pcol;
     pad_bx = std::min<int64_t>(std::max<int64_t>((pad + kQThreads * gy - 1) / (kQThreads * gy), 1), 64);
   }
-  dim3 grid((unsigned)(main_bx + pad_bx), (unsigned)gy);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(main_bx + pad_bx), (unsigned)gy);
+  cfg.blockDim = dim3(kQThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int r = (int)rows, c = (int)cols, pr = (int)prow, pc = (int)pcol, mb = (int)main_bx;
   if (mode == 2 && sr)
-    quantize_kernel<2, true><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, gs, xq, scales, tiled, (int)prow,
-                                                        (int)pcol, (int)main_bx, seed, offset);
-  else if (mode == 2)
-    quantize_kernel<2, false><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, gs, xq, scales, tiled, (int)prow,
-                                                         (int)pcol, (int)main_bx, 0, 0);
-  else if (sr)
-    quantize_kernel<1, true><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, nullptr, xq, scales, tiled,
-                                                        (int)prow, (int)pcol, (int)main_bx, seed, offset);
-  else
-    quantize_kernel<1, false><<<grid, kQThreads, 0, s>>>(x, (int)rows, (int)cols, nullptr, xq, scales, tiled,
-                                                         (int)prow, (int)pcol, (int)main_bx, 0, 0);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<2, true>, x, r, c, gs, xq, scales, tiled, pr, pc, mb, seed, offset);
+  if (mode == 2)
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<2, false>, x, r, c, gs, xq, scales, tiled, pr, pc, mb,
+                              (uint64_t)0, (uint64_t)0);
+  if (sr)
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<1, true>, x, r, c, (const float*)nullptr, xq, scales, tiled, pr,
+                              pc, mb, seed, offset);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<1, false>, x, r, c, (const float*)nullptr, xq, scales, tiled, pr,
+                            pc, mb, (uint64_t)0, (uint64_t)0);
 }
+
 
 cudaError_t launch_dequantize(const DevInfo& d, const uint32_t* wq, const void* scales,
                               const uint16_t* biases, int64_t rows, int64_t cols, int mode,
