@@ -82,6 +82,24 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
+// 32 lanes x 64 consecutive 32-bit tensor-memory columns (one register per column)
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+}
+
 // byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -132,7 +150,8 @@ __device__ __forceinline__ void dequant_item(uint4 q, uint32_t sc, uint8_t* b_hi
 
 template <int MODE, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
-    const __grid_constant__ CUtensorMap tmX, const uint16_t* __restrict__ x, const int32_t* __restrict__ lhs,
+    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ lhs,
     const int32_t* __restrict__ rhs, int R, const uint32_t* __restrict__ w, const void* __restrict__ scales,
     const uint16_t* __restrict__ biases, const float* __restrict__ gs_w, int E, int N, int K, int group,
     uint16_t* __restrict__ out, unsigned* __restrict__ err, int inject_timeout) {
@@ -348,32 +367,54 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
   }
 
   // -------------------------------------------------------------- epilogue --
+  // Warp (q, hh) owns rows BM hh + 32 q .. + 31 of the tile: 64 columns at a time
+  // from tensor memory, times the NVFP4 global scale, rounded to bf16.  A band
+  // whose 32 rows all belong to the tile leaves through a 4 KB shared-memory
+  // stage (128-byte swizzled; the ring is idle once the last MMA completed)
+  // and a TMA tensor store, which clips columns >= N; the tile's last, partial
+  // band is stored row by row.
   if (warp < 4 * halves) {
     mbar_wait(accum_full, 0, err, failed);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const float gsw = (MODE == 2 && gs_w) ? __ldg(gs_w) : 1.0f;
     const int q = warp & 3, hh = warp >> 2;  // lane quadrant, half
-    const int r = BM * hh + 32 * q + lane;
+    const int rb = BM * hh + 32 * q;         // first row of the band
+    const int r = rb + lane;
+    const bool full_band = rb + 32 <= rows;
+    uint8_t* stage_o = smem + warp * 8192;   // two 4 KB boxes per warp
     uint16_t* orow = out + (int64_t)(row0 + r) * N;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      uint32_t v[16];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-          : "r"(tmem + ((uint32_t)(32 * q) << 16) + 256u * hh + c));
+    for (int c = 0; c < BN; c += 64) {
+      uint32_t v[64];
+      tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + 256u * hh + c, v);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int col = n0 + c;
-      if (r < rows) {
-        uint32_t o[8];
+      uint32_t o[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          o[e] = pack_bf16x2_rn(__fmul_rn(__uint_as_float(v[2 * e]), gsw), __fmul_rn(__uint_as_float(v[2 * e + 1]), gsw));
-        if (col < N) *reinterpret_cast<uint4*>(orow + col) = make_uint4(o[0], o[1], o[2], o[3]);
-        if (col + 8 < N) *reinterpret_cast<uint4*>(orow + col + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+      for (int e = 0; e < 32; ++e)
+        o[e] = pack_bf16x2_rn(__fmul_rn(__uint_as_float(v[2 * e]), gsw), __fmul_rn(__uint_as_float(v[2 * e + 1]), gsw));
+      const int col = n0 + c;
+      if (full_band) {
+        uint8_t* box = stage_o + ((c >> 6) & 1) * 4096;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // this box's previous store read it
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+              make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && col < N) {
+          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                       :: "l"(&tmO), "r"(col), "r"(row0 + rb), "r"(smem_u32(box)) : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      } else if (r < rows) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (col + 8 * k < N) *reinterpret_cast<uint4*>(orow + col + 8 * k) = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
       }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -404,12 +445,25 @@ cudaError_t launch_w4a16(const DevInfo& d, const uint16_t* x, const int32_t* lhs
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // output [R, N] bf16: TMA stores of 32-row x 64-column boxes, 128-byte swizzle
+  CUtensorMap tmO;
+  {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)R};
+    cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(w4a16_kernel<MODE, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t m_tiles = DENSE ? (R + TM - 1) / TM : (R + TM - 1) / TM + E;  // gather: upper bound on per-expert tiles
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)m_tiles);
-  w4a16_kernel<MODE, DENSE><<<grid, kThreads, C::kSmemBytes, s>>>(tmX, x, lhs, rhs, (int)R, w, scales, biases, gs_w,
+  w4a16_kernel<MODE, DENSE><<<grid, kThreads, C::kSmemBytes, s>>>(tmX, tmO, x, lhs, rhs, (int)R, w, scales, biases, gs_w,
                                                                    (int)E, (int)N, (int)K, group, out, d.err, inject);
   return cudaGetLastError();
 }
