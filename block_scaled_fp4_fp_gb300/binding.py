@@ -44,6 +44,7 @@ SIGNATURES = {
     "qmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _INT, _INT, _VP, _VP]),
     "qqmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP, _VP]),
     "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
+    "gather_rows": (_INT, [_VP, _I64, _VP, _I64, _I64, _VP, _VP]),
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
     "qqmm_batched": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
@@ -259,6 +260,15 @@ def gather_qmm(x: torch.Tensor, lhs_idx: torch.Tensor, rhs_idx: torch.Tensor, w:
         out = torch.empty((R, N), dtype=torch.bfloat16, device=w.device)
     _check(lib().gather_qmm(_p(x), _p(lhs_idx), _p(rhs_idx), R, _p(w), _p(scales), _p(biases), E, N, K, mode, 4,
                             group_size, 1 if sorted_indices else 0, _p(out), _s(stream)), "gather_qmm")
+    return out
+
+
+def gather_rows(x: torch.Tensor, idx: torch.Tensor, out=None, stream=None):
+    """out[i] = x[idx[i]] (bf16 rows; the routed activations in routing order)."""
+    R, (T, K) = idx.numel(), x.shape
+    if out is None:
+        out = torch.empty((R, K), dtype=x.dtype, device=x.device)
+    _check(lib().gather_rows(_p(x), T, _p(idx), R, K, _p(out), _s(stream)), "gather_rows")
     return out
 
 

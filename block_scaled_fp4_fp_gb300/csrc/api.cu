@@ -353,6 +353,17 @@ fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* 
                                      group_size, out, g_inject_timeout.load(), stream));
 }
 
+fp4_status gather_rows(const fp4_bf16* x, int64_t x_rows, const int32_t* idx, int64_t R, int64_t K, fp4_bf16* out,
+                       cudaStream_t stream) {
+  if (!x || !idx || !out || x_rows <= 0 || R <= 0 || K <= 0 || K % 8 != 0) return FP4_ERR_INVALID_ARG;
+  if (R > INT32_MAX || x_rows > INT32_MAX || K > (1 << 24)) return FP4_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(idx, 4)) return FP4_ERR_ALIGNMENT;
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  return from_cuda(launch_gather_rows(*d, x, x_rows, idx, R, K, out, stream));
+}
+
 fp4_status qmm(const fp4_bf16* x, const uint32_t* w, const void* scales, const fp4_bf16* biases,
                const float* global_scale_w, int64_t M, int64_t N, int64_t K, fp4_mode mode, int bits, int group_size,
                fp4_bf16* out, cudaStream_t stream) {

@@ -12,9 +12,9 @@
 //
 // Design.  A CTA owns one tile of up to 256 rows and one 256-column slice of N.
 // gather_qmm: rows arrive sorted by expert; tiles never straddle experts (the
-// tile -> expert map is rebuilt in every CTA by binary searches over the sorted
-// expert ids, so no workspace is needed).  qmm: the identity routing, one
-// "expert", tile t = rows 256 t ...  Per K = 64 stage:
+// tile -> expert map is rebuilt in every CTA from the expert ids, copied once
+// into the still idle stage ring, so no workspace is needed).  qmm: the
+// identity routing, one "expert", tile t = rows 256 t ...  Per K = 64 stage:
 //   * 16 producer warps dequantize the 256 x 64 weight slice exactly to bf16
 //     into the 128-byte-swizzled K-major layout the MMA reads, once for both
 //     128-row halves of the tile; each thread's codes and scales are loaded kPD
@@ -23,19 +23,20 @@
 //     epilogue); affine: w = q * scale + bias in fp32 split into two bf16 terms
 //     hi = bf16(w), lo = bf16(w - hi) (a single bf16 rounding of w would cost
 //     ~2.5e-3 relative error), each its own B operand;
-//   * gather_qmm: the producers gather the tile's activation rows with cp.async
-//     (16 bytes per copy, written in the same swizzled layout), and the copies
-//     arrive on the stage barrier by themselves when they land; qmm: one TMA box
-//     of 256 rows x 128 bytes per stage (rows past M read as zeros);
+//   * activations: qmm loads one TMA box of 256 rows x 128 bytes per stage (rows
+//     past M read as zeros); gather_qmm loads a tile whose routed rows are
+//     consecutive rows of x by 128-row TMA boxes, and otherwise gathers rows
+//     with cp.async (16 bytes per copy, written in the same swizzled layout),
+//     the copies arriving on the stage barrier by themselves when they land;
 //   * one thread issues tcgen05.mma.kind::f16 (bf16 x bf16, fp32 accumulators
 //     in tensor memory, M 128, N 256, K 16 per instruction): per half that holds
 //     rows one MMA (two for affine: hi then lo), each half into its own
 //     256-column accumulator;
 //   * after the last stage warps 0-7 (lane quadrant warp % 4, half warp / 4)
-//     read the accumulators (tcgen05.ld) and store bf16 rows of `out`.
+//     read the accumulators (tcgen05.ld) and write bf16 rows of `out` through a
+//     swizzled shared-memory stage and TMA tensor stores.
 // Every mbarrier wait is bounded (an expired wait records FP4_ERR_TIMEOUT).
 #include <algorithm>
-#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,30 +48,41 @@ namespace fp4 {
 namespace {
 
 constexpr int BM = 128;                // rows per MMA (one accumulator)
-constexpr int TM = 2 * BM;             // rows per tile: two MMA halves share each weight slice
-constexpr int BN = 256;
 constexpr int BK = 64;                 // bf16 elements per stage row: 128 bytes
 constexpr int kProducerWarps = 16;
 constexpr int kPD = 2;                 // weight prefetch distance (stages) in the producers' registers
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kProducers + 32;  // + MMA warp
 constexpr uint32_t A_HALF = BM * BK * 2;   // 16 KB: one 128-row half of the activations
+constexpr uint32_t TMEM_COLS = 512;
+
+// Tile geometry (qmm and gather_qmm): 256 rows (two 128-row MMA halves) x 256
+// columns.  Measured on the MoE shapes against 384 x 160 (three halves, so that
+// an expert of up to 384 rows is one tile) and 512 x 128: the N = 256 MMA is the
+// fastest per flop by a wide margin, which outweighs dequantizing the weight
+// slice again for an expert's last few rows.
+constexpr int TM = 2 * BM;                 // rows per tile
+constexpr int BN = 256;                    // columns per tile
 constexpr uint32_t A_BYTES = 2 * A_HALF;   // 32 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB per weight term
-constexpr uint32_t TMEM_COLS = 512;        // accumulator of half h at column 256 h
-constexpr int kItems = (BN * 2) / kProducers;  // (row, 32-code half) items per producer thread per stage
-static_assert(kItems == 1, "one weight item per producer thread per stage");
+constexpr int kItems = 2 * BN;             // (row, 32-code half) items per stage: one per producer thread
+static_assert(kItems == kProducers, "one weight item per producer thread per stage");
 // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, K-major, N>>3, M>>4
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(BM >> 4) << 24);
 
 // MODE 0 (affine) carries two weight terms per stage and fits two stages; the
 // FP4 formats one term and three stages.
-template <int MODE> struct Cfg {
+template <int MODE, bool DENSE> struct Cfg {
   static constexpr int kTerms = MODE == 0 ? 2 : 1;
   static constexpr int kStages = MODE == 0 ? 2 : 3;
   static constexpr uint32_t kStageBytes = A_BYTES + kTerms * B_BYTES;
-  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 2048;
+  // + 1024 alignment slack, 256 for barriers and the tile info, and gather_qmm's
+  // row map -- kept tight: past 196 KB per block the L1 that serves the weight
+  // scale loads shrinks from 60 to 28 KB, which costs qmm ~20 %
+  static constexpr uint32_t kReserve = 1024 + 256 + (DENSE ? 0 : TM * 4);
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + kReserve;
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
 };
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
@@ -155,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
     const int32_t* __restrict__ rhs, int R, const uint32_t* __restrict__ w, const void* __restrict__ scales,
     const uint16_t* __restrict__ biases, const float* __restrict__ gs_w, int E, int N, int K, int group,
     uint16_t* __restrict__ out, unsigned* __restrict__ err, int inject_timeout) {
-  using C = Cfg<MODE>;
+  using C = Cfg<MODE, DENSE>;
   constexpr int STAGES = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -182,12 +194,37 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
       tile_info[1] = tile_id * TM;
       tile_info[2] = min(TM, R - tile_id * TM);
     }
-  } else if (warp == 0) {
+  }
+  // The segment starts start[e] (first routed row whose id is >= e, e in [0, E]):
+  // while the ids fit in the idle stage ring, one coalesced pass copies them to
+  // shared memory and each row boundary fills the starts it separates (ids are
+  // clamped to [-1, E], so a broken contract cannot index outside start[]);
+  // otherwise warp 0 binary-searches global memory per expert.
+  const bool smem_map = !DENSE && (int64_t)R + E + 1 <= (int64_t)(C::kStages * C::kStageBytes / 4);
+  int* seg_start = reinterpret_cast<int*>(smem) + R;
+  if (smem_map) {
+    int* ids = reinterpret_cast<int*>(smem);
+#pragma unroll 8
+    for (int i = threadIdx.x; i < R; i += blockDim.x) {  // (unrolled: the loads overlap)
+      const int e = __ldg(rhs + i);
+      ids[i] = e < 0 ? -1 : min(e, E);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i <= R; i += blockDim.x) {
+      const int prev = i > 0 ? ids[i - 1] : -1, cur = i < R ? ids[i] : E;
+      for (int e = max(prev + 1, 0); e <= cur; ++e) seg_start[e] = i;
+    }
+    __syncthreads();
+  }
+  if (!DENSE && warp == 0) {
     int prefix = 0, found = 0, fe = 0, frow = 0, frows = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       int lo_b = 0, hi_b = 0;
-      if (e < E) {
+      if (e < E && smem_map) {
+        lo_b = seg_start[e];
+        hi_b = max(seg_start[e + 1], lo_b);
+      } else if (e < E) {
         int lo = 0, hi = R;  // first index with rhs >= e
         while (lo < hi) { const int mid = (lo + hi) >> 1; if (__ldg(rhs + mid) < e) lo = mid + 1; else hi = mid; }
         lo_b = lo;
@@ -250,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
   const int row0 = tile_info[1], rows = tile_info[2];
   if (!DENSE)
     for (int r = threadIdx.x; r < TM; r += blockDim.x) row_src[r] = (r < rows) ? __ldg(lhs + row0 + r) : 0;
-  const int halves = rows > BM ? 2 : 1;  // 128-row halves holding rows (uniform)
+  const int halves = (rows + BM - 1) / BM;  // 128-row halves holding rows (uniform)
   if (warp == kProducerWarps) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
@@ -262,6 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
   const uint32_t tmem = *tmem_slot;
   const int num_kb = K / BK;
   bool failed = false;  // this thread gave up a wait (see mbar_wait)
+  // gather_qmm: a tile whose routed rows are consecutive rows of x (activations
+  // already in routed order) loads its full 128-row halves by TMA boxes, like
+  // qmm; a partial last half, and every half of a scattered tile, by cp.async
+  int tma_halves = 0;
+  if (!DENSE) {
+    bool ok = true;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) ok &= row_src[r] == row_src[0] + r;
+    tma_halves = __syncthreads_and(ok) ? rows / BM : 0;
+  }
 
   if (warp < kProducerWarps) {
     // ---------------------------------------------------------- producers --
@@ -271,6 +317,20 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
     const int n = t >> 1, g = t & 1;            // this thread's item: row n, codes 32 g .. 32 g + 31 of a stage
     const bool nrow_ok = n0 + n < N;
     const uint32_t* wrow = w + (erow0 + n0 + n) * words_per_row;
+    // gather_qmm: this thread's activation copies, fixed for the tile -- 16-byte
+    // chunk t % 8 of rows t / 8 + 64 i (source pointer at K offset 0, swizzled
+    // destination offset within a stage)
+    constexpr int kCopies = (TM * 8) / kProducers;
+    const uint16_t* cp_src[kCopies];
+    uint32_t cp_dst[kCopies];
+    int cp_row[kCopies];
+#pragma unroll
+    for (int i = 0; i < kCopies; ++i) {
+      const int idx = t + kProducers * i;
+      cp_row[i] = idx >> 3;
+      cp_dst[i] = sw128(idx >> 3, idx & 7);
+      cp_src[i] = DENSE ? x : x + (int64_t)row_src[idx >> 3] * K + (idx & 7) * 8;
+    }
     // codes and scales of the item, kPD stages ahead in a register ring
     uint4 qr[kPD + 1];
     uint32_t sr[kPD + 1];
@@ -298,24 +358,30 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
           const uint32_t a_s = base + s * C::kStageBytes;
           uint8_t* b_s = smem + s * C::kStageBytes + A_BYTES;
           if (DENSE) {
-            // activations: one TMA box of 256 rows x 128 bytes (rows past the matrix read as zeros)
+            // activations: one TMA box of TM rows x 128 bytes (rows past the matrix read as zeros)
             if (t == 0) {
               mbar_arrive_expect_tx(&full[s], (uint32_t)A_BYTES);
               tma_load_2d(smem + s * C::kStageBytes, &tmX, &full[s], kb * BK, row0);
             }
           } else {
-            // activations: up to 256 rows x 8 chunks of 16 bytes by cp.async (half h at
-            // A_HALF h; a second half with no rows is not copied, its MMA is not issued);
-            // each thread's copies arrive on the stage barrier by themselves when they
-            // land (cp.async.mbarrier.arrive.noinc), so no producer waits for them
+            // activations: up to 256 rows x 8 chunks of 16 bytes (half h at A_HALF h; a
+            // half with no rows is not loaded, its MMA is not issued).  Halves below
+            // tma_halves: one TMA box of 128 whole rows each, whose bytes thread 0
+            // adds to the stage's expected transaction count (no arrival); the rest by
+            // cp.async, every thread's copies arriving on the stage barrier by
+            // themselves when they land (cp.async.mbarrier.arrive.noinc), so no
+            // producer waits for them.
+            if (t == 0 && tma_halves > 0) {
+              asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
+                           :: "r"(smem_u32(&full[s])), "r"((uint32_t)(tma_halves * A_HALF)) : "memory");
+              for (int h = 0; h < tma_halves; ++h)
+                tma_load_2d(smem + s * C::kStageBytes + h * A_HALF, &tmX, &full[s], kb * BK, row_src[0] + h * BM);
+            }
+            if (tma_halves < halves) {  // (uniform) rows left for the 16-byte copies
 #pragma unroll
-            for (int i = 0; i < (TM * 8) / kProducers; ++i) {
-              const int idx = t + kProducers * i;
-              const int r = idx >> 3, c = idx & 7;
-              if (r < BM * halves) {
-                const uint16_t* src = x + (int64_t)row_src[r] * K + kb * BK + c * 8;
-                cp_async16(a_s + sw128(r, c), src, r < rows ? 16u : 0u);
-              }
+              for (int i = 0; i < kCopies; ++i)
+                if (cp_row[i] >= BM * tma_halves && cp_row[i] < BM * halves)
+                  cp_async16(a_s + cp_dst[i], cp_src[i] + kb * BK, cp_row[i] < rows ? 16u : 0u);
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(&full[s])) : "memory");
           }
@@ -353,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                   "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                  :: "r"(tmem + 256u * hh), "l"(adesc + (uint64_t)(2 * k + (A_HALF >> 4) * hh)),
+                  :: "r"(tmem + (uint32_t)(BN * hh)), "l"(adesc + (uint64_t)(2 * k + (A_HALF >> 4) * hh)),
                      "l"(bdesc + (uint64_t)(2 * k + (B_BYTES >> 4) * tt)), "r"(IDESC), "r"(acc)
                   : "memory");
           }
@@ -386,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
 #pragma unroll 1
     for (int c = 0; c < BN; c += 64) {
       uint32_t v[64];
-      tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + 256u * hh + c, v);
+      tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * hh + c), v);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       uint32_t o[32];
 #pragma unroll
@@ -403,15 +469,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
               make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0 && col < N) {
-          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
-                       :: "l"(&tmO), "r"(col), "r"(row0 + rb), "r"(smem_u32(box)) : "memory");
+        if (lane == 0) {
+          if (col < N)
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                         :: "l"(&tmO), "r"(col), "r"(row0 + rb), "r"(smem_u32(box)) : "memory");
+          // one group per box, empty past N, so that "at most one pending" above
+          // always means this box's previous store has read it
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
       } else if (r < rows) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          if (col + 8 * k < N) *reinterpret_cast<uint4*>(orow + col + 8 * k) = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          if (col + 8 * k < N)
+            *reinterpret_cast<uint4*>(orow + col + 8 * k) = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
       }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -428,47 +498,87 @@ template <int MODE, bool DENSE>
 cudaError_t launch_w4a16(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
                          const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w, int64_t E,
                          int64_t N, int64_t K, int group, uint16_t* out, int inject, cudaStream_t s) {
-  using C = Cfg<MODE>;
+  using C = Cfg<MODE, DENSE>;
   if (C::kSmemBytes > d.smem_optin) return cudaErrorInvalidValue;
-  CUtensorMap tmX;
-  memset(&tmX, 0, sizeof(tmX));
-  if (DENSE) {
-    // activations [R, K] bf16: boxes of 256 rows x 64 elements (128 bytes), 128-byte swizzle
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorInvalidValue;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)TM};
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  auto map2d = [&](CUtensorMap* m, const void* p, int64_t inner, int64_t outer, uint32_t bi, uint32_t bo,
+                   CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {bi, bo};
     cuuint32_t estr[2] = {1, 1};
-    if (fn(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  // output [R, N] bf16: TMA stores of 32-row x 64-column boxes, 128-byte swizzle
-  CUtensorMap tmO;
-  {
-    auto fn = encode_fn();
-    if (!fn) return cudaErrorInvalidValue;
-    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)R};
-    cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-    cuuint32_t box[2] = {64, 32};
-    cuuint32_t estr[2] = {1, 1};
-    if (fn(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  CUtensorMap tmX, tmO;
+  // activations [rows, K]: boxes of 256 (qmm) or 128 (gather_qmm) rows x 64 elements
+  // (128 bytes), 128-byte swizzle (gather_qmm: x's row count is not an argument --
+  // the map is open-ended and only boxes of rows the routing names are loaded);
+  // output [R, N]: TMA stores of 32 rows x 64 columns, 128-byte swizzle
+  if (!map2d(&tmX, x, K, DENSE ? R : (int64_t)1 << 30, BK, DENSE ? TM : BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !map2d(&tmO, out, N, R, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(w4a16_kernel<MODE, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t m_tiles = DENSE ? (R + TM - 1) / TM : (R + TM - 1) / TM + E;  // gather: upper bound on per-expert tiles
+  // gather: an upper bound on the per-expert tiles; slots past the last tile exit at once
+  const int64_t m_tiles = DENSE ? (R + TM - 1) / TM : (R + TM - 1) / TM + E;
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)m_tiles);
-  w4a16_kernel<MODE, DENSE><<<grid, kThreads, C::kSmemBytes, s>>>(tmX, tmO, x, lhs, rhs, (int)R, w, scales, biases, gs_w,
-                                                                   (int)E, (int)N, (int)K, group, out, d.err, inject);
+  w4a16_kernel<MODE, DENSE><<<grid, kThreads, C::kSmemBytes, s>>>(tmX, tmO, x, lhs, rhs, (int)R, w, scales,
+                                                                   biases, gs_w, (int)E, (int)N, (int)K, group, out,
+                                                                   d.err, inject);
   return cudaGetLastError();
 }
 
+// out[i, :] = x[idx[i], :]: one warp per row at a time, 16-byte pieces; an index
+// outside [0, x_rows) leaves its row unwritten and is reported.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int64_t x_rows,
+                                                          const int32_t* __restrict__ idx, int64_t R, int pieces,
+                                                          uint4* __restrict__ out, unsigned* __restrict__ err) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < R; i += warps) {
+    const int64_t src = __ldg(idx + i);
+    if (src < 0 || src >= x_rows) {
+      if (lane == 0) record_error(err, kErrIndex);
+      continue;
+    }
+    const uint4* a = x + src * pieces;
+    uint4* o = out + i * pieces;
+    int c = lane;
+    for (; c + 96 < pieces; c += 128) {  // four 16-byte loads in flight per lane
+      const uint4 v0 = ld_stream_v4(a + c), v1 = ld_stream_v4(a + c + 32), v2 = ld_stream_v4(a + c + 64),
+                  v3 = ld_stream_v4(a + c + 96);
+      o[c] = v0;
+      o[c + 32] = v1;
+      o[c + 64] = v2;
+      o[c + 96] = v3;
+    }
+    for (; c < pieces; c += 32) o[c] = ld_stream_v4(a + c);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const DevInfo& d, const uint16_t* x, int64_t x_rows, const int32_t* idx, int64_t R,
+                               int64_t K, uint16_t* out, cudaStream_t s) {
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((R + 7) / 8, (int64_t)d.sm_count * 8));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, reinterpret_cast<const uint4*>(x), x_rows, idx, R, (int)(K / 8),
+                            reinterpret_cast<uint4*>(out), d.err);
+}
 
 cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
                               const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w,

@@ -84,6 +84,8 @@ cudaError_t launch_weight_stream(const DevInfo& d, const uint32_t* w, const uint
 // gather_qmm.cu: W4A16 GEMMs (MXFP4 = 1, NVFP4 = 2, affine = 0 weights) -- the MoE
 // gather_qmm (rows sorted by expert) and the dense qmm (gs_w: NVFP4 weight global
 // scale or nullptr; biases: affine only)
+cudaError_t launch_gather_rows(const DevInfo& d, const uint16_t* x, int64_t x_rows, const int32_t* idx, int64_t R,
+                               int64_t K, uint16_t* out, cudaStream_t s);
 cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
                               const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w,
                               int64_t E, int64_t N, int64_t K, int mode, int group, uint16_t* out, int inject_timeout,

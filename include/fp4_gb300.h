@@ -222,11 +222,25 @@ fp4_status qqmm(const uint32_t* xq, const uint8_t* sx, const uint32_t* wq, const
  * live in device memory, so the kernel checks them: an id outside [0, E) or a
  * decrease leaves the affected output rows unwritten and makes the next
  * fp4_check_device_error return FP4_ERR_INVALID_ARG.  lhs_idx values must lie in
- * [0, T); they are not checked. */
+ * [0, T); they are not checked.  A tile whose routed rows are consecutive rows
+ * of x (activations already in routed order, e.g. after gather_rows) loads
+ * them by TMA; scattered rows are gathered 16 bytes at a time. */
 fp4_status gather_qmm(const fp4_bf16* x, const int32_t* lhs_idx, const int32_t* rhs_idx, int64_t R,
                       const uint32_t* w, const void* scales, const fp4_bf16* biases, int64_t E,
                       int64_t N, int64_t K, fp4_mode mode, int bits, int group_size, int sorted,
                       fp4_bf16* out, cudaStream_t stream);
+
+/* gather_rows: the routed activations in routing order [P2 Diagnosis 5: the
+ * MoE grouped GEMM gathers each routed row's activations], so that a following
+ * gather_qmm with lhs_idx = 0 .. R-1 reads them as whole tiles.
+ *   out[i, :] = x[idx[i], :]   for i < R (pure data movement, bit-exact)
+ *   x      bf16[x_rows, K], 16-byte aligned;  idx int32[R], 4-byte aligned
+ *   out    bf16[R, K], 16-byte aligned, caller-owned (R K 2 bytes)
+ * Requires K % 8 == 0.  An index outside [0, x_rows) leaves its output row
+ * unwritten and makes the next fp4_check_device_error return
+ * FP4_ERR_INVALID_ARG. */
+fp4_status gather_rows(const fp4_bf16* x, int64_t x_rows, const int32_t* idx, int64_t R, int64_t K, fp4_bf16* out,
+                       cudaStream_t stream);
 
 /* qqmm_batched: batch_count independent FP4 x FP4 GEMMs in one launch [P3
  * qqmm_impl: the page's cuBLASLt call fixes the batch count at 1; this is the

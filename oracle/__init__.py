@@ -389,6 +389,13 @@ def gather_qmm(x, lhs, rhs, w, scales, biases, mode, group, rows=None):
 GROUP_OF = {MODE_NVFP4: 16, MODE_MXFP4: 32}
 
 
+def gather_rows(x, idx):
+    """The routed activations in routing order: out[i] = x[idx[i]] (bf16 bits,
+    "epic: NVIDIA Volta (sm_70) inference acceleration program #1536",
+    Diagnosis 5: the grouped GEMM gathers each routed row)."""
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint16)[np.asarray(idx, dtype=np.int64)])
+
+
 def quantize_dequantize(x, mode, gs=None):
     """fp_quantize_dequantize: quantize bf16 ``x`` [rows, cols] (NVFP4 with the
     optional multiplier-form global scale ``gs``, or MXFP4) and dequantize it

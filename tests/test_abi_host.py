@@ -114,5 +114,10 @@ def test_validation_rejects_before_launch(B):
                              None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.qqmm_quantize_x(p, None, p, p, None, 128, 256, 256, B.MODE_NVFP4, ctypes.c_void_p(256 + 64), wsb, None,
                              p, None) == B.FP4_ERR_ALIGNMENT  # workspace not 128-byte aligned
+    assert L.gather_rows(p, 4, p, 8, 12, p, None) == B.FP4_ERR_INVALID_ARG  # K % 8
+    assert L.gather_rows(p, 0, p, 8, 16, p, None) == B.FP4_ERR_INVALID_ARG  # no x rows
+    assert L.gather_rows(p, 4, p, 0, 16, p, None) == B.FP4_ERR_INVALID_ARG  # R = 0
+    assert L.gather_rows(None, 4, p, 8, 16, p, None) == B.FP4_ERR_INVALID_ARG
+    assert L.gather_rows(odd, 4, p, 8, 16, p, None) == B.FP4_ERR_ALIGNMENT
     assert L.fp4_debug_stream_weights(p, p, 64, 320, None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.fp4_debug_stream_weights(odd, p, 64, 256, None) == B.FP4_ERR_ALIGNMENT

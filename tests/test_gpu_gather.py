@@ -71,12 +71,12 @@ def test_gather_moe_down_full_size_sampled(B):
 
 def test_gather_segments_on_tile_boundaries(B):
     """Hand-built routing whose expert segments are empty, one row, and 127 /
-    128 / 129 / 255 / 256 / 257 / 384 / 513 rows long, so the tiles of up to
-    256 rows (two 128-row MMA halves) start, end and straddle every boundary
-    case: one half, both halves, a one-row tail; activation rows repeat and
-    come in any order."""
-    E, N, K = 11, 96, 128
-    sizes = [0, 1, 127, 128, 0, 129, 255, 256, 257, 384, 513]
+    128 / 129 / 255 / 256 / 257 / 383 / 384 / 385 / 513 / 769 rows long, so the
+    tiles of up to 256 rows (two 128-row MMA halves) start, end and straddle
+    every boundary case: one half, both halves, a one-row tail; activation rows
+    repeat and come in any order (the 16-byte gather path)."""
+    E, N, K = 14, 96, 128
+    sizes = [0, 1, 127, 128, 0, 129, 255, 256, 257, 383, 384, 385, 513, 769]
     rhs = np.repeat(np.arange(E, dtype=np.int32), sizes)
     R = len(rhs)
     tokens = 200
@@ -132,4 +132,65 @@ def test_gather_routing_contract_violation_is_reported(B, bad):
     assert B.fp4_check_device_error() == B.FP4_ERR_INVALID_ARG
     good = np.repeat(np.arange(E, dtype=np.int32), tokens // E)
     B.gather_qmm(x, torch.from_numpy(lhs).cuda(), torch.from_numpy(good).cuda(), q3, s3)
+    assert B.fp4_check_device_error() == B.FP4_OK
+
+
+@pytest.mark.parametrize("scatter", [False, True])
+def test_gather_contiguous_rows_tma_path(B, scatter):
+    """Activations already in routed order: every tile's rows are consecutive rows
+    of x (starting 7 rows in, x longer than the routing), so the full 128-row
+    halves arrive by TMA boxes and a partial last half by the 16-byte gather.
+    With `scatter`, one expert's segment has two rows swapped, so that tile
+    falls back to the gather while the others keep the TMA path."""
+    E, N, K = 12, 160 + 48, 192
+    sizes = [1, 127, 128, 129, 256, 257, 383, 384, 385, 0, 513, 200]
+    rhs = np.repeat(np.arange(E, dtype=np.int32), sizes)
+    R = len(rhs)
+    lhs = (np.arange(R) + 7).astype(np.int32)
+    if scatter:
+        a = sum(sizes[:6]) + 10
+        lhs[a], lhs[a + 100] = lhs[a + 100], lhs[a]
+    x = synth.bf16_normal((R + 20, K), 1.0, seed=61)
+    w = synth.bf16_normal((E * N, K), 0.02, seed=62)
+    q, s = oracle.mxfp4_quantize(synth.to_u16(w))
+    q3, s3 = q.reshape(E, N, K // 8), s.reshape(E, N, K // 32)
+    out = B.gather_qmm(x.cuda(), torch.from_numpy(lhs).cuda(), torch.from_numpy(rhs).cuda(),
+                       torch.from_numpy(q3.view(np.int32)).cuda(), torch.from_numpy(s3).cuda())
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    ref = oracle.gather_qmm(synth.to_u16(x), lhs, rhs, q3, s3, None, oracle.MODE_MXFP4, 32)
+    assert_close_to_oracle(out, ref, f"gather contiguous rows (scatter={scatter})")
+
+
+@pytest.mark.parametrize("T,R,K", [(1, 1, 8), (37, 300, 2880), (2048, 8192, 2880), (5, 64, 4104)])
+def test_gather_rows_bit_exact(B, T, R, K):
+    """gather_rows moves bf16 rows into routing order: bit-exact against the
+    oracle's indexing (ragged K, repeated and arbitrary indices)."""
+    x = synth.bf16_normal((T, K), 1.0, seed=T + K)
+    idx = np.random.default_rng(R).integers(0, T, R).astype(np.int32)
+    out = B.gather_rows(x.cuda(), torch.from_numpy(idx).cuda())
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    ref = oracle.gather_rows(synth.to_u16(x), idx)
+    assert np.array_equal(synth.to_u16(out.cpu()), ref)
+
+
+def test_gather_rows_bad_index_is_reported(B):
+    """An index outside [0, x_rows) leaves its row unwritten and is reported;
+    the other rows are still moved, and the next valid call reports nothing."""
+    T, R, K = 10, 6, 64
+    x = synth.bf16_normal((T, K), 1.0, seed=71).cuda()
+    idx = torch.tensor([0, 9, -1, 3, 10, 4], dtype=torch.int32).cuda()
+    out = torch.full((R, K), 7.0, dtype=torch.bfloat16).cuda()
+    B.fp4_check_device_error()
+    B.gather_rows(x, idx, out=out)
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_ERR_INVALID_ARG
+    for i, j in enumerate([0, 9, None, 3, None, 4]):
+        if j is None:
+            assert bool((out[i] == 7.0).all())
+        else:
+            assert torch.equal(out[i], x[j])
+    B.gather_rows(x, idx.clamp(0, T - 1), out=out)
+    torch.cuda.synchronize()
     assert B.fp4_check_device_error() == B.FP4_OK

@@ -153,6 +153,31 @@ def test_gather_qmm_routes_rows_to_experts():
     assert np.array_equal(sub, out[[5, 1]])
 
 
+def test_gather_rows_is_row_indexing_and_commutes_with_gather_qmm():
+    """gather_rows against a plain loop over the index list, and the identity the
+    routed-order path relies on: gather_qmm over x with routing lhs equals
+    gather_qmm over gather_rows(x, lhs) with the identity routing."""
+    T, K = 7, 16
+    x = synth.to_u16(synth.bf16_normal((T, K), 1.0, seed=11))
+    idx = np.array([6, 0, 0, 3, 6, 2, 5], np.int32)
+    g = oracle.gather_rows(x, idx)
+    assert g.dtype == np.uint16 and g.shape == (len(idx), K)
+    for i, j in enumerate(idx):
+        for k in range(K):
+            assert g[i, k] == x[j, k]
+    E, N, K2 = 3, 16, 64
+    w = synth.bf16_normal((E * N, K2), 0.02, seed=12)
+    q, s = oracle.mxfp4_quantize(synth.to_u16(w))
+    q3, s3 = q.reshape(E, N, K2 // 8), s.reshape(E, N, K2 // 32)
+    xb = synth.to_u16(synth.bf16_normal((T, K2), 1.0, seed=13))
+    lhs = np.array([4, 1, 1, 6, 0, 2, 3, 5], np.int32)
+    rhs = np.array([0, 0, 0, 1, 1, 2, 2, 2], np.int32)
+    a = oracle.gather_qmm(xb, lhs, rhs, q3, s3, None, oracle.MODE_MXFP4, 32)
+    b = oracle.gather_qmm(oracle.gather_rows(xb, lhs), np.arange(len(lhs), dtype=np.int32), rhs, q3, s3, None,
+                          oracle.MODE_MXFP4, 32)
+    assert np.array_equal(a, b)
+
+
 def test_moe_routing_is_sorted_topk_without_repeats():
     lhs, rhs = synth.moe_routing(tokens=64, experts=8, topk=4, seed=0)
     assert len(lhs) == 256 and np.all(np.diff(rhs) >= 0)
