@@ -200,9 +200,18 @@ class DecodeStack:
         self.B, self.mode, self.layers, self.qx = B, mode, layers, qx
         self.mats = []
         self.bytes = 0
+        # "split_grouped": one matrix per projection, as "split", but the projections
+        # that multiply the same x (q, k, v; gate, up) run as one qmv_grouped launch
+        self.grouped = layout == "split_grouped"
+        self.launch_groups = []
         for l in range(layers):
-            for N, K, grp in layer_groups(layout):
+            for N, K, grp in layer_groups("split" if self.grouped else layout):
                 self.mats.append(self._make(l, N, K, grp, device))
+            base = len(self.mats) - len(layer_groups("split" if self.grouped else layout))
+            if self.grouped:
+                self.launch_groups += [[base + p for p in g] for _, _, g in layer_groups("fused")]
+            else:
+                self.launch_groups += [[i] for i in range(base, len(self.mats))]
         self.x = {K: synth.decode_x(K, device=device) for K in {k for _, _, k in synth.LAYER_PROJECTIONS}}
         self.gs_x = {K: (B.fp4_amax_global_scale(v) if qx and mode == B.MODE_NVFP4 else None)
                      for K, v in self.x.items()}
@@ -226,6 +235,17 @@ class DecodeStack:
 
     def step(self, stream=None):
         B = self.B
+        if self.grouped:
+            for g in self.launch_groups:
+                ms = [self.mats[i] for i in g]
+                if len(g) == 1:
+                    m = ms[0]
+                    B.qmv(self.x[m["K"]], m["q"], m["s"], m["b"], m["gs"], mode=self.mode, y=self.y[g[0]],
+                          stream=stream)
+                else:
+                    B.qmv_grouped(self.x[ms[0]["K"]], [(m["q"], m["s"], m["b"], m["gs"]) for m in ms],
+                                  mode=self.mode, ys=[self.y[i] for i in g], stream=stream)
+            return
         for m, y in zip(self.mats, self.y):
             if self.qx:
                 B.qqmv(self.x[m["K"]], m["q"], m["s"], self.gs_x[m["K"]], m["gs"], mode=self.mode, y=y, stream=stream)
@@ -240,7 +260,7 @@ class DecodeStack:
 
     @property
     def launches(self):
-        return len(self.mats)
+        return len(self.launch_groups)
 
 
 WORKLOAD = ("decode qmv over a 64-layer hidden-5120 stack (q,k,v,o 5120x5120; gate,up 17408x5120; "
@@ -614,8 +634,11 @@ def run_ours(args):
     # the headline: NVFP4 weights in the fused layout (4 GEMVs a layer); the
     # per-projection layout and the other formats are components
     modes = [("nvfp4_fused", B.MODE_NVFP4, "fused", False)] + (
-        [] if args.quick else [("nvfp4", B.MODE_NVFP4, "split", False), ("mxfp4_fused", B.MODE_MXFP4, "fused", False),
+        [] if args.quick else [("nvfp4", B.MODE_NVFP4, "split", False),
+                               ("nvfp4_grouped", B.MODE_NVFP4, "split_grouped", False),
+                               ("mxfp4_fused", B.MODE_MXFP4, "fused", False),
                                ("mxfp4", B.MODE_MXFP4, "split", False),
+                               ("mxfp4_grouped", B.MODE_MXFP4, "split_grouped", False),
                                ("affine_g64", B.MODE_AFFINE, "split", False),
                                ("affine_g64_fused", B.MODE_AFFINE, "fused", False),
                                ("nvfp4_fused_quantized_x", B.MODE_NVFP4, "fused", True),
@@ -638,7 +661,9 @@ def run_ours(args):
         results[name] = {"ms_per_step": ms, "GB/s": stack.bytes / ms / 1e6, "bytes_per_step": stack.bytes,
                          "frac_of_hbm": stack.bytes / ms / 1e6 / peaks["hbm_gbs"],
                          "launches_per_step": stack.launches, "layout": layout,
-                         "entry_point": "qqmv (x quantized inside the GEMV)" if qx else "qmv"}
+                         "entry_point": ("qqmv (x quantized inside the GEMV)" if qx else
+                                         "qmv_grouped (q,k,v and gate,up one launch each) + qmv"
+                                         if layout == "split_grouped" else "qmv")}
         if name != "nvfp4_fused":
             del stack, graph
             torch.cuda.empty_cache()

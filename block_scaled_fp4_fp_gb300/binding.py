@@ -45,6 +45,7 @@ SIGNATURES = {
     "qqmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP, _VP]),
     "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
     "gather_rows": (_INT, [_VP, _I64, _VP, _I64, _I64, _VP, _VP]),
+    "qmv_grouped": (_INT, [_VP, _INT, _VP, _VP, _VP, _VP, _VP, _I64, _INT, _INT, _INT, _VP, _VP]),
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
     "qqmm_batched": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
@@ -261,6 +262,27 @@ def gather_qmm(x: torch.Tensor, lhs_idx: torch.Tensor, rhs_idx: torch.Tensor, w:
     _check(lib().gather_qmm(_p(x), _p(lhs_idx), _p(rhs_idx), R, _p(w), _p(scales), _p(biases), E, N, K, mode, 4,
                             group_size, 1 if sorted_indices else 0, _p(out), _s(stream)), "gather_qmm")
     return out
+
+
+def qmv_grouped(x: torch.Tensor, mats, mode: int = MODE_NVFP4, group_size: int = None, ys=None, stream=None):
+    """One x against up to 4 matrices of the same K in one launch.  mats: a list of
+    (w, scales, biases, global_scale_w) tuples (biases / global scale may be None);
+    returns the list of y vectors."""
+    group_size = group_size or GROUP[mode]
+    count = len(mats)
+    K = mats[0][0].shape[1] * 8
+    Ns = [m[0].shape[0] for m in mats]
+    if ys is None:
+        ys = [torch.empty((n,), dtype=torch.bfloat16, device=mats[0][0].device) for n in Ns]
+    P = c.c_void_p * count
+    w = P(*[m[0].data_ptr() for m in mats])
+    sc = P(*[m[1].data_ptr() for m in mats])
+    bi = P(*[m[2].data_ptr() for m in mats]) if mats[0][2] is not None else None
+    gs = P(*[(m[3].data_ptr() if m[3] is not None else None) for m in mats]) if any(m[3] is not None for m in mats) else None
+    nn = (c.c_int64 * count)(*Ns)
+    yy = P(*[y.data_ptr() for y in ys])
+    _check(lib().qmv_grouped(_p(x), count, w, sc, bi, gs, nn, K, mode, 4, group_size, yy, _s(stream)), "qmv_grouped")
+    return ys
 
 
 def gather_rows(x: torch.Tensor, idx: torch.Tensor, out=None, stream=None):

@@ -221,6 +221,57 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
                               g_inject_timeout.load(), stream));
 }
 
+fp4_status qmv_grouped(const fp4_bf16* x, int count, const uint32_t* const* w, const void* const* scales,
+                       const fp4_bf16* const* biases, const float* const* global_scale_w, const int64_t* N, int64_t K,
+                       fp4_mode mode, int bits, int group_size, fp4_bf16* const* y, cudaStream_t stream) {
+  if (count < 1 || count > 4 || !w || !scales || !N || !y) return FP4_ERR_INVALID_ARG;
+  // every matrix must be a valid qmv on its own (same checks, same x)
+  for (int i = 0; i < count; ++i) {
+    if (!w[i] || !scales[i] || !y[i]) return FP4_ERR_INVALID_ARG;
+    const fp4_bf16* b = biases ? biases[i] : nullptr;
+    const float* g = global_scale_w ? global_scale_w[i] : nullptr;
+    fp4_status st = check_format(mode, bits, group_size);
+    if (st != FP4_OK) return st;
+    if (!x || N[i] <= 0 || K <= 0 || K % 32 != 0 || K % group_size != 0 || N[i] > INT32_MAX / 2)
+      return FP4_ERR_INVALID_ARG;
+    if (K > 65536) return FP4_ERR_UNSUPPORTED;
+    if (mode == FP4_MODE_AFFINE) {
+      if (!b || g) return FP4_ERR_INVALID_ARG;
+      if (!aligned(scales[i], 2) || !aligned(b, 2)) return FP4_ERR_ALIGNMENT;
+    } else {
+      if (b) return FP4_ERR_INVALID_ARG;
+      if (g && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+      if (g && !aligned(g, 4)) return FP4_ERR_ALIGNMENT;
+      if (mode == FP4_MODE_NVFP4 && !aligned(scales[i], 2)) return FP4_ERR_ALIGNMENT;
+    }
+    if (!aligned(x, 16) || !aligned(w[i], 16) || !aligned(y[i], 2)) return FP4_ERR_ALIGNMENT;
+  }
+  const DevInfo* d = nullptr;
+  fp4_status st = current(&d);
+  if (st != FP4_OK) return st;
+  // one launch on the tensor-core GEMV when it takes the whole group (FP4 formats,
+  // 16-byte aligned scale rows, a plan for the stacked rows); otherwise one qmv each
+  bool one = (mode == FP4_MODE_NVFP4 || mode == FP4_MODE_MXFP4) && qmv_tc_group_supported(*d, mode, count, N, K);
+  for (int i = 0; i < count && one; ++i) one = aligned(scales[i], 16);
+  if (one) {
+    const uint8_t* sc[4];
+    uint16_t* yy[4];
+    for (int i = 0; i < count; ++i) {
+      sc[i] = static_cast<const uint8_t*>(scales[i]);
+      yy[i] = reinterpret_cast<uint16_t*>(y[i]);
+    }
+    return from_cuda(launch_qmv_tc_group(*d, mode, x, nullptr, 0, count, w, sc, global_scale_w, N, K, yy,
+                                         g_inject_timeout.load(), stream));
+  }
+  for (int i = 0; i < count; ++i) {
+    const cudaError_t e = launch_qmv(*d, x, nullptr, 0, w[i], scales[i], biases ? biases[i] : nullptr,
+                                     global_scale_w ? global_scale_w[i] : nullptr, N[i], K, mode, group_size, y[i],
+                                     g_inject_timeout.load(), stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return FP4_OK;
+}
+
 fp4_status qqmv(const fp4_bf16* x, const float* global_scale_x, const uint32_t* w, const uint8_t* scales,
                 const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, fp4_bf16* y,
                 cudaStream_t stream) {

@@ -56,6 +56,7 @@
 //           quadrant 0 read D's term lanes (16x256b loads) and add them per
 //           column with warp shuffles into the partials.
 #include <algorithm>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -75,6 +76,7 @@ constexpr int kXPre = 5;            // weight stages issued before x has landed 
 constexpr int kChunk = 256;         // codes per TMA box (128 bytes per row)
 constexpr int kRows = 256;          // W rows per CTA at most (MMA N <= 256)
 constexpr int kMaxSplit = 4;        // CTAs per cluster at most (the plan takes 1, 2 or 4)
+constexpr int kMaxGroup = 4;        // matrices of one grouped launch at most
 constexpr int kGroups = 4;          // prep groups; group g prepares local stages i % kGroups == g
 constexpr int kGroupThreads = 128;  // one group = 4 warps, one per lane quadrant
 constexpr int kPrep = kGroups * kGroupThreads;
@@ -163,15 +165,27 @@ __device__ __forceinline__ uint32_t map_rank(const void* p, int rank) {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
+// The matrices of one launch: a plain GEMV is a group of one; a grouped GEMV
+// multiplies the same x by up to kMaxGroup matrices of the same K (q, k and v
+// stored apart, say).  Matrix m owns row blocks blk0[m] .. blk0[m+1]-1, its rows
+// dealt out evenly over them; each has its own tensor maps, global scale and y.
+struct QmvGroup {
+  CUtensorMap tmW[kMaxGroup];  // codes [N_m, K/2] bytes, boxes of R rows x 128 bytes
+  CUtensorMap tmS[kMaxGroup];  // linear scales [N_m, K/group], boxes of R rows x 16 bytes
+  const float* gs_w[kMaxGroup];
+  uint16_t* y[kMaxGroup];
+  int N[kMaxGroup];
+  int blk0[kMaxGroup + 1];
+  int count;
+};
+
 template <int MODE, bool QX>
-__global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                              const __grid_constant__ CUtensorMap tmS,
+__global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_constant__ QmvGroup mats,
                                                               const uint16_t* __restrict__ x,
-                                                              const float* __restrict__ gs_x,
-                                                              const float* __restrict__ gs_w, int N, int K,
+                                                              const float* __restrict__ gs_x, int K,
                                                               int R, int split, int nslots, uint32_t wslot,
-                                                              uint32_t sslot, uint16_t* __restrict__ y,
-                                                              unsigned* __restrict__ err, int inject_timeout) {
+                                                              uint32_t sslot, unsigned* __restrict__ err,
+                                                              int inject_timeout) {
   using F = Fmt<MODE>;
   using G = Geo<MODE>;
   using L = Lay<MODE>;
@@ -200,9 +214,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)(blockIdx.x % (unsigned)split);  // rank within the cluster (clusters are consecutive)
   const int blk = (int)(blockIdx.x / (unsigned)split);
-  const int nblk = (int)(gridDim.x / (unsigned)split);
-  const int r0 = (int)(((int64_t)N * blk) / nblk);
-  const int r1 = (int)(((int64_t)N * (blk + 1)) / nblk);
+  int mi = 0;  // this CTA's matrix
+  while (mi + 1 < mats.count && blk >= mats.blk0[mi + 1]) ++mi;
+  const int lb = blk - mats.blk0[mi], nblk = mats.blk0[mi + 1] - mats.blk0[mi];
+  const int r0 = (int)(((int64_t)mats.N[mi] * lb) / nblk);
+  const int r1 = (int)(((int64_t)mats.N[mi] * (lb + 1)) / nblk);
+  const CUtensorMap* tmW = &mats.tmW[mi];
+  const CUtensorMap* tmS = &mats.tmS[mi];
   const int rows = r1 - r0;  // <= R <= 256
   const int nmma = (R + 15) & ~15;  // MMA N
   const int nkb = K / kBK;
@@ -251,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (weights)
     if (elect_one_sync()) {
-      prefetch_tmap(&tmW);
-      prefetch_tmap(&tmS);
+      prefetch_tmap(tmW);
+      prefetch_tmap(tmS);
       // out-of-range rows are zero-filled and counted
       const uint32_t tx = (uint32_t)R * (128u * kCh + G::kSB);
       int s = 0, round = 0;
@@ -265,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
         mbar_arrive_expect_tx(&wfull[s], tx);
 #pragma unroll
         for (int h = 0; h < kCh; ++h)
-          tma_load_2d(smem + s * wslot + h * wchunk, &tmW, &wfull[s], ((kb0 + i) * kCh + h) * 128, r0);
-        tma_load_2d(smem + offS + s * sslot, &tmS, &wfull[s], (kb0 + i) * G::kSB, r0);
+          tma_load_2d(smem + s * wslot + h * wchunk, tmW, &wfull[s], ((kb0 + i) * kCh + h) * 128, r0);
+        tma_load_2d(smem + offS + s * sslot, tmS, &wfull[s], (kb0 + i) * G::kSB, r0);
         if (++s == nslots) { s = 0; ++round; }
       }
       // no copy may still be writing shared memory when the CTA exits
@@ -541,7 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
           if (grp == 0 && lane == 0) mbar_arrive_expect_tx(pbar, (uint32_t)(split - 1) * (uint32_t)rows * 4u);
           mbar_wait(pbar, 0, err, failed);  // every other rank's partials have landed
         }
-        const float g = gs_w ? __ldg(gs_w) : 1.0f;
+        const float g = mats.gs_w[mi] ? __ldg(mats.gs_w[mi]) : 1.0f;
+        uint16_t* y = mats.y[mi];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int n = nb + k;
@@ -605,6 +624,24 @@ struct TcPlan {
   uint32_t sslot = 0;  // bytes of linear scales per slot
 };
 
+// The weight ring for blocks of at most R rows: slot sizes, and up to ~200 KB in
+// flight (about the whole ring: measured +1.3 % over 128 KB on the fused decode
+// stack, whose launches start with the ring filling while x is read), at least
+// kMeta slots if it can (for the slot relay) and at least two.  False if two
+// slots do not fit.
+template <int MODE>
+bool size_ring(TcPlan& p, int R) {
+  using G = Geo<MODE>;
+  p.R = R;
+  p.wslot = (uint32_t)G::kCh * (uint32_t)((R + 7) / 8) * 1024u;
+  p.sslot = ((uint32_t)R * G::kSB + 127u) / 128u * 128u;
+  const uint32_t slot = p.wslot + p.sslot;
+  if (Lay<MODE>::kRing / slot < 2u) return false;
+  p.nslots = (int)std::min<uint32_t>(kMaxSlots, Lay<MODE>::kRing / slot);
+  p.nslots = std::max<int>(std::min<int>(p.nslots, kMeta), std::min<int>(p.nslots, kInflightBytes / slot));
+  return true;
+}
+
 // Choose the row blocks and the K split (1, 2 or 4 CTAs per cluster: clusters
 // of 3, 5 or more measured slower to schedule).  A CTA's time is about the
 // larger of its MMA issue time (stages x about 0.2 us per 4 MMAs of K = 64,
@@ -650,51 +687,78 @@ TcPlan plan_qmv_tc(const DevInfo& d, int64_t N, int64_t K) {
     }
   }
   if (best.split == 0) return best;
-  // up to ~200 KB in flight (about the whole ring): measured +1.3 % over 128 KB on the
-  // fused decode stack, whose launches start with the ring filling while x is read
-  const uint32_t slot = best.wslot + best.sslot;
-  best.nslots = (int)std::min<uint32_t>(kMaxSlots, Lay<MODE>::kRing / slot);
-  best.nslots = std::max<int>(std::min<int>(best.nslots, kMeta), std::min<int>(best.nslots, kInflightBytes / slot));
+  size_ring<MODE>(best, best.R);
   return best;
 }
 
+// The plan of a group: the single-matrix plan of all its rows stacked (split,
+// number of row blocks); for more than one matrix, the smallest block height R
+// that deals every matrix whole blocks within that number of blocks.
+template <int MODE>
+TcPlan plan_group_tc(const DevInfo& d, int count, const int64_t* N, int64_t K, int* nb) {
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) total += N[i];
+  TcPlan p = plan_qmv_tc<MODE>(d, total, K);
+  if (p.split == 0) return p;
+  if (count == 1) {
+    nb[0] = p.nblk;
+    return p;
+  }
+  for (int R = (int)((total + p.nblk - 1) / p.nblk); R <= kRows; ++R) {
+    int64_t blocks = 0;
+    for (int i = 0; i < count; ++i) blocks += (N[i] + R - 1) / R;
+    if (blocks <= p.nblk) {
+      if (!size_ring<MODE>(p, R)) break;
+      for (int i = 0; i < count; ++i) nb[i] = (int)((N[i] + R - 1) / R);
+      return p;
+    }
+  }
+  p.split = 0;
+  return p;
+}
+
 template <int MODE, bool QX>
-cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const float* gs_x, const uint32_t* w,
-                           const uint8_t* scales, const float* gs_w, int64_t N, int64_t K, uint16_t* y, int inject,
-                           cudaStream_t s) {
+cudaError_t launch_group_tc(const DevInfo& d, const uint16_t* x, const float* gs_x, int count,
+                            const uint32_t* const* w, const uint8_t* const* scales, const float* const* gs_w,
+                            const int64_t* N, int64_t K, uint16_t* const* y, int inject, cudaStream_t s) {
+  if (count < 1 || count > kMaxGroup) return cudaErrorInvalidValue;
   auto fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
-  const TcPlan p = plan_qmv_tc<MODE>(d, N, K);
+  int nb[kMaxGroup] = {0, 0, 0, 0};
+  const TcPlan p = plan_group_tc<MODE>(d, count, N, K, nb);
   if (p.split == 0) return cudaErrorInvalidValue;
   const int group = MODE == 2 ? 16 : 32;
   cuuint32_t estr[2] = {1, 1};
-  // W codes: [N, K/2] bytes, boxes of R rows x 128 bytes, 128-byte swizzle
-  CUtensorMap tmW;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
+  QmvGroup g;
+  memset(&g, 0, sizeof(g));
+  g.count = count;
+  for (int i = 0; i < count; ++i) {
+    // W codes: [N, K/2] bytes, boxes of R rows x 128 bytes, 128-byte swizzle
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N[i]};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
     cuuint32_t box[2] = {128, (cuuint32_t)p.R};
-    if (fn(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(w), dims, strides, box, estr,
+    if (fn(&g.tmW[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(w[i]), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  }
-  // W scales: [N, K/group] bytes (a multiple of 16 per row), boxes of R rows x kSB bytes
-  CUtensorMap tmS;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)(K / group), (cuuint64_t)N};
-    cuuint64_t strides[1] = {(cuuint64_t)(K / group)};
-    cuuint32_t box[2] = {(cuuint32_t)Geo<MODE>::kSB, (cuuint32_t)p.R};
-    if (fn(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(scales), dims, strides, box, estr,
+    // W scales: [N, K/group] bytes (a multiple of 16 per row), boxes of R rows x kSB bytes
+    cuuint64_t sdims[2] = {(cuuint64_t)(K / group), (cuuint64_t)N[i]};
+    cuuint64_t sstrides[1] = {(cuuint64_t)(K / group)};
+    cuuint32_t sbox[2] = {(cuuint32_t)Geo<MODE>::kSB, (cuuint32_t)p.R};
+    if (fn(&g.tmS[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(scales[i]), sdims, sstrides, sbox, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    g.gs_w[i] = gs_w ? gs_w[i] : nullptr;
+    g.y[i] = y[i];
+    g.N[i] = (int)N[i];
+    g.blk0[i + 1] = g.blk0[i] + nb[i];
   }
   cudaError_t e =
       cudaFuncSetAttribute(qmv_tc_kernel<MODE, QX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.nblk * p.split));
+  cfg.gridDim = dim3((unsigned)(g.blk0[count] * p.split));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
@@ -707,8 +771,8 @@ cudaError_t launch_mode_tc(const DevInfo& d, const uint16_t* x, const float* gs_
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel<MODE, QX>, tmW, tmS, x, gs_x, gs_w, (int)N, (int)K, p.R, p.split,
-                            p.nslots, p.wslot, p.sslot, y, d.err, inject);
+  return cudaLaunchKernelEx(&cfg, qmv_tc_kernel<MODE, QX>, g, x, gs_x, (int)K, p.R, p.split, p.nslots, p.wslot,
+                            p.sslot, d.err, inject);
 }
 
 }  // namespace
@@ -729,9 +793,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Whether the tensor-core GEMV handles this NVFP4 (mode 2) or MXFP4 (mode 1)
 // problem (else the mma.sync kernel does).
 bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K) {
-  if (kSmemBytes > d.smem_optin || N > (int64_t)kRows * d.sm_count) return false;
-  if (mode == 2) return plan_qmv_tc<2>(d, N, K).split > 0;
-  if (mode == 1) return plan_qmv_tc<1>(d, N, K).split > 0;
+  return qmv_tc_group_supported(d, mode, 1, &N, K);
+}
+
+bool qmv_tc_group_supported(const DevInfo& d, int mode, int count, const int64_t* N, int64_t K) {
+  if (count < 1 || count > kMaxGroup || kSmemBytes > d.smem_optin) return false;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) total += N[i];
+  if (total > (int64_t)kRows * d.sm_count) return false;
+  int nb[kMaxGroup];
+  if (mode == 2) return plan_group_tc<2>(d, count, N, K, nb).split > 0;
+  if (mode == 1) return plan_group_tc<1>(d, count, N, K, nb).split > 0;
   return false;
 }
 
@@ -745,14 +817,22 @@ bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nb
   return true;
 }
 
+cudaError_t launch_qmv_tc_group(const DevInfo& d, int mode, const uint16_t* x, const float* gs_x, int qx, int count,
+                                const uint32_t* const* w, const uint8_t* const* scales, const float* const* gs_w,
+                                const int64_t* N, int64_t K, uint16_t* const* y, int inject_timeout, cudaStream_t s) {
+  if (mode == 2 && qx)
+    return launch_group_tc<2, true>(d, x, gs_x, count, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 1 && qx)
+    return launch_group_tc<1, true>(d, x, gs_x, count, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 2) return launch_group_tc<2, false>(d, x, nullptr, count, w, scales, gs_w, N, K, y, inject_timeout, s);
+  if (mode == 1) return launch_group_tc<1, false>(d, x, nullptr, count, w, scales, gs_w, N, K, y, inject_timeout, s);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const float* gs_x, int qx,
                           const uint32_t* w, const uint8_t* scales, const float* gs_w, int64_t N, int64_t K,
                           uint16_t* y, int inject_timeout, cudaStream_t s) {
-  if (mode == 2 && qx) return launch_mode_tc<2, true>(d, x, gs_x, w, scales, gs_w, N, K, y, inject_timeout, s);
-  if (mode == 1 && qx) return launch_mode_tc<1, true>(d, x, gs_x, w, scales, gs_w, N, K, y, inject_timeout, s);
-  if (mode == 2) return launch_mode_tc<2, false>(d, x, nullptr, w, scales, gs_w, N, K, y, inject_timeout, s);
-  if (mode == 1) return launch_mode_tc<1, false>(d, x, nullptr, w, scales, gs_w, N, K, y, inject_timeout, s);
-  return cudaErrorInvalidValue;
+  return launch_qmv_tc_group(d, mode, x, gs_x, qx, 1, &w, &scales, &gs_w, &N, K, &y, inject_timeout, s);
 }
 
 }  // namespace fp4

@@ -114,6 +114,18 @@ def test_validation_rejects_before_launch(B):
                              None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.qqmm_quantize_x(p, None, p, p, None, 128, 256, 256, B.MODE_NVFP4, ctypes.c_void_p(256 + 64), wsb, None,
                              p, None) == B.FP4_ERR_ALIGNMENT  # workspace not 128-byte aligned
+    P1 = ctypes.c_void_p * 1
+    n1 = (ctypes.c_int64 * 1)(64)
+    assert L.qmv_grouped(p, 0, P1(256), P1(256), None, None, n1, 256, B.MODE_NVFP4, 4, 16, P1(256),
+                         None) == B.FP4_ERR_INVALID_ARG  # count 0
+    assert L.qmv_grouped(p, 5, P1(256), P1(256), None, None, n1, 256, B.MODE_NVFP4, 4, 16, P1(256),
+                         None) == B.FP4_ERR_INVALID_ARG  # count above 4
+    assert L.qmv_grouped(p, 1, P1(256), P1(256), None, None, n1, 48, B.MODE_NVFP4, 4, 16, P1(256),
+                         None) == B.FP4_ERR_INVALID_ARG  # K % 32
+    assert L.qmv_grouped(p, 1, P1(258), P1(256), None, None, n1, 256, B.MODE_NVFP4, 4, 16, P1(256),
+                         None) == B.FP4_ERR_ALIGNMENT  # w not 16-byte aligned
+    assert L.qmv_grouped(p, 1, P1(256), P1(256), None, None, n1, 256, B.MODE_AFFINE, 4, 64, P1(256),
+                         None) == B.FP4_ERR_INVALID_ARG  # affine without biases
     assert L.gather_rows(p, 4, p, 8, 12, p, None) == B.FP4_ERR_INVALID_ARG  # K % 8
     assert L.gather_rows(p, 0, p, 8, 16, p, None) == B.FP4_ERR_INVALID_ARG  # no x rows
     assert L.gather_rows(p, 4, p, 0, 16, p, None) == B.FP4_ERR_INVALID_ARG  # R = 0
