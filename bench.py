@@ -188,7 +188,8 @@ layer_groups = synth.layer_groups
 class DecodeStack:
     """64-layer weight stack in one format, weights resident on the device."""
 
-    def __init__(self, B, mode: int, layers: int, device, layout: str = "split", qx: bool = False):
+    def __init__(self, B, mode: int, layers: int, device, layout: str = "split", qx: bool = False,
+                 prefetch: bool = False):
         """layout "split": one matrix per projection, 7 GEMVs a layer.  "fused":
         the projections that multiply the same x stored as one matrix, as serving
         engines store them -- q|k|v as [3*5120, 5120] and gate|up as [2*17408,
@@ -196,7 +197,9 @@ class DecodeStack:
         weights (each output slice is that projection's y).  "fused_qkv": only
         q|k|v fused, 5 GEMVs a layer.  qx: the quantized-activation route (qqmv:
         x quantized and dequantized inside each GEMV; NVFP4 with a static
-        activation global scale, as a calibrated checkpoint carries one)."""
+        activation global scale, as a calibrated checkpoint carries one).  prefetch:
+        every launch goes through qmv_grouped naming the next launch's weights, which
+        it warms in L2 once its own weight loads are issued."""
         self.B, self.mode, self.layers, self.qx = B, mode, layers, qx
         self.mats = []
         self.bytes = 0
@@ -216,6 +219,9 @@ class DecodeStack:
         self.gs_x = {K: (B.fp4_amax_global_scale(v) if qx and mode == B.MODE_NVFP4 else None)
                      for K, v in self.x.items()}
         self.y = [torch.empty((m["N"],), dtype=torch.bfloat16, device=device) for m in self.mats]
+        self.prefetch = prefetch and not qx
+        self.mgroups = [B.matrix_group([(self.mats[i]["q"], self.mats[i]["s"], self.mats[i]["b"], self.mats[i]["gs"])
+                                        for i in g]) for g in self.launch_groups]
 
     def _make(self, layer, N, K, grp, device):
         B = self.B
@@ -235,6 +241,12 @@ class DecodeStack:
 
     def step(self, stream=None):
         B = self.B
+        if self.prefetch:
+            n = len(self.launch_groups)
+            for j, g in enumerate(self.launch_groups):
+                B.qmv_grouped(self.x[self.mats[g[0]]["K"]], self.mgroups[j], mode=self.mode,
+                              ys=[self.y[i] for i in g], stream=stream, prefetch_next=self.mgroups[(j + 1) % n])
+            return
         if self.grouped:
             for g in self.launch_groups:
                 ms = [self.mats[i] for i in g]
@@ -267,7 +279,8 @@ WORKLOAD = ("decode qmv over a 64-layer hidden-5120 stack (q,k,v,o 5120x5120; ga
             "down 5120x17408), NVFP4 g16 weights, bf16 x, one token")
 LAYOUT = ("q|k|v stored as one [15360, 5120] matrix and gate|up as one [34816, 5120] matrix (they "
           "multiply the same x): 4 GEMVs a layer, the same weights and outputs; one matrix per "
-          "projection (7 GEMVs a layer) is components.decode_qmv.nvfp4")
+          "projection (7 GEMVs a layer) is components.decode_qmv.nvfp4; every launch names the next "
+          "launch's weights (qmv_grouped's L2 prefetch hint)")
 
 
 def time_graph(graph, steps, warmup, stream):
@@ -562,7 +575,8 @@ def run_case(args):
         base = c.replace("_fused", "").replace("qqmv_", "qmv_")
         mode = {"qmv_nvfp4": B.MODE_NVFP4, "qmv_mxfp4": B.MODE_MXFP4, "qmv_affine": B.MODE_AFFINE}[base]
         # 4 layers: 0.84 GB of weights, well above L2
-        stack = DecodeStack(B, mode, 4, dev, layout=layout, qx=c.startswith("qqmv_"))
+        qx = c.startswith("qqmv_")
+        stack = DecodeStack(B, mode, 4, dev, layout=layout, qx=qx, prefetch=not qx and mode != B.MODE_AFFINE)
         for _ in range(3):
             stack.step()
     elif c.startswith("qqmm_m"):
@@ -633,20 +647,23 @@ def run_ours(args):
 
     # the headline: NVFP4 weights in the fused layout (4 GEMVs a layer); the
     # per-projection layout and the other formats are components
-    modes = [("nvfp4_fused", B.MODE_NVFP4, "fused", False)] + (
-        [] if args.quick else [("nvfp4", B.MODE_NVFP4, "split", False),
-                               ("nvfp4_grouped", B.MODE_NVFP4, "split_grouped", False),
-                               ("mxfp4_fused", B.MODE_MXFP4, "fused", False),
-                               ("mxfp4", B.MODE_MXFP4, "split", False),
-                               ("mxfp4_grouped", B.MODE_MXFP4, "split_grouped", False),
-                               ("affine_g64", B.MODE_AFFINE, "split", False),
-                               ("affine_g64_fused", B.MODE_AFFINE, "fused", False),
-                               ("nvfp4_fused_quantized_x", B.MODE_NVFP4, "fused", True),
-                               ("mxfp4_fused_quantized_x", B.MODE_MXFP4, "fused", True)])
+    # (name, format, layout, quantized x, next-launch prefetch hints); the FP4 layouts run as
+    # a serving loop runs them: every launch names the next launch's weights
+    modes = [("nvfp4_fused", B.MODE_NVFP4, "fused", False, True)] + (
+        [] if args.quick else [("nvfp4_fused_no_prefetch", B.MODE_NVFP4, "fused", False, False),
+                               ("nvfp4", B.MODE_NVFP4, "split", False, True),
+                               ("nvfp4_grouped", B.MODE_NVFP4, "split_grouped", False, True),
+                               ("mxfp4_fused", B.MODE_MXFP4, "fused", False, True),
+                               ("mxfp4", B.MODE_MXFP4, "split", False, True),
+                               ("mxfp4_grouped", B.MODE_MXFP4, "split_grouped", False, True),
+                               ("affine_g64", B.MODE_AFFINE, "split", False, False),
+                               ("affine_g64_fused", B.MODE_AFFINE, "fused", False, False),
+                               ("nvfp4_fused_quantized_x", B.MODE_NVFP4, "fused", True, False),
+                               ("mxfp4_fused_quantized_x", B.MODE_MXFP4, "fused", True, False)])
     results = {}
     headline = None
-    for name, mode, layout, qx in modes:
-        stack = DecodeStack(B, mode, args.layers, device, layout=layout, qx=qx)
+    for name, mode, layout, qx, pf in modes:
+        stack = DecodeStack(B, mode, args.layers, device, layout=layout, qx=qx, prefetch=pf)
         graph = capture(stack.step, stream)
         if name == "nvfp4_fused":
             with ClockSampler(local) as clk, nvtx(f"decode {name}"):
@@ -662,8 +679,9 @@ def run_ours(args):
                          "frac_of_hbm": stack.bytes / ms / 1e6 / peaks["hbm_gbs"],
                          "launches_per_step": stack.launches, "layout": layout,
                          "entry_point": ("qqmv (x quantized inside the GEMV)" if qx else
-                                         "qmv_grouped (q,k,v and gate,up one launch each) + qmv"
-                                         if layout == "split_grouped" else "qmv")}
+                                         "qmv_grouped, each launch naming the next one's weights (L2 prefetch hint)"
+                                         if pf else "qmv"),
+                         "prefetch_next": pf}
         if name != "nvfp4_fused":
             del stack, graph
             torch.cuda.empty_cache()

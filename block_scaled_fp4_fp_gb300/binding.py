@@ -45,7 +45,7 @@ SIGNATURES = {
     "qqmv": (_INT, [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _INT, _VP, _VP]),
     "qqmm": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _VP, _VP]),
     "gather_rows": (_INT, [_VP, _I64, _VP, _I64, _I64, _VP, _VP]),
-    "qmv_grouped": (_INT, [_VP, _INT, _VP, _VP, _VP, _VP, _VP, _I64, _INT, _INT, _INT, _VP, _VP]),
+    "qmv_grouped": (_INT, [_VP, _VP, _INT, _INT, _INT, _VP, _VP, _VP]),
     "gather_qmm": (_INT, [_VP, _VP, _VP, _I64, _VP, _VP, _VP, _I64, _I64, _I64, _INT, _INT, _INT, _INT,
                           _VP, _VP]),
     "qqmm_batched": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
@@ -264,24 +264,41 @@ def gather_qmm(x: torch.Tensor, lhs_idx: torch.Tensor, rhs_idx: torch.Tensor, w:
     return out
 
 
-def qmv_grouped(x: torch.Tensor, mats, mode: int = MODE_NVFP4, group_size: int = None, ys=None, stream=None):
+class MatrixGroup(c.Structure):
+    """fp4_matrix_group: up to 4 matrices of one K for qmv_grouped."""
+    _fields_ = [("count", c.c_int), ("w", c.c_void_p * 4), ("scales", c.c_void_p * 4), ("biases", c.c_void_p * 4),
+                ("global_scale_w", c.c_void_p * 4), ("N", c.c_int64 * 4), ("K", c.c_int64)]
+
+
+def matrix_group(mats) -> MatrixGroup:
+    """mats: a list of (w, scales, biases, global_scale_w) tuples (None where absent)."""
+    g = MatrixGroup()
+    g.count = len(mats)
+    for i, (w, s, b, gs) in enumerate(mats):
+        g.w[i] = w.data_ptr()
+        g.scales[i] = s.data_ptr()
+        g.biases[i] = b.data_ptr() if b is not None else None
+        g.global_scale_w[i] = gs.data_ptr() if gs is not None else None
+        g.N[i] = w.shape[0]
+    g.K = mats[0][0].shape[1] * 8
+    return g
+
+
+def qmv_grouped(x: torch.Tensor, mats, mode: int = MODE_NVFP4, group_size: int = None, ys=None, stream=None,
+                prefetch_next=None):
     """One x against up to 4 matrices of the same K in one launch.  mats: a list of
-    (w, scales, biases, global_scale_w) tuples (biases / global scale may be None);
-    returns the list of y vectors."""
+    (w, scales, biases, global_scale_w) tuples; prefetch_next: the same for the
+    GEMV launched next (an L2 warm-up hint) or None.  Returns the y vectors."""
     group_size = group_size or GROUP[mode]
-    count = len(mats)
-    K = mats[0][0].shape[1] * 8
-    Ns = [m[0].shape[0] for m in mats]
+    g = mats if isinstance(mats, MatrixGroup) else matrix_group(mats)
     if ys is None:
-        ys = [torch.empty((n,), dtype=torch.bfloat16, device=mats[0][0].device) for n in Ns]
-    P = c.c_void_p * count
-    w = P(*[m[0].data_ptr() for m in mats])
-    sc = P(*[m[1].data_ptr() for m in mats])
-    bi = P(*[m[2].data_ptr() for m in mats]) if mats[0][2] is not None else None
-    gs = P(*[(m[3].data_ptr() if m[3] is not None else None) for m in mats]) if any(m[3] is not None for m in mats) else None
-    nn = (c.c_int64 * count)(*Ns)
-    yy = P(*[y.data_ptr() for y in ys])
-    _check(lib().qmv_grouped(_p(x), count, w, sc, bi, gs, nn, K, mode, 4, group_size, yy, _s(stream)), "qmv_grouped")
+        ys = [torch.empty((int(g.N[i]),), dtype=torch.bfloat16, device=x.device) for i in range(g.count)]
+    yy = (c.c_void_p * g.count)(*[y.data_ptr() for y in ys])
+    nx = None
+    if prefetch_next is not None:
+        nx = prefetch_next if isinstance(prefetch_next, MatrixGroup) else matrix_group(prefetch_next)
+    _check(lib().qmv_grouped(_p(x), c.byref(g), mode, 4, group_size, yy, c.byref(nx) if nx is not None else None,
+                             _s(stream)), "qmv_grouped")
     return ys
 
 

@@ -221,51 +221,83 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
                               g_inject_timeout.load(), stream));
 }
 
-fp4_status qmv_grouped(const fp4_bf16* x, int count, const uint32_t* const* w, const void* const* scales,
-                       const fp4_bf16* const* biases, const float* const* global_scale_w, const int64_t* N, int64_t K,
-                       fp4_mode mode, int bits, int group_size, fp4_bf16* const* y, cudaStream_t stream) {
-  if (count < 1 || count > 4 || !w || !scales || !N || !y) return FP4_ERR_INVALID_ARG;
-  // every matrix must be a valid qmv on its own (same checks, same x)
-  for (int i = 0; i < count; ++i) {
-    if (!w[i] || !scales[i] || !y[i]) return FP4_ERR_INVALID_ARG;
-    const fp4_bf16* b = biases ? biases[i] : nullptr;
-    const float* g = global_scale_w ? global_scale_w[i] : nullptr;
-    fp4_status st = check_format(mode, bits, group_size);
-    if (st != FP4_OK) return st;
-    if (!x || N[i] <= 0 || K <= 0 || K % 32 != 0 || K % group_size != 0 || N[i] > INT32_MAX / 2)
-      return FP4_ERR_INVALID_ARG;
-    if (K > 65536) return FP4_ERR_UNSUPPORTED;
+namespace {
+// one group of qmv_grouped: each matrix a valid qmv on its own (same checks, same x)
+fp4_status check_group(const fp4_bf16* x, const fp4_matrix_group* g, fp4_mode mode, int bits, int group_size) {
+  if (!g || g->count < 1 || g->count > 4) return FP4_ERR_INVALID_ARG;
+  fp4_status st = check_format(mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  const int64_t K = g->K;
+  if (!x || K <= 0 || K % 32 != 0 || K % group_size != 0) return FP4_ERR_INVALID_ARG;
+  if (K > 65536) return FP4_ERR_UNSUPPORTED;
+  for (int i = 0; i < g->count; ++i) {
+    if (!g->w[i] || !g->scales[i] || g->N[i] <= 0 || g->N[i] > INT32_MAX / 2) return FP4_ERR_INVALID_ARG;
+    const fp4_bf16* b = g->biases[i];
+    const float* gs = g->global_scale_w[i];
     if (mode == FP4_MODE_AFFINE) {
-      if (!b || g) return FP4_ERR_INVALID_ARG;
-      if (!aligned(scales[i], 2) || !aligned(b, 2)) return FP4_ERR_ALIGNMENT;
+      if (!b || gs) return FP4_ERR_INVALID_ARG;
+      if (!aligned(g->scales[i], 2) || !aligned(b, 2)) return FP4_ERR_ALIGNMENT;
     } else {
       if (b) return FP4_ERR_INVALID_ARG;
-      if (g && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
-      if (g && !aligned(g, 4)) return FP4_ERR_ALIGNMENT;
-      if (mode == FP4_MODE_NVFP4 && !aligned(scales[i], 2)) return FP4_ERR_ALIGNMENT;
+      if (gs && mode != FP4_MODE_NVFP4) return FP4_ERR_INVALID_ARG;
+      if (gs && !aligned(gs, 4)) return FP4_ERR_ALIGNMENT;
+      if (mode == FP4_MODE_NVFP4 && !aligned(g->scales[i], 2)) return FP4_ERR_ALIGNMENT;
     }
-    if (!aligned(x, 16) || !aligned(w[i], 16) || !aligned(y[i], 2)) return FP4_ERR_ALIGNMENT;
+    if (!aligned(x, 16) || !aligned(g->w[i], 16)) return FP4_ERR_ALIGNMENT;
+  }
+  return FP4_OK;
+}
+
+// whether the tensor-core GEMV takes the whole group in one launch
+bool group_on_tc(const DevInfo& d, const fp4_matrix_group* g, fp4_mode mode) {
+  if (mode != FP4_MODE_NVFP4 && mode != FP4_MODE_MXFP4) return false;
+  for (int i = 0; i < g->count; ++i)
+    if (!aligned(g->scales[i], 16)) return false;
+  return qmv_tc_group_supported(d, mode, g->count, g->N, g->K);
+}
+}  // namespace
+
+fp4_status qmv_grouped(const fp4_bf16* x, const fp4_matrix_group* mats, fp4_mode mode, int bits, int group_size,
+                       fp4_bf16* const* y, const fp4_matrix_group* prefetch_next, cudaStream_t stream) {
+  fp4_status st = check_group(x, mats, mode, bits, group_size);
+  if (st != FP4_OK) return st;
+  if (!y) return FP4_ERR_INVALID_ARG;
+  for (int i = 0; i < mats->count; ++i) {
+    if (!y[i]) return FP4_ERR_INVALID_ARG;
+    if (!aligned(y[i], 2)) return FP4_ERR_ALIGNMENT;
+  }
+  if (prefetch_next) {  // the hint is checked as strictly as the group itself
+    st = check_group(x, prefetch_next, mode, bits, group_size);
+    if (st != FP4_OK) return st;
   }
   const DevInfo* d = nullptr;
-  fp4_status st = current(&d);
+  st = current(&d);
   if (st != FP4_OK) return st;
-  // one launch on the tensor-core GEMV when it takes the whole group (FP4 formats,
-  // 16-byte aligned scale rows, a plan for the stacked rows); otherwise one qmv each
-  bool one = (mode == FP4_MODE_NVFP4 || mode == FP4_MODE_MXFP4) && qmv_tc_group_supported(*d, mode, count, N, K);
-  for (int i = 0; i < count && one; ++i) one = aligned(scales[i], 16);
-  if (one) {
+  if (group_on_tc(*d, mats, mode)) {
     const uint8_t* sc[4];
     uint16_t* yy[4];
-    for (int i = 0; i < count; ++i) {
-      sc[i] = static_cast<const uint8_t*>(scales[i]);
+    for (int i = 0; i < mats->count; ++i) {
+      sc[i] = static_cast<const uint8_t*>(mats->scales[i]);
       yy[i] = reinterpret_cast<uint16_t*>(y[i]);
     }
-    return from_cuda(launch_qmv_tc_group(*d, mode, x, nullptr, 0, count, w, sc, global_scale_w, N, K, yy,
-                                         g_inject_timeout.load(), stream));
+    GemvGroupDesc nd;
+    const bool hint = prefetch_next && group_on_tc(*d, prefetch_next, mode);
+    if (hint) {
+      nd.count = prefetch_next->count;
+      nd.K = prefetch_next->K;
+      for (int i = 0; i < nd.count; ++i) {
+        nd.w[i] = prefetch_next->w[i];
+        nd.scales[i] = static_cast<const uint8_t*>(prefetch_next->scales[i]);
+        nd.N[i] = prefetch_next->N[i];
+      }
+    }
+    return from_cuda(launch_qmv_tc_group(*d, mode, x, nullptr, 0, mats->count, mats->w, sc, mats->global_scale_w,
+                                         mats->N, mats->K, yy, hint ? &nd : nullptr, g_inject_timeout.load(),
+                                         stream));
   }
-  for (int i = 0; i < count; ++i) {
-    const cudaError_t e = launch_qmv(*d, x, nullptr, 0, w[i], scales[i], biases ? biases[i] : nullptr,
-                                     global_scale_w ? global_scale_w[i] : nullptr, N[i], K, mode, group_size, y[i],
+  for (int i = 0; i < mats->count; ++i) {
+    const cudaError_t e = launch_qmv(*d, x, nullptr, 0, mats->w[i], mats->scales[i], mats->biases[i],
+                                     mats->global_scale_w[i], mats->N[i], mats->K, mode, group_size, y[i],
                                      g_inject_timeout.load(), stream);
     if (e != cudaSuccess) return from_cuda(e);
   }

@@ -47,9 +47,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // driver's tensor-map encoder (
 bool qmv_tc_geometry(const DevInfo& d, int64_t N, int64_t K, int* split, int* nblk, int* R, int* nslots);
 bool qmv_tc_supported(const DevInfo& d, int mode, int64_t N, int64_t K);
 bool qmv_tc_group_supported(const DevInfo& d, int mode, int count, const int64_t* N, int64_t K);
+// the weights of a GEMV launch (a group of up to 4 matrices of one K)
+struct GemvGroupDesc {
+  int count = 0;
+  const uint32_t* w[4] = {};
+  const uint8_t* scales[4] = {};
+  int64_t N[4] = {};
+  int64_t K = 0;
+};
 cudaError_t launch_qmv_tc_group(const DevInfo& d, int mode, const uint16_t* x, const float* gs_x, int qx, int count,
                                 const uint32_t* const* w, const uint8_t* const* scales, const float* const* gs_w,
-                                const int64_t* N, int64_t K, uint16_t* const* y, int inject_timeout, cudaStream_t s);
+                                const int64_t* N, int64_t K, uint16_t* const* y, const GemvGroupDesc* next,
+                                int inject_timeout, cudaStream_t s);
 cudaError_t launch_qmv_tc(const DevInfo& d, int mode, const uint16_t* x, const float* gs_x, int qx,
                           const uint32_t* w, const uint8_t* scales, const float* gs_w, int64_t N, int64_t K,
                           uint16_t* y, int inject_timeout, cudaStream_t s);

@@ -174,19 +174,34 @@ fp4_status qmv(const fp4_bf16* x, const uint32_t* w, const void* scales, const f
                const float* global_scale_w, int64_t N, int64_t K, fp4_mode mode, int bits,
                int group_size, fp4_bf16* y, cudaStream_t stream);
 
-/* qmv_grouped: the decode GEMV of one x against up to 4 matrices of the same K
- * in one launch -- the projections that multiply the same activation (q, k and
- * v; gate and up) stored as separate matrices [P2 Baseline: the decode step is
- * the qmv weight stream; grouping them pays the per-launch fixed cost once].
- *   y_i = x . deq(W_i)^T  for i < count (each y_i as qmv computes it)
- *   w, scales, biases, global_scale_w, N, y: HOST arrays of `count` entries, each
- *   entry as qmv takes it (biases / global_scale_w may be NULL arrays: none)
+/* The weights of one GEMV launch: up to 4 matrices of the same K, each given as
+ * qmv takes it (biases: affine only; global_scale_w: NVFP4 only, may be NULL). */
+typedef struct fp4_matrix_group {
+  int count; /* 1 .. 4 */
+  const uint32_t* w[4];
+  const void* scales[4];
+  const fp4_bf16* biases[4];
+  const float* global_scale_w[4];
+  int64_t N[4];
+  int64_t K;
+} fp4_matrix_group;
+
+/* qmv_grouped: the decode GEMV of one x against the matrices of `mats` in one
+ * launch -- the projections that multiply the same activation (q, k and v;
+ * gate and up) stored as separate matrices [P2 Baseline: the decode step is the
+ * qmv weight stream; grouping them pays the per-launch fixed cost once].
+ *   y[i] = x . deq(W_i)^T  for i < mats->count (each y[i] as qmv computes it);
+ *   y: a HOST array of mats->count device pointers.
+ * prefetch_next (NULL: none): the weights of the GEMV the caller launches next
+ * on this stream, same mode.  A hint: once this launch has issued its own
+ * weight loads, it warms L2 with the first stages that launch will read, so
+ * that its start does not wait on DRAM.  It is validated like `mats` (its
+ * pointers must be device memory); nothing is written through it.
  * NVFP4 and MXFP4 run as one tensor-core launch when the stacked rows have a
  * plan and every scale row is 16-byte aligned; affine or other cases run as
- * `count` qmv launches.  Requires 1 <= count <= 4; otherwise qmv's rules. */
-fp4_status qmv_grouped(const fp4_bf16* x, int count, const uint32_t* const* w, const void* const* scales,
-                       const fp4_bf16* const* biases, const float* const* global_scale_w, const int64_t* N, int64_t K,
-                       fp4_mode mode, int bits, int group_size, fp4_bf16* const* y, cudaStream_t stream);
+ * mats->count qmv launches (and ignore the hint).  Otherwise qmv's rules. */
+fp4_status qmv_grouped(const fp4_bf16* x, const fp4_matrix_group* mats, fp4_mode mode, int bits, int group_size,
+                       fp4_bf16* const* y, const fp4_matrix_group* prefetch_next, cudaStream_t stream);
 
 /* qqmv: the one-row route of the quantized-activation matmul [P3 qqmm.cpp,
  * QQMatmul::eval_gpu: with quantized W and a single row of x, x goes through

@@ -114,17 +114,22 @@ def test_validation_rejects_before_launch(B):
                              None) == B.FP4_ERR_INVALID_ARG  # K % 256
     assert L.qqmm_quantize_x(p, None, p, p, None, 128, 256, 256, B.MODE_NVFP4, ctypes.c_void_p(256 + 64), wsb, None,
                              p, None) == B.FP4_ERR_ALIGNMENT  # workspace not 128-byte aligned
-    P1 = ctypes.c_void_p * 1
-    n1 = (ctypes.c_int64 * 1)(64)
-    assert L.qmv_grouped(p, 0, P1(256), P1(256), None, None, n1, 256, B.MODE_NVFP4, 4, 16, P1(256),
-                         None) == B.FP4_ERR_INVALID_ARG  # count 0
-    assert L.qmv_grouped(p, 5, P1(256), P1(256), None, None, n1, 256, B.MODE_NVFP4, 4, 16, P1(256),
-                         None) == B.FP4_ERR_INVALID_ARG  # count above 4
-    assert L.qmv_grouped(p, 1, P1(256), P1(256), None, None, n1, 48, B.MODE_NVFP4, 4, 16, P1(256),
-                         None) == B.FP4_ERR_INVALID_ARG  # K % 32
-    assert L.qmv_grouped(p, 1, P1(258), P1(256), None, None, n1, 256, B.MODE_NVFP4, 4, 16, P1(256),
-                         None) == B.FP4_ERR_ALIGNMENT  # w not 16-byte aligned
-    assert L.qmv_grouped(p, 1, P1(256), P1(256), None, None, n1, 256, B.MODE_AFFINE, 4, 64, P1(256),
+    def grp(count=1, w=256, K=256, N=64):
+        g = B.MatrixGroup()
+        g.count = count
+        for i in range(4):
+            g.w[i], g.scales[i], g.N[i] = w, 256, N
+        g.K = K
+        return g
+    Y = (ctypes.c_void_p * 4)(256, 256, 256, 256)
+    for g, want in ((grp(count=0), B.FP4_ERR_INVALID_ARG), (grp(count=5), B.FP4_ERR_INVALID_ARG),
+                    (grp(K=48), B.FP4_ERR_INVALID_ARG), (grp(N=0), B.FP4_ERR_INVALID_ARG),
+                    (grp(w=258), B.FP4_ERR_ALIGNMENT)):
+        assert L.qmv_grouped(p, ctypes.byref(g), B.MODE_NVFP4, 4, 16, Y, None, None) == want
+    # the prefetch hint is validated as strictly as the group
+    assert L.qmv_grouped(p, ctypes.byref(grp()), B.MODE_NVFP4, 4, 16, Y, ctypes.byref(grp(w=258)),
+                         None) == B.FP4_ERR_ALIGNMENT
+    assert L.qmv_grouped(p, ctypes.byref(grp()), B.MODE_AFFINE, 4, 64, Y, None,
                          None) == B.FP4_ERR_INVALID_ARG  # affine without biases
     assert L.gather_rows(p, 4, p, 8, 12, p, None) == B.FP4_ERR_INVALID_ARG  # K % 8
     assert L.gather_rows(p, 0, p, 8, 16, p, None) == B.FP4_ERR_INVALID_ARG  # no x rows

@@ -67,3 +67,32 @@ def test_qmv_grouped_decode_shapes_sampled(B, mode, Ns):
 def test_qmv_grouped_split_k(B, mode):
     """A K long enough that the stacked rows take the K-split plan (clusters)."""
     run_group(B, mode, [300, 700], 34816, seed=77)
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+def test_qmv_grouped_prefetch_hint_changes_nothing(B, mode):
+    """A chain of launches each naming the next one's weights (the L2 warm-up
+    hint, wrapping around): every y is bit-identical to the same launches without
+    hints, and matches the oracle."""
+    K = 1024
+    shapes = [[300, 700], [64], [1000, 1000, 5], [2048]]
+    groups, host = [], []
+    for j, Ns in enumerate(shapes):
+        mats, hm = [], []
+        for i, N in enumerate(Ns):
+            q, s, b, gs, g = make_weights(mode, N, K, seed=100 * j + i)
+            hm.append((q, s, b, gs, g))
+            mats.append(to_dev(mode, q, s, b, gs))
+        groups.append(mats)
+        host.append(hm)
+    x = synth.bf16_normal((K,), 1.0, seed=3).cuda()
+    plain = [B.qmv_grouped(x, m, mode=mode) for m in groups]
+    hinted = [B.qmv_grouped(x, m, mode=mode, prefetch_next=groups[(j + 1) % len(groups)])
+              for j, m in enumerate(groups)]
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    for j in range(len(groups)):
+        for i, (q, s, b, gs, g) in enumerate(host[j]):
+            assert torch.equal(plain[j][i], hinted[j][i])
+            ref = oracle.qmv(synth.to_u16(x.cpu()), q, s, b, mode, g, gs)
+            assert_close_to_oracle(hinted[j][i], ref, f"hinted launch {j} matrix {i}")
