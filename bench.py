@@ -576,7 +576,7 @@ def run_case(args):
         mode = {"qmv_nvfp4": B.MODE_NVFP4, "qmv_mxfp4": B.MODE_MXFP4, "qmv_affine": B.MODE_AFFINE}[base]
         # 4 layers: 0.84 GB of weights, well above L2
         qx = c.startswith("qqmv_")
-        stack = DecodeStack(B, mode, 4, dev, layout=layout, qx=qx, prefetch=not qx and mode != B.MODE_AFFINE)
+        stack = DecodeStack(B, mode, 4, dev, layout=layout, qx=qx, prefetch=not qx)
         for _ in range(3):
             stack.step()
     elif c.startswith("qqmm_m"):
@@ -656,8 +656,9 @@ def run_ours(args):
                                ("mxfp4_fused", B.MODE_MXFP4, "fused", False, True),
                                ("mxfp4", B.MODE_MXFP4, "split", False, True),
                                ("mxfp4_grouped", B.MODE_MXFP4, "split_grouped", False, True),
-                               ("affine_g64", B.MODE_AFFINE, "split", False, False),
-                               ("affine_g64_fused", B.MODE_AFFINE, "fused", False, False),
+                               ("affine_g64", B.MODE_AFFINE, "split", False, True),
+                               ("affine_g64_grouped", B.MODE_AFFINE, "split_grouped", False, True),
+                               ("affine_g64_fused", B.MODE_AFFINE, "fused", False, True),
                                ("nvfp4_fused_quantized_x", B.MODE_NVFP4, "fused", True, False),
                                ("mxfp4_fused_quantized_x", B.MODE_MXFP4, "fused", True, False)])
     results = {}

@@ -255,6 +255,25 @@ bool group_on_tc(const DevInfo& d, const fp4_matrix_group* g, fp4_mode mode) {
     if (!aligned(g->scales[i], 16)) return false;
   return qmv_tc_group_supported(d, mode, g->count, g->N, g->K);
 }
+
+// whether the affine TMA GEMV takes the whole group in one launch
+bool group_on_affine(const DevInfo& d, const fp4_matrix_group* g, fp4_mode mode, int group_size) {
+  if (mode != FP4_MODE_AFFINE) return false;
+  for (int i = 0; i < g->count; ++i)
+    if (!aligned(g->scales[i], 16) || !aligned(g->biases[i], 16)) return false;
+  return qmv_affine_group_supported(d, g->count, g->N, g->K, group_size);
+}
+
+void fill_desc(const fp4_matrix_group* g, GemvGroupDesc* nd) {
+  nd->count = g->count;
+  nd->K = g->K;
+  for (int i = 0; i < g->count; ++i) {
+    nd->w[i] = g->w[i];
+    nd->scales[i] = static_cast<const uint8_t*>(g->scales[i]);
+    nd->biases[i] = reinterpret_cast<const uint16_t*>(g->biases[i]);
+    nd->N[i] = g->N[i];
+  }
+}
 }  // namespace
 
 fp4_status qmv_grouped(const fp4_bf16* x, const fp4_matrix_group* mats, fp4_mode mode, int bits, int group_size,
@@ -282,18 +301,25 @@ fp4_status qmv_grouped(const fp4_bf16* x, const fp4_matrix_group* mats, fp4_mode
     }
     GemvGroupDesc nd;
     const bool hint = prefetch_next && group_on_tc(*d, prefetch_next, mode);
-    if (hint) {
-      nd.count = prefetch_next->count;
-      nd.K = prefetch_next->K;
-      for (int i = 0; i < nd.count; ++i) {
-        nd.w[i] = prefetch_next->w[i];
-        nd.scales[i] = static_cast<const uint8_t*>(prefetch_next->scales[i]);
-        nd.N[i] = prefetch_next->N[i];
-      }
-    }
+    if (hint) fill_desc(prefetch_next, &nd);
     return from_cuda(launch_qmv_tc_group(*d, mode, x, nullptr, 0, mats->count, mats->w, sc, mats->global_scale_w,
                                          mats->N, mats->K, yy, hint ? &nd : nullptr, g_inject_timeout.load(),
                                          stream));
+  }
+  if (group_on_affine(*d, mats, mode, group_size)) {
+    const uint16_t* sc[4];
+    const uint16_t* bi[4];
+    uint16_t* yy[4];
+    for (int i = 0; i < mats->count; ++i) {
+      sc[i] = static_cast<const uint16_t*>(mats->scales[i]);
+      bi[i] = reinterpret_cast<const uint16_t*>(mats->biases[i]);
+      yy[i] = reinterpret_cast<uint16_t*>(y[i]);
+    }
+    GemvGroupDesc nd;
+    const bool hint = prefetch_next && group_on_affine(*d, prefetch_next, mode, group_size);
+    if (hint) fill_desc(prefetch_next, &nd);
+    return from_cuda(launch_qmv_affine_group(*d, x, mats->count, mats->w, sc, bi, mats->N, mats->K, group_size, yy,
+                                             hint ? &nd : nullptr, stream));
   }
   for (int i = 0; i < mats->count; ++i) {
     const cudaError_t e = launch_qmv(*d, x, nullptr, 0, mats->w[i], mats->scales[i], mats->biases[i],

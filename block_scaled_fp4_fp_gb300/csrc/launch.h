@@ -51,7 +51,8 @@ bool qmv_tc_group_supported(const DevInfo& d, int mode, int count, const int64_t
 struct GemvGroupDesc {
   int count = 0;
   const uint32_t* w[4] = {};
-  const uint8_t* scales[4] = {};
+  const uint8_t* scales[4] = {};   // FP4: E4M3/E8M0 bytes; affine: bf16 scales
+  const uint16_t* biases[4] = {};  // affine only
   int64_t N[4] = {};
   int64_t K = 0;
 };
@@ -69,6 +70,11 @@ bool qmv_affine_supported(const DevInfo& d, int64_t N, int64_t K, int group);
 cudaError_t launch_qmv_affine(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint16_t* scales,
                               const uint16_t* biases, int64_t N, int64_t K, int group, uint16_t* y,
                               cudaStream_t s);
+bool qmv_affine_group_supported(const DevInfo& d, int count, const int64_t* N, int64_t K, int group);
+cudaError_t launch_qmv_affine_group(const DevInfo& d, const uint16_t* x, int count, const uint32_t* const* w,
+                                    const uint16_t* const* scales, const uint16_t* const* biases, const int64_t* N,
+                                    int64_t K, int group, uint16_t* const* y, const GemvGroupDesc* next,
+                                    cudaStream_t s);
 
 // qqmm.cu: batch b reads xq + b stride_xq (uint32 words), sx + b stride_sx (bytes),
 // wq + b stride_wq (0: one W for every batch), sw + b stride_sw, gs_x[b], gs_w[b],

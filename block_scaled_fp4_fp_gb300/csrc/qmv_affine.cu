@@ -38,6 +38,7 @@
 //     in shared memory and are added in item-column order (deterministic).
 // Every mbarrier wait is bounded (an expired wait records FP4_ERR_TIMEOUT).
 #include <algorithm>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -130,11 +131,37 @@ __host__ __device__ inline uint32_t x_region_bytes(int K, int group) {
   return (uint32_t)K * 2u + 64u + nconst * 16u;
 }
 
+// The matrices of one launch (as the FP4 GEMV's table): a plain GEMV is a group
+// of one; a grouped launch multiplies the same x by up to four matrices of the
+// same K and group.  Matrix m owns row blocks blk0[m] .. blk0[m+1]-1, its rows
+// dealt out evenly over them.
+constexpr int kMaxGroup = 4;
+struct AffGroup {
+  CUtensorMap tmW[kMaxGroup];  // codes [N_m, K/2] bytes, boxes of R rows x 128 bytes
+  CUtensorMap tmS[kMaxGroup];  // bf16 scales [N_m, K/GROUP], boxes of R rows x KS/GROUP
+  CUtensorMap tmB[kMaxGroup];  // bf16 biases, the same boxes
+  uint16_t* y[kMaxGroup];
+  int N[kMaxGroup];
+  int blk0[kMaxGroup + 1];
+  int count;
+};
+// The launch that follows on the stream, if the caller names it: once all of a
+// CTA's own weights have landed, its producer warms L2 with the first `stages`
+// stages the same-numbered CTA of that launch will read (its own maps, stage
+// width ks codes).  A hint only: nothing is written.
+struct AffNext {
+  CUtensorMap tmW[kMaxGroup];
+  CUtensorMap tmS[kMaxGroup];
+  CUtensorMap tmB[kMaxGroup];
+  int N[kMaxGroup];
+  int blk0[kMaxGroup + 1];
+  int count, ks, nst, stages;  // count 0: no prefetch; ks codes per stage, nst stages in all
+};
+
 template <int GROUP, int IPS_>
 __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
-    const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
-    const __grid_constant__ CUtensorMap tmB, const uint16_t* __restrict__ x, int N, int K, AffGeo geo,
-    uint16_t* __restrict__ y, unsigned* __restrict__ err) {
+    const __grid_constant__ AffGroup mats, const __grid_constant__ AffNext next, const uint16_t* __restrict__ x,
+    int K, AffGeo geo, unsigned* __restrict__ err) {
   using CF = AffCfg<GROUP, IPS_>;
   constexpr int KS = CF::KS, IPS = CF::IPS, WR = CF::WR, RGW = CF::RGW;
   constexpr int kLpg = GROUP / 32;  // 32-code chunks per group
@@ -153,8 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
   uint64_t* xready = empty + kMaxSlots;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = (int)(((int64_t)N * blockIdx.x) / geo.nblk);
-  const int rows = (int)(((int64_t)N * (blockIdx.x + 1)) / geo.nblk) - r0;  // <= R
+  int mi = 0;  // this CTA's matrix
+  while (mi + 1 < mats.count && (int)blockIdx.x >= mats.blk0[mi + 1]) ++mi;
+  const int lb = (int)blockIdx.x - mats.blk0[mi], nb = mats.blk0[mi + 1] - mats.blk0[mi];
+  const int r0 = (int)(((int64_t)mats.N[mi] * lb) / nb);
+  const int rows = (int)(((int64_t)mats.N[mi] * (lb + 1)) / nb) - r0;  // <= R
+  const CUtensorMap* tmW = &mats.tmW[mi];
+  const CUtensorMap* tmS = &mats.tmS[mi];
+  const CUtensorMap* tmB = &mats.tmB[mi];
   const int nst = K / KS;
   constexpr int nbox = KS / 256;
 
@@ -173,9 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
   if (warp == kCWarps) {
     // ------------------------------------------------------------ producer --
     if (elect_one_sync()) {
-      prefetch_tmap(&tmW);
-      prefetch_tmap(&tmS);
-      prefetch_tmap(&tmB);
+      prefetch_tmap(tmW);
+      prefetch_tmap(tmS);
+      prefetch_tmap(tmB);
       const uint32_t tx = (uint32_t)geo.R * ((uint32_t)KS / 2u + 2u * geo.sbytes);
       int s = 0, round = 0;
       for (int i = 0; i < nst; ++i) {
@@ -183,15 +216,33 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
         if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
         uint8_t* sl = smem + s * geo.slot;
         mbar_arrive_expect_tx(&full[s], tx);
-        for (int h = 0; h < nbox; ++h) tma_load_2d(sl + h * geo.cb, &tmW, &full[s], (i * KS + h * 256) / 2, r0);
+        for (int h = 0; h < nbox; ++h) tma_load_2d(sl + h * geo.cb, tmW, &full[s], (i * KS + h * 256) / 2, r0);
         uint8_t* ss = sl + nbox * geo.cb;
-        tma_load_2d(ss, &tmS, &full[s], i * (KS / GROUP), r0);
-        tma_load_2d(ss + geo.RG * 16 * geo.sbytes, &tmB, &full[s], i * (KS / GROUP), r0);
+        tma_load_2d(ss, tmS, &full[s], i * (KS / GROUP), r0);
+        tma_load_2d(ss + geo.RG * 16 * geo.sbytes, tmB, &full[s], i * (KS / GROUP), r0);
         if (++s == geo.nslots) { s = 0; ++round; }
       }
       // no copy may still be writing shared memory when the CTA exits
       for (int i = max(0, nst - geo.nslots); i < nst; ++i)
         mbar_wait(&full[i % geo.nslots], (i / geo.nslots) & 1, err, failed);
+      // every weight byte of this CTA has landed: warm L2 for the next launch (AffNext)
+      if (next.count > 0) {
+        const int ncta = next.blk0[next.count];
+        for (int c = blockIdx.x; c < ncta; c += gridDim.x) {
+          int m = 0;
+          while (m + 1 < next.count && c >= next.blk0[m + 1]) ++m;
+          const int nr0 = (int)(((int64_t)next.N[m] * (c - next.blk0[m])) / (next.blk0[m + 1] - next.blk0[m]));
+          for (int i = 0; i < min(next.nst, next.stages); ++i) {
+            for (int h = 0; h < next.ks / 256; ++h)
+              asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                           :: "l"(&next.tmW[m]), "r"((i * next.ks + h * 256) / 2), "r"(nr0) : "memory");
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                         :: "l"(&next.tmS[m]), "r"(i * (next.ks / GROUP)), "r"(nr0) : "memory");
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                         :: "l"(&next.tmB[m]), "r"(i * (next.ks / GROUP)), "r"(nr0) : "memory");
+          }
+        }
+      }
     }
     return;
   }
@@ -358,22 +409,21 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
     float v = 0.f;
 #pragma unroll
     for (int k = 0; k < IPS; ++k) v += part[k * kMaxRows + r];
-    y[r0 + r] = (uint16_t)f32_to_bf16_rn(v);
+    mats.y[mi][r0 + r] = (uint16_t)f32_to_bf16_rn(v);
   }
 }
 
 // The plan: one CTA per SM (more when N > 256 per SM), R rows per CTA, the
 // widest stage (IPS item columns) whose ring still holds at least three slots,
-// as many slots as fit.
+// as many slots as fit.  A group stacks its matrices' rows for the block count,
+// then takes the smallest R that gives every matrix whole blocks within it.
 struct Plan {
   AffGeo geo;
   int ips = 0;
+  int nb[kMaxGroup] = {0, 0, 0, 0};  // row blocks of each matrix
 };
 
-bool plan_affine(const DevInfo& d, int64_t N, int64_t K, int group, Plan* p) {
-  if (K > kMaxK || d.sm_count < 1 || (group != 32 && group != 64 && group != 128)) return false;
-  const int64_t nblk0 = std::max<int64_t>(d.sm_count, (N + kMaxRows - 1) / kMaxRows);
-  const int64_t R = (N + nblk0 - 1) / nblk0;
+bool plan_geo(int64_t R, int nblk, int64_t K, int group, Plan* p) {
   if (R < 1 || R > kMaxRows) return false;
   const uint32_t fixed = 1024u + x_region_bytes((int)K, group) + kPartBytes + kBarBytes;
   if (fixed >= kSmemBytes) return false;
@@ -381,7 +431,7 @@ bool plan_affine(const DevInfo& d, int64_t N, int64_t K, int group, Plan* p) {
     const int KS = 128 * ips;
     if (KS < 8 * group || K % KS != 0) continue;
     AffGeo g;
-    g.nblk = (int)std::min<int64_t>(nblk0, N);  // rows per block <= ceil(N / nblk) = R
+    g.nblk = nblk;
     g.R = (int)R;
     g.RG = (int)((R + 15) / 16);
     g.cb = (uint32_t)g.RG * 16u * 128u;
@@ -398,6 +448,27 @@ bool plan_affine(const DevInfo& d, int64_t N, int64_t K, int group, Plan* p) {
   return false;
 }
 
+bool plan_affine(const DevInfo& d, int count, const int64_t* N, int64_t K, int group, Plan* p) {
+  if (count < 1 || count > kMaxGroup || K > kMaxK || d.sm_count < 1 || (group != 32 && group != 64 && group != 128))
+    return false;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) total += N[i];
+  const int64_t nblk0 = std::max<int64_t>(d.sm_count, (total + kMaxRows - 1) / kMaxRows);
+  if (count == 1) {
+    p->nb[0] = (int)std::min<int64_t>(nblk0, N[0]);  // rows per block <= ceil(N / nblk) = R
+    return plan_geo((N[0] + nblk0 - 1) / nblk0, p->nb[0], K, group, p);
+  }
+  for (int64_t R = (total + nblk0 - 1) / nblk0; R <= kMaxRows; ++R) {
+    int64_t blocks = 0;
+    for (int i = 0; i < count; ++i) blocks += (N[i] + R - 1) / R;
+    if (blocks <= nblk0) {
+      for (int i = 0; i < count; ++i) p->nb[i] = (int)((N[i] + R - 1) / R);
+      return plan_geo(R, (int)blocks, K, group, p);
+    }
+  }
+  return false;
+}
+
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* p, uint64_t inner, uint64_t rows,
               uint64_t pitch, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
@@ -410,25 +481,28 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* p, uint64_t in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One matrix's maps for blocks of R rows and stages of KS codes.
+bool make_maps(CUtensorMap* tw, CUtensorMap* ts, CUtensorMap* tb, const void* w, const void* scales,
+               const void* biases, int64_t N, int64_t K, int group, int R, int KS) {
+  const uint64_t groups = (uint64_t)(K / group);
+  return make_map(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128,
+                  (uint32_t)R, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map(ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, groups, (uint64_t)N, groups * 2, (uint32_t)(KS / group),
+                  (uint32_t)R, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_map(tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, groups, (uint64_t)N, groups * 2, (uint32_t)(KS / group),
+                  (uint32_t)R, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+constexpr int kPrefetchStages = 3;  // stages of the next launch warmed in L2 (as the FP4 GEMV)
+
 template <int GROUP, int IPS>
-cudaError_t launch_group(const DevInfo& d, const AffGeo& geo, const uint16_t* x, const uint32_t* w,
-                         const uint16_t* scales, const uint16_t* biases, int64_t N, int64_t K, uint16_t* y,
-                         cudaStream_t s) {
-  constexpr int KS = AffCfg<GROUP, IPS>::KS;
-  CUtensorMap tw, ts, tb;
-  const uint64_t groups = (uint64_t)(K / GROUP);
-  if (!make_map(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2, 128,
-                (uint32_t)geo.R, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, groups, (uint64_t)N, groups * 2,
-                (uint32_t)(KS / GROUP), (uint32_t)geo.R, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, groups, (uint64_t)N, groups * 2,
-                (uint32_t)(KS / GROUP), (uint32_t)geo.R, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+cudaError_t launch_group(const DevInfo& d, const Plan& p, const AffGroup& g, const AffNext& nx, const uint16_t* x,
+                         int64_t K, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(qmv_affine_kernel<GROUP, IPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)geo.nblk);
+  cfg.gridDim = dim3((unsigned)p.geo.nblk);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
@@ -437,15 +511,15 @@ cudaError_t launch_group(const DevInfo& d, const AffGeo& geo, const uint16_t* x,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qmv_affine_kernel<GROUP, IPS>, tw, ts, tb, x, (int)N, (int)K, geo, y, d.err);
+  return cudaLaunchKernelEx(&cfg, qmv_affine_kernel<GROUP, IPS>, g, nx, x, (int)K, p.geo, d.err);
 }
 
 template <int GROUP>
-cudaError_t launch_ips(const DevInfo& d, const Plan& p, const uint16_t* x, const uint32_t* w, const uint16_t* scales,
-                       const uint16_t* biases, int64_t N, int64_t K, uint16_t* y, cudaStream_t s) {
-  if (p.ips == 16) return launch_group<GROUP, 16>(d, p.geo, x, w, scales, biases, N, K, y, s);
-  if (p.ips == 8) return launch_group<GROUP, 8>(d, p.geo, x, w, scales, biases, N, K, y, s);
-  if (GROUP <= 64 && p.ips == 4) return launch_group<GROUP, (GROUP <= 64 ? 4 : 8)>(d, p.geo, x, w, scales, biases, N, K, y, s);
+cudaError_t launch_ips(const DevInfo& d, const Plan& p, const AffGroup& g, const AffNext& nx, const uint16_t* x,
+                       int64_t K, cudaStream_t s) {
+  if (p.ips == 16) return launch_group<GROUP, 16>(d, p, g, nx, x, K, s);
+  if (p.ips == 8) return launch_group<GROUP, 8>(d, p, g, nx, x, K, s);
+  if (GROUP <= 64 && p.ips == 4) return launch_group<GROUP, (GROUP <= 64 ? 4 : 8)>(d, p, g, nx, x, K, s);
   return cudaErrorInvalidValue;
 }
 
@@ -453,18 +527,63 @@ cudaError_t launch_ips(const DevInfo& d, const Plan& p, const uint16_t* x, const
 
 bool qmv_affine_supported(const DevInfo& d, int64_t N, int64_t K, int group) {
   Plan p;
-  return plan_affine(d, N, K, group, &p);
+  return plan_affine(d, 1, &N, K, group, &p);
+}
+
+bool qmv_affine_group_supported(const DevInfo& d, int count, const int64_t* N, int64_t K, int group) {
+  Plan p;
+  return plan_affine(d, count, N, K, group, &p);
+}
+
+cudaError_t launch_qmv_affine_group(const DevInfo& d, const uint16_t* x, int count, const uint32_t* const* w,
+                                    const uint16_t* const* scales, const uint16_t* const* biases, const int64_t* N,
+                                    int64_t K, int group, uint16_t* const* y, const GemvGroupDesc* nextd,
+                                    cudaStream_t s) {
+  Plan p;
+  if (!plan_affine(d, count, N, K, group, &p)) return cudaErrorInvalidValue;
+  AffGroup g;
+  memset(&g, 0, sizeof(g));
+  g.count = count;
+  for (int i = 0; i < count; ++i) {
+    if (!make_maps(&g.tmW[i], &g.tmS[i], &g.tmB[i], w[i], scales[i], biases[i], N[i], K, group, p.geo.R,
+                   128 * p.ips))
+      return cudaErrorInvalidValue;
+    g.y[i] = y[i];
+    g.N[i] = (int)N[i];
+    g.blk0[i + 1] = g.blk0[i] + p.nb[i];
+  }
+  // the next launch as it will be planned (a hint: dropped if it has no plan)
+  AffNext nx;
+  memset(&nx, 0, sizeof(nx));
+  if (nextd && nextd->count >= 1 && nextd->count <= kMaxGroup) {
+    Plan np;
+    bool ok = plan_affine(d, nextd->count, nextd->N, nextd->K, group, &np);
+    for (int i = 0; ok && i < nextd->count; ++i) {
+      ok = nextd->biases[i] != nullptr &&
+           make_maps(&nx.tmW[i], &nx.tmS[i], &nx.tmB[i], nextd->w[i], nextd->scales[i], nextd->biases[i],
+                     nextd->N[i], nextd->K, group, np.geo.R, 128 * np.ips);
+      nx.N[i] = (int)nextd->N[i];
+      nx.blk0[i + 1] = nx.blk0[i] + np.nb[i];
+    }
+    if (ok) {
+      nx.count = nextd->count;
+      nx.ks = 128 * np.ips;
+      nx.nst = (int)(nextd->K / nx.ks);
+      nx.stages = kPrefetchStages;
+    } else {
+      memset(&nx, 0, sizeof(nx));
+    }
+  }
+  if (group == 32) return launch_ips<32>(d, p, g, nx, x, K, s);
+  if (group == 64) return launch_ips<64>(d, p, g, nx, x, K, s);
+  if (group == 128) return launch_ips<128>(d, p, g, nx, x, K, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_qmv_affine(const DevInfo& d, const uint16_t* x, const uint32_t* w, const uint16_t* scales,
                               const uint16_t* biases, int64_t N, int64_t K, int group, uint16_t* y,
                               cudaStream_t s) {
-  Plan p;
-  if (!plan_affine(d, N, K, group, &p)) return cudaErrorInvalidValue;
-  if (group == 32) return launch_ips<32>(d, p, x, w, scales, biases, N, K, y, s);
-  if (group == 64) return launch_ips<64>(d, p, x, w, scales, biases, N, K, y, s);
-  if (group == 128) return launch_ips<128>(d, p, x, w, scales, biases, N, K, y, s);
-  return cudaErrorInvalidValue;
+  return launch_qmv_affine_group(d, x, 1, &w, &scales, &biases, &N, K, group, &y, nullptr, s);
 }
 
 }  // namespace fp4

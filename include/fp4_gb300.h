@@ -197,9 +197,10 @@ typedef struct fp4_matrix_group {
  * weight loads, it warms L2 with the first stages that launch will read, so
  * that its start does not wait on DRAM.  It is validated like `mats` (its
  * pointers must be device memory); nothing is written through it.
- * NVFP4 and MXFP4 run as one tensor-core launch when the stacked rows have a
- * plan and every scale row is 16-byte aligned; affine or other cases run as
- * mats->count qmv launches (and ignore the hint).  Otherwise qmv's rules. */
+ * NVFP4 and MXFP4 run as one tensor-core launch, affine as one launch of the
+ * affine GEMV, when the stacked rows have a plan and every scale (and bias)
+ * row is 16-byte aligned; other cases run as mats->count qmv launches (and
+ * ignore the hint).  Otherwise qmv's rules. */
 fp4_status qmv_grouped(const fp4_bf16* x, const fp4_matrix_group* mats, fp4_mode mode, int bits, int group_size,
                        fp4_bf16* const* y, const fp4_matrix_group* prefetch_next, cudaStream_t stream);
 

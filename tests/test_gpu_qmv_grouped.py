@@ -48,12 +48,13 @@ def test_qmv_grouped_small(B, mode, Ns, K):
     run_group(B, mode, Ns, K, seed=sum(Ns) + K)
 
 
-@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("mode", [2, 1, 0])
 @pytest.mark.parametrize("Ns", [[synth.HIDDEN] * 3, [17408, 17408]])
 def test_qmv_grouped_decode_shapes_sampled(B, mode, Ns):
     """q, k, v (3 x 5120 x 5120) and gate, up (2 x 17408 x 5120) stored apart, in
-    the launch configuration the bench uses; the oracle checks a seeded sample of
-    rows of every matrix, including the first and last rows."""
+    the launch configuration the bench uses (FP4 on the tensor-core GEMV, affine
+    g64 on the affine GEMV, one launch each); the oracle checks a seeded sample
+    of rows of every matrix, including the first and last rows."""
     K = synth.HIDDEN
 
     def rows_per(N, i):
@@ -69,7 +70,7 @@ def test_qmv_grouped_split_k(B, mode):
     run_group(B, mode, [300, 700], 34816, seed=77)
 
 
-@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("mode", [2, 1, 0])
 def test_qmv_grouped_prefetch_hint_changes_nothing(B, mode):
     """A chain of launches each naming the next one's weights (the L2 warm-up
     hint, wrapping around): every y is bit-identical to the same launches without
