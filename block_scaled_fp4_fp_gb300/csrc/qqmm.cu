@@ -648,6 +648,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) qqmm_pa
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
+  // programmatic dependent launch: the set-up above overlapped the previous
+  // kernel's tail; x, its scales and the global scales may come from it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -928,9 +932,18 @@ cudaError_t launch_pair_mode(const DevInfo& d, int npairs_max, const uint32_t* x
   bt.stride_out = ba.stride_out;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + 255) / 256) * ba.batch;
   const int npairs = (int)std::min<int64_t>(tiles, npairs_max);
-  qqmm_pair_kernel<MODE><<<dim3((unsigned)(2 * npairs)), kThreads, P::SMEM_BYTES, s>>>(
-      ta, tb, tsa, tsb, to, gs_x, gs_w, (int)M, (int)N, (int)K, bt, d.err, inject);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * npairs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, qqmm_pair_kernel<MODE>, ta, tb, tsa, tsb, to, gs_x, gs_w, (int)M, (int)N, (int)K,
+                            bt, d.err, inject);
 }
 
 // Workspace of a fused call: [codes | tiled scales | per-CTA partial maxima |

@@ -26,6 +26,8 @@ constexpr float kNvfp4MaxProduct = 2688.0f;  // 448 * 6
 __global__ void __launch_bounds__(kThreads) amax_partial_kernel(const uint16_t* __restrict__ x,
                                                                  int64_t n,
                                                                  uint32_t* __restrict__ partials) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // x may come from the previous kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t nvec = n >> 3;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   uint32_t m2 = 0;
@@ -65,6 +67,8 @@ __global__ void __launch_bounds__(kThreads) amax_partial_kernel(const uint16_t* 
 __global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __restrict__ partials,
                                                                int np, float* __restrict__ gs_out,
                                                                float* __restrict__ amax_out) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials of the kernel before
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint32_t m = 0;
   for (int i = threadIdx.x; i < np; i += blockDim.x) m = max(m, partials[i]);
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -287,9 +291,19 @@ cudaError_t launch_amax(const DevInfo& d, const uint16_t* x, int64_t n, float* g
   int64_t blocks = (nvec + 2 * kThreads - 1) / (2 * kThreads);
   blocks = std::min<int64_t>(blocks, std::min<int64_t>(max_partials, (int64_t)d.sm_count * 4));
   blocks = std::max<int64_t>(blocks, 1);
-  amax_partial_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(x, n, partials);
-  amax_final_kernel<<<1, kThreads, 0, s>>>(partials, (int)blocks, gs_out, amax_out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)blocks);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, amax_partial_kernel, x, n, partials);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(1);
+  return cudaLaunchKernelEx(&cfg, amax_final_kernel, (const uint32_t*)partials, (int)blocks, gs_out, amax_out);
 }
 
 cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, int64_t cols,
