@@ -39,6 +39,7 @@
 // Every mbarrier wait is bounded (an expired wait records FP4_ERR_TIMEOUT).
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -52,14 +53,16 @@ namespace {
 
 constexpr int kCWarps = 16;                   // consumer warps
 constexpr int kThreads = (kCWarps + 1) * 32;  // + the TMA producer warp
-constexpr int kMaxK = 32768;                  // x is staged whole in shared memory
+constexpr int kMaxK = 32768;                  // a CTA stages its whole x slice in shared memory
 constexpr int kMaxRows = 256;                 // rows per CTA (TMA box height)
 constexpr int kMaxSlots = 24;
 constexpr int kXPre = 4;                      // stages issued before x has been staged
 constexpr uint32_t kSmemBytes = 227u * 1024u;
 constexpr uint32_t kBarBytes = 512;
 constexpr uint32_t kPartBytes = 16 * kMaxRows * 4;  // [item column][row] partial sums
-static_assert(2 * kMaxSlots + 2 <= kBarBytes / 8, "barrier area");
+constexpr int kMaxSplit = 4;                        // CTAs per cluster (K slices) at most
+constexpr uint32_t kXPartBytes = kMaxSplit * kMaxRows * 4;  // rank 0: the other ranks' row partials
+static_assert(2 * kMaxSlots + 3 <= kBarBytes / 8, "barrier area");
 
 // A stage is IPS item columns of 128 codes (KS = 128 IPS codes per row); IPS is
 // chosen per launch (4, 8 or 16: wider stages give each warp several independent
@@ -92,6 +95,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 __device__ __forceinline__ float4 lds128f(uint32_t a) {
   const uint4 v = lds128(a);
   return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+
+// shared::cluster address of a shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
 }
 
 __device__ __forceinline__ float lds_bf16(uint32_t a) {
@@ -155,13 +165,13 @@ struct AffNext {
   CUtensorMap tmB[kMaxGroup];
   int N[kMaxGroup];
   int blk0[kMaxGroup + 1];
-  int count, ks, nst, stages;  // count 0: no prefetch; ks codes per stage, nst stages in all
+  int count, ks, nst, split, stages;  // count 0: no prefetch; ks codes per stage, nst stages of K, split ranks
 };
 
 template <int GROUP, int IPS_>
 __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
     const __grid_constant__ AffGroup mats, const __grid_constant__ AffNext next, const uint16_t* __restrict__ x,
-    int K, AffGeo geo, unsigned* __restrict__ err) {
+    int K, int split, AffGeo geo, unsigned* __restrict__ err) {
   using CF = AffCfg<GROUP, IPS_>;
   constexpr int KS = CF::KS, IPS = CF::IPS, WR = CF::WR, RGW = CF::RGW;
   constexpr int kLpg = GROUP / 32;  // 32-code chunks per group
@@ -169,26 +179,35 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const int C = K >> 5;
+  // K split: a cluster of `split` CTAs owns a row block; rank q takes stages
+  // kb0 .. kb0 + nst - 1 and stages x only over them (kslice codes at most)
+  const int rank = (int)(blockIdx.x % (unsigned)split), blk = (int)(blockIdx.x / (unsigned)split);
+  const int nst_all = K / KS;
+  const int kb0 = (int)(((int64_t)nst_all * rank) / split);
+  const int nst = (int)(((int64_t)nst_all * (rank + 1)) / split) - kb0;
+  const int kslice = (nst_all + split - 1) / split * KS;
+  const int C = (nst * KS) >> 5;  // x chunks of this rank
   const uint32_t ring_bytes = (uint32_t)geo.nslots * geo.slot;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + ring_bytes);
-  uint4* zero16 = reinterpret_cast<uint4*>(smem + ring_bytes + (uint32_t)K * 2u);
-  float4* cst = reinterpret_cast<float4*>(smem + ring_bytes + (uint32_t)K * 2u + 64u);
-  float* part = reinterpret_cast<float*>(smem + ring_bytes + x_region_bytes(K, GROUP));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes + x_region_bytes(K, GROUP) + kPartBytes);
+  uint4* zero16 = reinterpret_cast<uint4*>(smem + ring_bytes + (uint32_t)kslice * 2u);
+  float4* cst = reinterpret_cast<float4*>(smem + ring_bytes + (uint32_t)kslice * 2u + 64u);
+  float* part = reinterpret_cast<float*>(smem + ring_bytes + x_region_bytes(kslice, GROUP));
+  float* xpart = part + kPartBytes / 4;  // rank 0: [rank][row] partials of the other ranks
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring_bytes + x_region_bytes(kslice, GROUP) + kPartBytes +
+                                               kXPartBytes);
   uint64_t* empty = full + kMaxSlots;
   uint64_t* xready = empty + kMaxSlots;
+  uint64_t* pbar = xready + 1;  // rank 0: the other ranks' partials have landed (byte count)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int mi = 0;  // this CTA's matrix
-  while (mi + 1 < mats.count && (int)blockIdx.x >= mats.blk0[mi + 1]) ++mi;
-  const int lb = (int)blockIdx.x - mats.blk0[mi], nb = mats.blk0[mi + 1] - mats.blk0[mi];
+  while (mi + 1 < mats.count && blk >= mats.blk0[mi + 1]) ++mi;
+  const int lb = blk - mats.blk0[mi], nb = mats.blk0[mi + 1] - mats.blk0[mi];
   const int r0 = (int)(((int64_t)mats.N[mi] * lb) / nb);
   const int rows = (int)(((int64_t)mats.N[mi] * (lb + 1)) / nb) - r0;  // <= R
   const CUtensorMap* tmW = &mats.tmW[mi];
   const CUtensorMap* tmS = &mats.tmS[mi];
   const CUtensorMap* tmB = &mats.tmB[mi];
-  const int nst = K / KS;
   constexpr int nbox = KS / 256;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -198,9 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
       mbar_init(&empty[s], kCWarps);
     }
     mbar_init(xready, 1);
-    fence_barrier_init();
+    mbar_init(pbar, 1);
+    fence_barrier_init();  // release of the barrier inits to the cluster
   }
   __syncthreads();
+  // the other ranks store into rank 0's shared memory only after this arrival of
+  // every thread of rank 0 (its barriers are initialised); rank 0 never waits on it
+  if (split > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   bool failed = false;
 
   if (warp == kCWarps) {
@@ -216,10 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
         if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
         uint8_t* sl = smem + s * geo.slot;
         mbar_arrive_expect_tx(&full[s], tx);
-        for (int h = 0; h < nbox; ++h) tma_load_2d(sl + h * geo.cb, tmW, &full[s], (i * KS + h * 256) / 2, r0);
+        const int kb = kb0 + i;
+        for (int h = 0; h < nbox; ++h) tma_load_2d(sl + h * geo.cb, tmW, &full[s], (kb * KS + h * 256) / 2, r0);
         uint8_t* ss = sl + nbox * geo.cb;
-        tma_load_2d(ss, tmS, &full[s], i * (KS / GROUP), r0);
-        tma_load_2d(ss + geo.RG * 16 * geo.sbytes, tmB, &full[s], i * (KS / GROUP), r0);
+        tma_load_2d(ss, tmS, &full[s], kb * (KS / GROUP), r0);
+        tma_load_2d(ss + geo.RG * 16 * geo.sbytes, tmB, &full[s], kb * (KS / GROUP), r0);
         if (++s == geo.nslots) { s = 0; ++round; }
       }
       // no copy may still be writing shared memory when the CTA exits
@@ -227,12 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
         mbar_wait(&full[i % geo.nslots], (i / geo.nslots) & 1, err, failed);
       // every weight byte of this CTA has landed: warm L2 for the next launch (AffNext)
       if (next.count > 0) {
-        const int ncta = next.blk0[next.count];
+        const int ncta = next.blk0[next.count] * next.split;
         for (int c = blockIdx.x; c < ncta; c += gridDim.x) {
+          const int nrank = c % next.split, nbk = c / next.split;
           int m = 0;
-          while (m + 1 < next.count && c >= next.blk0[m + 1]) ++m;
-          const int nr0 = (int)(((int64_t)next.N[m] * (c - next.blk0[m])) / (next.blk0[m + 1] - next.blk0[m]));
-          for (int i = 0; i < min(next.nst, next.stages); ++i) {
+          while (m + 1 < next.count && nbk >= next.blk0[m + 1]) ++m;
+          const int nr0 = (int)(((int64_t)next.N[m] * (nbk - next.blk0[m])) / (next.blk0[m + 1] - next.blk0[m]));
+          const int k0 = (int)(((int64_t)next.nst * nrank) / next.split);
+          const int k1 = (int)(((int64_t)next.nst * (nrank + 1)) / next.split);
+          for (int i = k0; i < min(k1, k0 + next.stages); ++i) {
             for (int h = 0; h < next.ks / 256; ++h)
               asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
                            :: "l"(&next.tmW[m]), "r"((i * next.ks + h * 256) / 2), "r"(nr0) : "memory");
@@ -256,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
   if (tid < 4) zero16[tid] = make_uint4(0, 0, 0, 0);
   for (int c = tid; c < C; c += kCWarps * 32) {
     const unsigned mask = __activemask();
-    const uint4* src = reinterpret_cast<const uint4*>(x + c * 32);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)kb0 * KS + c * 32);
     uint4 xv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) xv[i] = __ldg(src + i);
@@ -405,31 +432,57 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
     }
   }
   asm volatile("bar.sync 1, %0;" :: "n"(kCWarps * 32) : "memory");
+  if (split > 1 && rank > 0) {
+    // this rank's row sums into rank 0's shared memory by asynchronous remote
+    // stores, which rank 0's barrier counts by bytes
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // rank 0 is initialised
+    for (int r = tid; r < rows; r += kCWarps * 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int k = 0; k < IPS; ++k) v += part[k * kMaxRows + r];
+      asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                   :: "r"(mapa_u32(smem_u32(xpart + rank * kMaxRows + r), 0)), "r"(__float_as_uint(v)),
+                      "r"(mapa_u32(smem_u32(pbar), 0)) : "memory");
+    }
+    return;
+  }
+  if (split > 1) {
+    if (tid == 0) mbar_arrive_expect_tx(pbar, (uint32_t)(split - 1) * (uint32_t)rows * 4u);
+    mbar_wait(pbar, 0, err, failed);  // every other rank's row sums have landed
+  }
   for (int r = tid; r < rows; r += kCWarps * 32) {
     float v = 0.f;
 #pragma unroll
     for (int k = 0; k < IPS; ++k) v += part[k * kMaxRows + r];
+    for (int c = 1; c < split; ++c) v += xpart[c * kMaxRows + r];  // in rank order: the same on every run
     mats.y[mi][r0 + r] = (uint16_t)f32_to_bf16_rn(v);
   }
 }
 
-// The plan: one CTA per SM (more when N > 256 per SM), R rows per CTA, the
-// widest stage (IPS item columns) whose ring still holds at least three slots,
-// as many slots as fit.  A group stacks its matrices' rows for the block count,
-// then takes the smallest R that gives every matrix whole blocks within it.
+// The plan: R rows per row block, the widest stage (IPS item columns) whose
+// ring still holds at least three slots, as many slots as fit.  A row block is
+// one CTA, or a cluster of 2 or 4 CTAs splitting K when one CTA per SM would
+// get fewer than kMinRows rows (the consumers' per-item latency makes short
+// blocks slow: 34-row blocks ran at ~2 TB/s).  A group stacks its matrices'
+// rows for the block count, then takes the smallest R that gives every matrix
+// whole blocks within it.
+constexpr int kMinRows = 96;
 struct Plan {
   AffGeo geo;
   int ips = 0;
+  int split = 1;
   int nb[kMaxGroup] = {0, 0, 0, 0};  // row blocks of each matrix
 };
 
-bool plan_geo(int64_t R, int nblk, int64_t K, int group, Plan* p) {
+bool plan_geo(int64_t R, int nblk, int64_t K, int split, int group, Plan* p) {
   if (R < 1 || R > kMaxRows) return false;
-  const uint32_t fixed = 1024u + x_region_bytes((int)K, group) + kPartBytes + kBarBytes;
-  if (fixed >= kSmemBytes) return false;
   for (int ips : {16, 8, 4}) {
     const int KS = 128 * ips;
-    if (KS < 8 * group || K % KS != 0) continue;
+    if (KS < 8 * group || K % KS != 0 || K / KS < split) continue;
+    const int64_t kslice = (K / KS + split - 1) / split * KS;
+    if (kslice > kMaxK) continue;
+    const uint32_t fixed = 1024u + x_region_bytes((int)kslice, group) + kPartBytes + kXPartBytes + kBarBytes;
+    if (fixed >= kSmemBytes) continue;
     AffGeo g;
     g.nblk = nblk;
     g.R = (int)R;
@@ -443,30 +496,76 @@ bool plan_geo(int64_t R, int nblk, int64_t K, int group, Plan* p) {
     g.nslots = (int)nslots;
     p->geo = g;
     p->ips = ips;
+    p->split = split;
     return true;
   }
   return false;
 }
 
-bool plan_affine(const DevInfo& d, int count, const int64_t* N, int64_t K, int group, Plan* p) {
-  if (count < 1 || count > kMaxGroup || K > kMaxK || d.sm_count < 1 || (group != 32 && group != 64 && group != 128))
-    return false;
+// Clusters of `split` CTAs of the kernel that can be resident at once (every
+// instantiation has the same block and shared memory; cached per device).
+int aff_max_clusters(const DevInfo& d, int split) {
+  static std::mutex mu;
+  static int cache[64][kMaxSplit + 1];
+  static bool have[64][kMaxSplit + 1];
+  if (d.device < 0 || d.device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (have[d.device][split]) return cache[d.device][split];
+  int n = 0;
+  if (cudaFuncSetAttribute(qmv_affine_kernel<64, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(split * std::max(1, d.sm_count / split)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, qmv_affine_kernel<64, 16>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a failed query leaves no sticky error behind
+  cache[d.device][split] = n;
+  have[d.device][split] = true;
+  return n;
+}
+
+bool plan_split(const DevInfo& d, int count, const int64_t* N, int64_t K, int group, int split, Plan* p) {
   int64_t total = 0;
   for (int i = 0; i < count; ++i) total += N[i];
-  const int64_t nblk0 = std::max<int64_t>(d.sm_count, (total + kMaxRows - 1) / kMaxRows);
+  const int64_t nblk0 = split == 1 ? std::max<int64_t>(d.sm_count, (total + kMaxRows - 1) / kMaxRows)
+                                   : std::min<int64_t>(aff_max_clusters(d, split), d.sm_count / split);
+  if (nblk0 < 1) return false;
   if (count == 1) {
     p->nb[0] = (int)std::min<int64_t>(nblk0, N[0]);  // rows per block <= ceil(N / nblk) = R
-    return plan_geo((N[0] + nblk0 - 1) / nblk0, p->nb[0], K, group, p);
+    return plan_geo((N[0] + nblk0 - 1) / nblk0, p->nb[0], K, split, group, p);
   }
   for (int64_t R = (total + nblk0 - 1) / nblk0; R <= kMaxRows; ++R) {
     int64_t blocks = 0;
     for (int i = 0; i < count; ++i) blocks += (N[i] + R - 1) / R;
     if (blocks <= nblk0) {
       for (int i = 0; i < count; ++i) p->nb[i] = (int)((N[i] + R - 1) / R);
-      return plan_geo(R, (int)blocks, K, group, p);
+      return plan_geo(R, (int)blocks, K, split, group, p);
     }
   }
   return false;
+}
+
+bool plan_affine(const DevInfo& d, int count, const int64_t* N, int64_t K, int group, Plan* p) {
+  if (count < 1 || count > kMaxGroup || d.sm_count < 1 || (group != 32 && group != 64 && group != 128))
+    return false;
+  bool any = false;
+  for (int split : {1, 2, 4}) {
+    Plan q;
+    if (!plan_split(d, count, N, K, group, split, &q)) continue;
+    *p = q;
+    any = true;
+    if (q.geo.R >= kMinRows) break;  // the first split whose blocks are tall enough
+  }
+  return any;
 }
 
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* p, uint64_t inner, uint64_t rows,
@@ -502,16 +601,20 @@ cudaError_t launch_group(const DevInfo& d, const Plan& p, const AffGroup& g, con
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.geo.nblk);
+  cfg.gridDim = dim3((unsigned)(p.geo.nblk * p.split));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)p.split;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qmv_affine_kernel<GROUP, IPS>, g, nx, x, (int)K, p.geo, d.err);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, qmv_affine_kernel<GROUP, IPS>, g, nx, x, (int)K, p.split, p.geo, d.err);
 }
 
 template <int GROUP>
@@ -569,6 +672,7 @@ cudaError_t launch_qmv_affine_group(const DevInfo& d, const uint16_t* x, int cou
       nx.count = nextd->count;
       nx.ks = 128 * np.ips;
       nx.nst = (int)(nextd->K / nx.ks);
+      nx.split = np.split;
       nx.stages = kPrefetchStages;
     } else {
       memset(&nx, 0, sizeof(nx));
