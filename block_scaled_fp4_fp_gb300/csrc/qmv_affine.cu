@@ -463,10 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
 // ring still holds at least three slots, as many slots as fit.  A row block is
 // one CTA, or a cluster of 2 or 4 CTAs splitting K when one CTA per SM would
 // get fewer than kMinRows rows (the consumers' per-item latency makes short
-// blocks slow: 34-row blocks ran at ~2 TB/s).  A group stacks its matrices'
+// blocks slow: 34-row blocks ran at ~2 TB/s; on the affine decode stack a
+// threshold of 64 / 96 / 128 / 200 rows gave 54.0 / 57.7 / 58.4 / 58.3 % of HBM).  A group stacks its matrices'
 // rows for the block count, then takes the smallest R that gives every matrix
 // whole blocks within it.
-constexpr int kMinRows = 96;
+constexpr int kMinRows = 128;
 struct Plan {
   AffGeo geo;
   int ips = 0;
