@@ -597,12 +597,14 @@ __device__ __forceinline__ void tc2_mma(uint32_t d, uint64_t a, uint64_t b, uint
   }
 }
 
-template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) qqmm_pair_kernel(
+// (launched with a cluster dimension of 2; FQ: the fused call's quantize
+// prologue first, in a cooperative launch)
+template <int MODE, bool FQ>
+__global__ void __launch_bounds__(kThreads, 1) qqmm_pair_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
     const __grid_constant__ CUtensorMap tmO, const float* __restrict__ gs_x, const float* __restrict__ gs_w, int M,
-    int N, int K, Batch bt, unsigned* __restrict__ err, int inject_timeout) {
+    int N, int K, Batch bt, unsigned* __restrict__ err, int inject_timeout, FusedX fx) {
   using P = PairCfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -652,6 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) qqmm_pa
   // kernel's tail; x, its scales and the global scales may come from it
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (FQ) quantize_prologue<MODE>(fx, M, K, err, failed);  // x -> codes and tiled scales in the workspace
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -743,7 +746,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) qqmm_pa
     for (int tile = pair; tile < num_tiles; tile += npairs, ++it) {
       const int b = tile / tiles_per_batch, rem = tile - b * tiles_per_batch;
       const int mp = rem % num_mp, n_blk = rem / num_mp;
-      const float gx = gs_x ? __ldg(gs_x + b) : 1.0f;
+      // (a fused call's activation scale was written by this grid: read it coherently)
+      const float gx = gs_x ? (FQ ? __ldcg(gs_x + b) : __ldg(gs_x + b)) : 1.0f;
       const float alpha = __fmul_rn(gx, gs_w ? __ldg(gs_w + b) : 1.0f);
       mbar_wait(acc_full, it & 1, err, failed);
       tc_fence_after();
@@ -893,13 +897,22 @@ int pair_clusters(const DevInfo& d) {
   if (have[d.device]) return cache[d.device];
   int n = 0;
   const int smem = (int)PairCfg<MODE>::SMEM_BYTES;
-  if (cudaFuncSetAttribute(qqmm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
-      cudaSuccess) {
+  if (cudaFuncSetAttribute(qqmm_pair_kernel<MODE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(qqmm_pair_kernel<MODE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+          cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * std::max(1, d.sm_count / 2)));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
-    if (cudaOccupancyMaxActiveClusters(&n, qqmm_pair_kernel<MODE>, &cfg) != cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, qqmm_pair_kernel<MODE, false>, &cfg) != cudaSuccess) {
       n = 0;
       cudaGetLastError();
     }
@@ -937,13 +950,17 @@ cudaError_t launch_pair_mode(const DevInfo& d, int npairs_max, const uint32_t* x
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = P::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, qqmm_pair_kernel<MODE>, ta, tb, tsa, tsb, to, gs_x, gs_w, (int)M, (int)N, (int)K,
-                            bt, d.err, inject);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, qqmm_pair_kernel<MODE, false>, ta, tb, tsa, tsb, to, gs_x, gs_w, (int)M, (int)N,
+                            (int)K, bt, d.err, inject, FusedX{});
 }
 
 // Workspace of a fused call: [codes | tiled scales | per-CTA partial maxima |
@@ -984,6 +1001,37 @@ cudaError_t launch_fused_mode(const DevInfo& d, const uint16_t* x, const float* 
   fx.bar = reinterpret_cast<unsigned*>(ws + L.bar);
   fx.padded_rows = (int)L.padded_rows;
   fx.padded_cols = (int)L.padded_cols;
+  const int np = pair_clusters<MODE>(d);
+  if (np > 0) {
+    // the CTA-pair kernel, cooperative (every CTA resident for the prologue's grid
+    // barriers) with clusters of two
+    using P = PairCfg<MODE>;
+    constexpr int group = MODE == 2 ? 16 : 32;
+    CUtensorMap ta, tb, tsa, tsb, to;
+    if (!make_code_map(&ta, fx.xq, M, K, 128, 1, 0) || !make_code_map(&tb, wq, N, K, 128, 1, 0) ||
+        !make_scale_map(&tsa, fx.sx, M, K, group, P::TPS, 1, 0) ||
+        !make_scale_map(&tsb, sw, N, K, group, P::TPS, 1, 0) || !make_out_map(&to, out, M, N, 1, 0))
+      return cudaErrorInvalidValue;
+    const int64_t tiles = ((N + BN - 1) / BN) * ((M + 255) / 256);
+    const int npairs = (int)std::min<int64_t>(std::min<int64_t>(tiles, np), 512);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * npairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = P::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, qqmm_pair_kernel<MODE, true>, ta, tb, tsa, tsb, to,
+                              (const float*)(MODE == 2 ? fx.gs_out : nullptr), gs_w, (int)M, (int)N, (int)K,
+                              Batch{}, d.err, inject, fx);
+  }
   CUtensorMap ta, tb;
   if (!make_code_map(&ta, fx.xq, M, K, BM, 1, 0) || !make_code_map(&tb, wq, N, K, BN, 1, 0))
     return cudaErrorInvalidValue;
