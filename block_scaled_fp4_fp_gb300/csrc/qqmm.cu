@@ -200,29 +200,87 @@ __device__ void grid_barrier(unsigned* bar, unsigned* err, bool& failed) {
   __syncthreads();
 }
 
+// 16 bytes from shared memory (32-bit shared address)
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// The fused activation quantize that runs before the GEMM in a cooperative
+// launch (all CTAs resident).  CTA b owns a contiguous share of x's scale
+// groups and moves it through the idle operand ring (`ring`, `ring_bytes`) in
+// NB chunks by bulk copies, so that a whole ring of bytes is in flight per SM:
+//   1. NVFP4 without a given activation scale: max |x| of the share from
+//      shared memory, one partial per CTA, a grid barrier, gs = amax / 2688
+//      ("NVFP4 and MXFP4 formats", the tensor-level scale);
+//   2. quantize every group of the share (the block-scale rule of the format,
+//      e2m1 rounding to nearest even) into codes and 128x4-tiled scales.
+// The chunks still in the ring after step 1 (all of them when the share fits)
+// are quantized first and are not read again from global memory.
 template <int MODE>
-__device__ void quantize_prologue(const FusedX& fx, int M, int K, unsigned* err, bool& failed) {
+__device__ void quantize_prologue(const FusedX& fx, int M, int K, uint8_t* ring, uint32_t ring_bytes,
+                                  unsigned* err, bool& failed) {
   constexpr int G = (MODE == 2) ? 16 : 32;
-  constexpr int NV = G / 8;
+  constexpr int GB = 2 * G;  // bytes of x per scale group
+  constexpr int NV = G / 8;  // 16-byte pieces per group
+  constexpr int NB = 4;      // chunk buffers
   __shared__ uint32_t red[kThreads / 32];
   __shared__ float gs_sh;
-  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  __shared__ uint64_t cbar[NB];
+  const int T = (int)blockDim.x;
+  const int scols = K / G;
+  const int64_t ngroups = (int64_t)M * scols;
+  const int64_t g_lo = ngroups * blockIdx.x / gridDim.x;
+  const int64_t share = ngroups * (blockIdx.x + 1) / gridDim.x - g_lo;
+  const int gpc = (int)(ring_bytes / NB / GB);  // groups per chunk
+  const uint32_t CH = (uint32_t)gpc * GB;
+  const int nchunks = (int)((share + gpc - 1) / gpc);
+  const uint8_t* xs = reinterpret_cast<const uint8_t*>(fx.x) + g_lo * GB;
+  const uint32_t ring_s = smem_u32(ring);
+  auto chunk_groups = [&](int j) { return (int)min((int64_t)gpc, share - (int64_t)j * gpc); };
+  auto issue = [&](int j, int b) {  // one thread: chunk j of the share into buffer b
+    const uint32_t bytes = (uint32_t)chunk_groups(j) * GB;
+    mbar_arrive_expect_tx(&cbar[b], bytes);
+    bulk_load(ring + (size_t)b * CH, xs + (int64_t)j * gpc * GB, bytes, &cbar[b]);
+  };
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NB; ++b) mbar_init(&cbar[b], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;  // bit b: parity of buffer b's next completion
   float gs = 1.0f;
+  int nres = 0;        // chunks left in the ring by the max pass
   if (MODE == 2 && fx.gs_in) {
     gs = __ldg(fx.gs_in);
   } else if (MODE == 2) {
     // tensor amax over bf16 magnitude bits (their unsigned order is |x|'s order)
-    const int64_t nvec = (int64_t)M * K / 8;
-    const uint4* xv = reinterpret_cast<const uint4*>(fx.x);
+    if (threadIdx.x == 0)
+      for (int j = 0; j < min(NB, nchunks); ++j) issue(j, j);
     uint32_t m = 0;
-    int64_t i = tid;
-    for (; i + 3 * nthreads < nvec; i += 4 * nthreads) {  // four 16-byte loads in flight per thread
-      const uint4 a = ld_stream_v4(xv + i), b = ld_stream_v4(xv + i + nthreads);
-      const uint4 c = ld_stream_v4(xv + i + 2 * nthreads), e = ld_stream_v4(xv + i + 3 * nthreads);
-      m = max(max(m, max(max_mag8(a), max_mag8(b))), max(max_mag8(c), max_mag8(e)));
+    for (int j = 0; j < nchunks; ++j) {
+      const int b = j % NB;
+      mbar_wait(&cbar[b], (phase >> b) & 1u, err, failed);
+      phase ^= 1u << b;
+      const uint32_t src = ring_s + (uint32_t)b * CH;
+      const int nv = chunk_groups(j) * NV;
+      int i = threadIdx.x;
+      for (; i + 3 * T < nv; i += 4 * T) {  // four independent loads per round
+        uint4 a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = lds_v4(src + 16u * (uint32_t)(i + u * T));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m = max(m, max_mag8(a[u]));
+      }
+      for (; i < nv; i += T) m = max(m, max_mag8(lds_v4(src + 16u * (uint32_t)i)));
+      if (j + NB < nchunks) {
+        __syncthreads();  // buffer b read by every thread
+        if (threadIdx.x == 0) issue(j + NB, b);
+      }
     }
-    for (; i < nvec; i += nthreads) m = max(m, max_mag8(ld_stream_v4(xv + i)));
+    nres = min(NB, nchunks);
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -231,9 +289,14 @@ __device__ void quantize_prologue(const FusedX& fx, int M, int K, unsigned* err,
       fx.partials[blockIdx.x] = m;
     }
     grid_barrier(fx.bar, err, failed);
+    // every thread reads its share of the per-CTA maxima (one L2 round trip, not gridDim.x)
+    uint32_t a = 0;
+    for (unsigned b = threadIdx.x; b < gridDim.x; b += blockDim.x) a = max(a, __ldcg(fx.partials + b));
+    for (int o = 16; o > 0; o >>= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+    __syncthreads();
     if (threadIdx.x == 0) {
-      uint32_t a = 0;
-      for (unsigned b = 0; b < gridDim.x; ++b) a = max(a, __ldcg(fx.partials + b));
+      for (int w = 1; w < kThreads / 32; ++w) a = max(a, red[w]);
       gs_sh = __fdiv_rn(__uint_as_float(a << 16), 2688.0f);
       if (blockIdx.x == 0) {
         *fx.gs_out = gs_sh;
@@ -243,61 +306,102 @@ __device__ void quantize_prologue(const FusedX& fx, int M, int K, unsigned* err,
     __syncthreads();
     gs = gs_sh;
   }
-  if (MODE == 2 && fx.gs_in && tid == 0) {
+  if (MODE == 2 && fx.gs_in && blockIdx.x == 0 && threadIdx.x == 0) {
     *fx.gs_out = gs;
     if (fx.gs_user) *fx.gs_user = gs;
   }
-  // quantize: one thread per block-scale group, scales straight into their tiles
-  const int scols = K / G;
-  const int64_t ngroups = (int64_t)M * scols;
-  constexpr int U = (MODE == 2) ? 4 : 2;  // groups per thread per round: 8 loads in flight
-  for (int64_t g0 = tid; g0 < ngroups; g0 += U * nthreads) {
-    uint4 v[U][NV];
+  // quantize: one thread per group.  A thread reads its group's 16-byte pieces
+  // in an order rotated by its lane so that eight neighbouring threads' reads
+  // fall in distinct shared-memory banks.
+  constexpr int U = (MODE == 2) ? 4 : 2;
+  const int dr = T / scols, dc = T % scols;
+  const uint32_t rot = (MODE == 2) ? ((threadIdx.x >> 2) & 1u) : ((threadIdx.x >> 1) & 3u);
+  const int base = nres > 0 ? (nchunks - nres) % NB : 0;
+  if (threadIdx.x == 0 && nres == 0)
+    for (int p = 0; p < min(NB, nchunks); ++p) issue(p, p);
+  for (int p = 0; p < nchunks; ++p) {
+    // the chunks left by the max pass come first, then the share from its start
+    const int b = (base + p) % NB;
+    const int j = p < nres ? nchunks - nres + p : p - nres;
+    if (p >= nres) {
+      mbar_wait(&cbar[b], (phase >> b) & 1u, err, failed);
+      phase ^= 1u << b;
+    }
+    const int cnt = chunk_groups(j);
+    const int64_t g0 = g_lo + (int64_t)j * gpc + threadIdx.x;
+    int r = (int)(g0 / scols), c = (int)(g0 % scols);
+    const uint32_t src = ring_s + (uint32_t)b * CH;
+    for (int l0 = threadIdx.x; l0 < cnt; l0 += U * T) {
+      // U independent groups per round (l0 + u T), for instruction-level parallelism
+      uint4 v[U][NV];
+      int rr[U], cc[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t gi = g0 + u * nthreads;
-      if (gi < ngroups) {
-        const int r = (int)(gi / scols), c = (int)(gi - (int64_t)r * scols);
-        const uint4* src = reinterpret_cast<const uint4*>(fx.x + (int64_t)r * K + (int64_t)c * G);
+      for (int u = 0; u < U; ++u) {
+        rr[u] = r;
+        cc[u] = c;
+        c += dc;
+        r += dr;
+        if (c >= scols) {
+          c -= scols;
+          ++r;
+        }
+        if (l0 + u * T < cnt) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i) v[u][i] = ld_stream_v4(src + i);
+          for (int k = 0; k < NV; ++k)
+            v[u][k] = lds_v4(src + (uint32_t)(l0 + u * T) * GB + 16u * ((k + rot) & (NV - 1)));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (l0 + u * T >= cnt) continue;
+        uint32_t mb = 0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) mb = max(mb, max_mag8(v[u][k]));
+        float mul, sval;
+        uint32_t sbyte;
+        block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
+        uint32_t w[NV];
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          const uint32_t wv[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
+          uint32_t word = 0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[q]), mul), __fmul_rn(bf16_hi(wv[q]), mul)) << (8 * q);
+          w[k] = word;
+        }
+        // piece i's codes are w[(i - rot) mod NV]
+        uint32_t* dst = fx.xq + (int64_t)rr[u] * (K / 8) + (int64_t)cc[u] * NV;
+        if constexpr (NV == 2) {
+          *reinterpret_cast<uint2*>(dst) = rot ? make_uint2(w[1], w[0]) : make_uint2(w[0], w[1]);
+        } else {
+          uint32_t a[4], o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a[i] = (rot & 1u) ? w[(i + 3) & 3] : w[i];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = (rot & 2u) ? a[(i + 2) & 3] : a[i];
+          *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fx.sx[tiled_scale_offset(rr[u], cc[u], fx.padded_cols)] = (uint8_t)sbyte;
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t gi = g0 + u * nthreads;
-      if (gi >= ngroups) break;
-      const int r = (int)(gi / scols), c = (int)(gi - (int64_t)r * scols);
-      uint32_t mb = 0;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) mb = max(mb, max_mag8(v[u][i]));
-      float mul, sval;
-      uint32_t sbyte;
-      block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
-      uint32_t words[NV];
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const uint32_t wv[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
-        uint32_t word = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
-        words[i] = word;
-      }
-      uint32_t* dst = fx.xq + (int64_t)r * (K / 8) + (int64_t)c * NV;
-      if (NV == 2) *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
-      fx.sx[tiled_scale_offset(r, c, fx.padded_cols)] = (uint8_t)sbyte;
+    if (p + NB < nchunks) {
+      __syncthreads();  // buffer b read by every thread
+      if (threadIdx.x == 0) issue(p + NB - nres, b);
     }
   }
   // the padding rows of the scale tiles are zero
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t pad = (int64_t)(fx.padded_rows - M) * fx.padded_cols;
   for (int64_t i = tid; i < pad; i += nthreads) {
     const int r = M + (int)(i / fx.padded_cols), c = (int)(i % fx.padded_cols);
     fx.sx[tiled_scale_offset(r, c, fx.padded_cols)] = 0;
   }
-  // generic-proxy writes, read next by TMA and bulk copies (async proxy) in other CTAs
+  // generic-proxy writes, read next by TMA and bulk copies (async proxy) in
+  // other CTAs; the ring, read here, is written next by the GEMM's TMA loads
   asm volatile("fence.proxy.async.global;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   grid_barrier(fx.bar, err, failed);
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -351,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool failed = false;  // this thread gave up a wait (see mbar_wait)
-  if (FQ) quantize_prologue<MODE>(fx, M, K, err, failed);
+  if (FQ) quantize_prologue<MODE>(fx, M, K, smem, STAGES * C::STAGE_BYTES, err, failed);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -654,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_pair_kernel(
   // kernel's tail; x, its scales and the global scales may come from it
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (FQ) quantize_prologue<MODE>(fx, M, K, err, failed);  // x -> codes and tiled scales in the workspace
+  if (FQ)  // x -> codes and tiled scales in the workspace, through the idle operand ring
+    quantize_prologue<MODE>(fx, M, K, smem, kPairStages * P::STAGE_BYTES, err, failed);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
