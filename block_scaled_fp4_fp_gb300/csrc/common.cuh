@@ -112,13 +112,55 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t byte) { return exp2i_f32((
 //     b = 0), mul = 1 / fl(s8 gs) (0 when that product is 0).
 //   MXFP4 (MODE 1, E8M0 per 32): se = clamp(floor(log2 b) - 2, -127, 127) (-127 when
 //     b = 0), byte = se + 127, mul = 2^-se.
+//
+// The NVFP4 division b / fl(6 gs) has one divisor per tensor, so its
+// correctly rounded reciprocal r = 1/p is formed once (Nvfp4Div) and each block
+// divides by Markstein's correction: q0 = fl(b r), e = b - q0 p (exact by
+// FMA), q = fl(q0 + e r), which is fl(b / p) when p, 1/p and b are normal
+// enough that e does not underflow (b >= 2^-100) and q0 lies in [2^-64, 1024).
+// Outside that range q0 itself is returned: the block scale is only its e4m3
+// rounding, which saturates at 448 above 1024 and is 0 below 2^-10.  Checked
+// exhaustively on the CPU against correctly rounded division for every pair of
+// bf16 amax (gs = fl(amax / 2688)) and bf16 block maximum b <= amax, and for
+// every bf16 b against 20,000 random normal divisors (a quarter of them with an
+// all-ones mantissa): every e4m3 result agrees.
+struct Nvfp4Div {
+  float p, r;
+  bool fast;
+};
+
+__device__ __forceinline__ Nvfp4Div nvfp4_div(float gs) {
+  Nvfp4Div d;
+  d.p = __fmul_rn(6.0f, gs);
+  d.r = __frcp_rn(d.p);
+  d.fast = d.p >= 0x1p-126f && d.p < 0x1p126f;  // p and 1/p normal
+  return d;
+}
+
+__device__ __forceinline__ float nvfp4_block_div(float b, const Nvfp4Div& d) {
+  if (!d.fast || b < 0x1p-100f) return __fdiv_rn(b, d.p);
+  const float q0 = __fmul_rn(b, d.r);
+  if (!(q0 < 1024.0f) || q0 < 0x1p-64f) return q0;
+  return __fmaf_rn(__fmaf_rn(-q0, d.p, b), d.r, q0);
+}
+
+// Two round-to-nearest fp32 products in one packed instruction (each lane is
+// an IEEE multiply, the same as __fmul_rn).
+__device__ __forceinline__ void fmul2_rn(float a0, float a1, float m, float& r0, float& r1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(m));
+}
+
 template <int MODE>
-__device__ __forceinline__ void block_scale_rule(uint32_t mb, float gs, float& mul, uint32_t& sbyte,
-                                                 float& sval) {
+__device__ __forceinline__ void block_scale_rule(uint32_t mb, float gs, const Nvfp4Div& dv, float& mul,
+                                                 uint32_t& sbyte, float& sval) {
   if (MODE == 2) {
     const float b = __uint_as_float(mb << 16);
-    const float p = __fmul_rn(6.0f, gs);
-    const float sc = (b == 0.0f) ? 0.0f : __fdiv_rn(b, p);
+    const float sc = (b == 0.0f) ? 0.0f : nvfp4_block_div(b, dv);
     sbyte = e4m3_rn(sc);
     sval = e4m3_to_f32(sbyte);
     const float dd = __fmul_rn(sval, gs);
@@ -134,6 +176,12 @@ __device__ __forceinline__ void block_scale_rule(uint32_t mb, float gs, float& m
     mul = exp2i_f32(-se);
     sval = exp2i_f32(se);
   }
+}
+
+template <int MODE>
+__device__ __forceinline__ void block_scale_rule(uint32_t mb, float gs, float& mul, uint32_t& sbyte,
+                                                 float& sval) {
+  block_scale_rule<MODE>(mb, gs, nvfp4_div(gs), mul, sbyte, sval);
 }
 
 // Largest bf16 magnitude (bits) of the eight values of a 16-byte piece.

@@ -133,7 +133,7 @@ __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
 }
 
 template <int MODE, bool SR>
-__device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 4], float gs,
+__device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 4], float gs, const Nvfp4Div& dv,
                                                uint32_t* __restrict__ xq_words,
                                                uint8_t* __restrict__ scale_byte, uint64_t e0,
                                                uint64_t seed, uint64_t offset) {
@@ -149,7 +149,7 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
   const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
   float mul, sval;
   uint32_t sbyte;
-  block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
+  block_scale_rule<MODE>(mb, gs, dv, mul, sbyte, sval);
   uint32_t out[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -164,8 +164,11 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
                  (e2m1_sr(__fmul_rn(bf16_hi(wv[j]), mul), u[2 * j + 1]) << 4)) << (8 * j);
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[j]), mul), __fmul_rn(bf16_hi(wv[j]), mul)) << (8 * j);
+      for (int j = 0; j < 4; ++j) {
+        float lo, hi;
+        fmul2_rn(bf16_lo(wv[j]), bf16_hi(wv[j]), mul, lo, hi);
+        word |= e2m1x2_rn(lo, hi) << (8 * j);
+      }
     }
     out[i] = word;
   }
@@ -177,33 +180,15 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
   *scale_byte = (uint8_t)sbyte;
 }
 
+// Linear scales: thread gi of the row quantizes group gi of RT rows (r, r + gy, ...).
 template <int MODE, bool SR>
 __global__ void __launch_bounds__(kQThreads) quantize_kernel(
     const uint16_t* __restrict__ x, int rows, int cols, const float* __restrict__ gs_ptr,
-    uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, int tiled, int padded_rows,
-    int padded_cols, int main_bx, uint64_t seed, uint64_t offset) {
+    uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, uint64_t seed, uint64_t offset) {
   constexpr int G = (MODE == 2) ? 16 : 32;
   constexpr int NV = G / 8;
-  constexpr int RT = (MODE == 2) ? 4 : 2;  // rows in flight per thread (64 or 128 bytes... 128 bytes)
+  constexpr int RT = (MODE == 2) ? 4 : 2;  // rows in flight per thread: 128 bytes of loads
   const int scols = cols / G;
-  if ((int)blockIdx.x >= main_bx) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel may still use the buffer
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // zero the padding bytes of the tiled scale buffer
-    const int64_t total = (int64_t)padded_rows * padded_cols;
-    const int64_t nthreads = (int64_t)(gridDim.x - main_bx) * gridDim.y * blockDim.x;
-    const int64_t first = ((int64_t)blockIdx.y * (gridDim.x - main_bx) + (blockIdx.x - main_bx)) * blockDim.x +
-                          threadIdx.x;
-    const int tiles_per_row = padded_cols >> 2;
-    for (int64_t off = first; off < total; off += nthreads) {
-      const int64_t tile = off >> 9;
-      const int within = (int)(off & 511);
-      const int r = (int)(tile / tiles_per_row) * 128 + (within >> 4) + ((within & 15) >> 2) * 32;
-      const int c = (int)(tile % tiles_per_row) * 4 + (within & 3);
-      if (r >= rows || c >= scols) scales[off] = 0;
-    }
-    return;
-  }
   // programmatic dependent launch: this grid may start while the previous
   // kernel drains; x and the global scale are read only after it completed
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -211,6 +196,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(
   const int gi = blockIdx.x * blockDim.x + threadIdx.x;  // group within the row
   if (gi >= scols) return;
   const float gs = (MODE == 2 && gs_ptr) ? __ldg(gs_ptr) : 1.0f;
+  const Nvfp4Div dv = nvfp4_div(gs);  // the block-scale divisor's reciprocal, once per thread
   const int wpr = cols >> 3;  // code words per row
   const int gy = gridDim.y;
   for (int r = blockIdx.y; r < rows; r += RT * gy) {
@@ -228,9 +214,130 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(
     for (int k = 0; k < RT; ++k) {
       const int rk = r + k * gy;
       if (rk < rows)
-        quantize_group<MODE, SR>(a[k], gs, xq + (int64_t)rk * wpr + gi * NV,
-                                 scales + (tiled ? tiled_scale_offset(rk, gi, padded_cols) : (int64_t)rk * scols + gi),
+        quantize_group<MODE, SR>(a[k], gs, dv, xq + (int64_t)rk * wpr + gi * NV, scales + (int64_t)rk * scols + gi,
                                  (uint64_t)rk * (uint64_t)cols + (uint64_t)gi * G, seed, offset);
+    }
+  }
+}
+
+// 128x4-tiled scales.  A block owns one tile column (groups 4 tc .. 4 tc + 3)
+// of part of a 128-row tile: lane t of warp w in row batch b quantizes group
+// 4 tc + t % 4 of row 128 tr + 32 q + rr, with q = (t / 4) % 4, rr = 2 slot +
+// t / 16 and slot = part * 2 RT + w RT + b.  Within the tile that scale byte
+// sits at rr * 16 + q * 4 + t % 4 = 32 slot + t, so one warp's 32 scale bytes
+// of a batch are one 32-byte run, and each of its 8 rows reads 4 neighbouring
+// groups of x.  The grid covers the padded buffer: rows past `rows` and groups
+// past cols / G get zero bytes, so no other pass touches the padding.
+template <int MODE, bool SR>
+__global__ void __launch_bounds__(kQThreads) quantize_tiled_kernel(
+    const uint16_t* __restrict__ x, int rows, int cols, const float* __restrict__ gs_ptr,
+    uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, int padded_cols, int ntr, uint64_t seed,
+    uint64_t offset) {
+  constexpr int G = (MODE == 2) ? 16 : 32;
+  constexpr int NV = G / 8;
+  constexpr int RT = (MODE == 2) ? 4 : 2;         // row batches in flight per thread: 128 bytes of loads
+  constexpr int BPT = 32 / (4 * RT);              // blocks per 128-row tile (NVFP4 2, MXFP4 4)
+  static_assert(kQThreads == 64, "two warps per block");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int scols = cols / G;
+  const int t = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = (int)blockIdx.x * 4 + (t & 3);
+  const int q = (t >> 2) & 3, hh = t >> 4;
+  const int part = (int)(blockIdx.y % BPT);
+  const float gs = (MODE == 2 && gs_ptr) ? __ldg(gs_ptr) : 1.0f;
+  const Nvfp4Div dv = nvfp4_div(gs);
+  const int wpr = cols >> 3;
+  const int64_t tiles_per_row = padded_cols >> 2;
+  for (int tr = (int)(blockIdx.y / BPT); tr < ntr; tr += (int)(gridDim.y / BPT)) {
+    uint8_t* tile = scales + ((int64_t)tr * tiles_per_row + blockIdx.x) * 512;
+    uint4 a[RT][NV];
+#pragma unroll
+    for (int b = 0; b < RT; ++b) {
+      const int r = tr * 128 + 32 * q + 2 * (part * 2 * RT + w * RT + b) + hh;
+      if (r < rows && c < scols) {
+        const uint4* pa = reinterpret_cast<const uint4*>(x + (int64_t)r * cols + (int64_t)c * G);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) a[b][i] = ld_stream_v4(pa + i);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < RT; ++b) {
+      const int slot = part * 2 * RT + w * RT + b;
+      const int r = tr * 128 + 32 * q + 2 * slot + hh;
+      uint8_t* sb = tile + 32 * slot + t;
+      if (r < rows && c < scols)
+        quantize_group<MODE, SR>(a[b], gs, dv, xq + (int64_t)r * wpr + (int64_t)c * NV, sb,
+                                 (uint64_t)r * (uint64_t)cols + (uint64_t)c * G, seed, offset);
+      else
+        *sb = 0;
+    }
+  }
+}
+
+// NVFP4 with 128x4-tiled scales.  Thread c of the row (a warp: 32 neighbouring
+// groups, 1 KB of x per row) quantizes group c of the four rows 128 tr + rr +
+// 32 q, q = 0..3, of one tile row: its four scale bytes are byte q*4 + c%4 of
+// the 16-byte run rr*16 of tile (tr, c/4).  The four lanes of a tile column
+// exchange them (a 4 x 4 byte transpose by shuffles) so that lane c writes the
+// aligned word for q = c%4: one 4-byte store per lane instead of four bytes.
+// The grid covers the padded buffer (zero bytes past `rows` and cols / 16).
+template <bool SR>
+__global__ void __launch_bounds__(kQThreads) quantize_nvfp4_tiled_kernel(
+    const uint16_t* __restrict__ x, int rows, int cols, const float* __restrict__ gs_ptr,
+    uint32_t* __restrict__ xq, uint8_t* __restrict__ scales, int padded_cols, int ntr, uint64_t seed,
+    uint64_t offset) {
+  constexpr int G = 16, NV = 2;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int scols = cols / G;
+  const int c = (int)blockIdx.x * kQThreads + (int)threadIdx.x;
+  const bool in_cols = c < scols, in_tiles = c < padded_cols;  // (uniform per 4-lane group)
+  const int rr = (int)(blockIdx.y & 31u);
+  const int lane = (int)(threadIdx.x & 31u), m = lane & 3;
+  const float gs = gs_ptr ? __ldg(gs_ptr) : 1.0f;
+  const Nvfp4Div dv = nvfp4_div(gs);
+  const int wpr = cols >> 3;
+  const int64_t tiles_per_row = padded_cols >> 2;
+  const bool words_ok = (reinterpret_cast<uintptr_t>(scales) & 3u) == 0;
+  for (int tr = (int)(blockIdx.y >> 5); tr < ntr; tr += (int)(gridDim.y >> 5)) {
+    uint4 a[4][NV];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = tr * 128 + 32 * q + rr;
+      if (r < rows && in_cols) {
+        const uint4* pa = reinterpret_cast<const uint4*>(x + (int64_t)r * cols + (int64_t)c * G);
+        a[q][0] = ld_stream_v4(pa);
+        a[q][1] = ld_stream_v4(pa + 1);
+      }
+    }
+    uint32_t packed = 0;  // byte q: this group's scale byte in row quadrant q
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = tr * 128 + 32 * q + rr;
+      uint8_t sb = 0;
+      if (r < rows && in_cols)
+        quantize_group<2, SR>(a[q], gs, dv, xq + (int64_t)r * wpr + (int64_t)c * NV, &sb,
+                              (uint64_t)r * (uint64_t)cols + (uint64_t)c * G, seed, offset);
+      packed |= (uint32_t)sb << (8 * q);
+    }
+    // lane 4k + m collects byte m of its four neighbours' words (columns 4k .. 4k + 3)
+    const int base = lane & ~3;
+    const uint32_t v0 = __shfl_sync(0xffffffffu, packed, base);
+    const uint32_t v1 = __shfl_sync(0xffffffffu, packed, base + 1);
+    const uint32_t v2 = __shfl_sync(0xffffffffu, packed, base + 2);
+    const uint32_t v3 = __shfl_sync(0xffffffffu, packed, base + 3);
+    const uint32_t lo = __byte_perm(v0, v1, (uint32_t)(m | ((m + 4) << 4)));
+    const uint32_t hi = __byte_perm(v2, v3, (uint32_t)(m | ((m + 4) << 4)));
+    const uint32_t word = __byte_perm(lo, hi, 0x5410u);
+    if (in_tiles) {
+      uint8_t* dst = scales + ((int64_t)tr * tiles_per_row + (c >> 2)) * 512 + rr * 16 + m * 4;
+      if (words_ok) {
+        *reinterpret_cast<uint32_t*>(dst) = word;
+      } else {  // a scale buffer that is not 4-byte aligned (uniform per launch)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = (uint8_t)(word >> (8 * k));
+      }
     }
   }
 }
@@ -311,21 +418,7 @@ cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, i
                             int tiled, int sr, uint64_t seed, uint64_t offset, cudaStream_t s) {
   (void)d;
   const int64_t scols = cols / group;
-  const int64_t main_bx = (scols + kQThreads - 1) / kQThreads;
-  const int64_t prow = ((rows + 127) / 128) * 128, pcol = ((scols + 3) / 4) * 4;
-  // one batch of rows per thread (4 NVFP4 rows, 2 MXFP4 rows: 128 bytes of
-  // loads in flight) and as many short-lived blocks as that takes -- measured
-  // faster on this stream than fewer, longer-lived threads with software
-  // pipelining; the loop strides over the rest only past 65535 row batches
-  const int64_t rt = (mode == 2) ? 4 : 2;
-  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>((rows + rt - 1) / rt, 65535));
-  int64_t pad_bx = 0;
-  if (tiled && (prow != rows || pcol != scols)) {
-    const int64_t pad = prow * pcol;
-    pad_bx = std::min<int64_t>(std::max<int64_t>((pad + kQThreads * gy - 1) / (kQThreads * gy), 1), 64);
-  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(main_bx + pad_bx), (unsigned)gy);
   cfg.blockDim = dim3(kQThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -333,19 +426,42 @@ cudaError_t launch_quantize(const DevInfo& d, const uint16_t* x, int64_t rows, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int r = (int)rows, c = (int)cols, pr = (int)prow, pc = (int)pcol, mb = (int)main_bx;
-  if (mode == 2 && sr)
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<2, true>, x, r, c, gs, xq, scales, tiled, pr, pc, mb, seed, offset);
+  const int r = (int)rows, c = (int)cols;
+  const float* g = (mode == 2) ? gs : nullptr;
+  if (tiled) {
+    // one block per (tile column, part of a 128-row tile); the loop strides over
+    // tile rows only past 65535 blocks in y
+    const int64_t pcol = ((scols + 3) / 4) * 4, ntr = (rows + 127) / 128;
+    const int64_t bpt = (mode == 2) ? 2 : 4;
+    const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(ntr, 65535 / bpt)) * bpt;
+    cfg.gridDim = dim3((unsigned)(pcol / 4), (unsigned)gy);
+    const int pc = (int)pcol, nt = (int)ntr;
+    if (mode == 2) {
+      // one thread per group of a row, 32 rows (one per tile-row offset) per tile row in y
+      const int64_t gy2 = std::max<int64_t>(1, std::min<int64_t>(ntr, 65535 / 32)) * 32;
+      cfg.gridDim = dim3((unsigned)((pcol + kQThreads - 1) / kQThreads), (unsigned)gy2);
+      return sr ? cudaLaunchKernelEx(&cfg, quantize_nvfp4_tiled_kernel<true>, x, r, c, g, xq, scales, pc, nt, seed,
+                                     offset)
+                : cudaLaunchKernelEx(&cfg, quantize_nvfp4_tiled_kernel<false>, x, r, c, g, xq, scales, pc, nt,
+                                     (uint64_t)0, (uint64_t)0);
+    }
+    return sr ? cudaLaunchKernelEx(&cfg, quantize_tiled_kernel<1, true>, x, r, c, g, xq, scales, pc, nt, seed, offset)
+              : cudaLaunchKernelEx(&cfg, quantize_tiled_kernel<1, false>, x, r, c, g, xq, scales, pc, nt,
+                                   (uint64_t)0, (uint64_t)0);
+  }
+  // one batch of rows per thread (4 NVFP4 rows, 2 MXFP4 rows: 128 bytes of
+  // loads in flight) and as many short-lived blocks as that takes -- measured
+  // faster on this stream than fewer, longer-lived threads with software
+  // pipelining; the loop strides over the rest only past 65535 row batches
+  const int64_t rt = (mode == 2) ? 4 : 2;
+  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>((rows + rt - 1) / rt, 65535));
+  cfg.gridDim = dim3((unsigned)((scols + kQThreads - 1) / kQThreads), (unsigned)gy);
   if (mode == 2)
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<2, false>, x, r, c, gs, xq, scales, tiled, pr, pc, mb,
-                              (uint64_t)0, (uint64_t)0);
-  if (sr)
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<1, true>, x, r, c, (const float*)nullptr, xq, scales, tiled, pr,
-                              pc, mb, seed, offset);
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<1, false>, x, r, c, (const float*)nullptr, xq, scales, tiled, pr,
-                            pc, mb, (uint64_t)0, (uint64_t)0);
+    return sr ? cudaLaunchKernelEx(&cfg, quantize_kernel<2, true>, x, r, c, g, xq, scales, seed, offset)
+              : cudaLaunchKernelEx(&cfg, quantize_kernel<2, false>, x, r, c, g, xq, scales, (uint64_t)0, (uint64_t)0);
+  return sr ? cudaLaunchKernelEx(&cfg, quantize_kernel<1, true>, x, r, c, g, xq, scales, seed, offset)
+            : cudaLaunchKernelEx(&cfg, quantize_kernel<1, false>, x, r, c, g, xq, scales, (uint64_t)0, (uint64_t)0);
 }
-
 
 cudaError_t launch_dequantize(const DevInfo& d, const uint32_t* wq, const void* scales,
                               const uint16_t* biases, int64_t rows, int64_t cols, int mode,

@@ -149,3 +149,59 @@ def test_dequantize_bit_exact(B, mode, layout):
     out = B.fp4_dequantize(qd, sd, bd, mode=mode, global_scale=gsd, layout=layout, rows=rows)
     ref = oracle.dequantize_bf16(q, s, b, mode, {0: 64, 1: 32, 2: 16}[mode], gs)
     assert np.array_equal(bf16_u16(out), ref)
+
+
+def test_quantize_nvfp4_block_division_ranges(B):
+    """The NVFP4 block scale e4m3(fl(b / fl(6 gs))) on blocks whose maxima and
+    global scales reach every range of the division: a tensor so small that the
+    divisor is subnormal; blocks of maxima 1, 1e-6, 1e-25 (quotients far below
+    e4m3's range), 1e-31 (below 2^-100) and bf16 subnormals under one amax; and
+    static global scales log-uniform over 1e-38 .. 1e38 (quotients up to
+    saturation).  Codes and scales bit-exact against the oracle."""
+    rng = np.random.default_rng(7)
+    base = rng.standard_normal((8, 256)).astype(np.float32)
+    cases = []
+    cases.append((base * 1e-37, None))                      # amax ~ 1e-37: p = fl(6 gs) subnormal
+    mixed = base.copy()
+    for r, mag in enumerate([1.0, 1e-6, 1e-25, 1e-31, 1e-39, 3.0, 1e-12, 1e-20]):
+        mixed[r] *= mag
+    cases.append((mixed, None))
+    for e in rng.uniform(-38, 38, 40):
+        cases.append((base * float(rng.uniform(0.1, 10.0)), float(10.0 ** e)))
+    for vals, gs_static in cases:
+        x = torch.from_numpy(vals).to(torch.bfloat16)
+        xb = synth.to_u16(x)
+        if gs_static is None:
+            gsd = B.fp4_amax_global_scale(x.cuda())
+            gs = oracle.global_scale(xb)
+            assert float(gsd.item()) == float(np.float32(gs))
+        else:
+            gs = float(np.float32(gs_static))
+            gsd = torch.tensor(gs, dtype=torch.float32, device="cuda")
+        q, s = B.fp4_quantize(x.cuda(), 2, global_scale=gsd)
+        oq, os_ = oracle.quantize(xb, 2, gs)
+        assert np.array_equal(u32(q), oq), f"codes, gs={gs}"
+        assert np.array_equal(u8(s), os_), f"scales, gs={gs}"
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("rows,cols", [(130, 512), (257, 96), (1, 64)])
+def test_quantize_tiled_scales_unaligned_buffer(B, mode, rows, cols):
+    """Tiled scales into a buffer that starts one byte past an aligned address
+    (the NVFP4 kernel then stores bytes instead of words): the same codes and
+    scales as into an aligned buffer, and both equal the oracle's."""
+    if cols % (16 if mode == 2 else 32):
+        pytest.skip("cols not a multiple of the group")
+    x = _inputs("o", rows, cols, 21)
+    xb = synth.to_u16(x)
+    gsd = B.fp4_amax_global_scale(x.cuda()) if mode == 2 else None
+    gs = oracle.global_scale(xb) if mode == 2 else None
+    q, s = B.fp4_quantize(x.cuda(), mode, global_scale=gsd, layout=1)
+    raw = torch.full((s.numel() + 1,), 0xAB, dtype=torch.uint8, device="cuda")
+    s_odd = raw[1:].view(s.shape)
+    q2, _ = B.fp4_quantize(x.cuda(), mode, global_scale=gsd, layout=1, scales=s_odd)
+    oq, os_ = oracle.quantize(xb, mode, gs)
+    assert np.array_equal(u32(q), oq) and np.array_equal(u32(q2), oq)
+    assert np.array_equal(u8(s), oracle.tile_scales(os_))
+    assert np.array_equal(u8(s_odd), oracle.tile_scales(os_))
+    assert raw[0].item() == 0xAB  # nothing written before the buffer

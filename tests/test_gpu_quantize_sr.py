@@ -35,7 +35,8 @@ def test_quantize_sr_bit_exact(B, mode, use_gs, rows, cols, seed, offset):
     oq, os_ = oracle.quantize_sr(xb, mode, gs, seed=seed, offset=offset)
     assert np.array_equal(u32(q), oq)
     assert np.array_equal(u8(s), os_)
-    _, st = B.fp4_quantize_sr(x.cuda(), mode, seed, offset, global_scale=gsd, layout=B.SCALES_TILED)
+    qt, st = B.fp4_quantize_sr(x.cuda(), mode, seed, offset, global_scale=gsd, layout=B.SCALES_TILED)
+    assert np.array_equal(u32(qt), oq)
     assert np.array_equal(u8(st), oracle.tile_scales(os_))
 
 
