@@ -60,6 +60,23 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
   return r;
 }
 
+// Eight fp32 values -> eight e2m1 codes (round to nearest even, saturating),
+// code k in bits 4k .. 4k + 3: four converts whose bytes are packed by moves.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b16 h0, h1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b16 h0, {b0, b1};\n\t"
+      "mov.b16 h1, {b2, b3};\n\t"
+      "mov.b32 %0, {h0, h1};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
 // One byte of two e2m1 codes -> f16x2 (low code in the low half).
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t r;

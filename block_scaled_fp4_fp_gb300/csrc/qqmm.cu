@@ -314,6 +314,7 @@ __device__ void quantize_prologue(const FusedX& fx, int M, int K, uint8_t* ring,
   // in an order rotated by its lane so that eight neighbouring threads' reads
   // fall in distinct shared-memory banks.
   constexpr int U = (MODE == 2) ? 4 : 2;
+  const Nvfp4Div dv = nvfp4_div(gs);  // the block-scale divisor's reciprocal, once per thread
   const int dr = T / scols, dc = T % scols;
   const uint32_t rot = (MODE == 2) ? ((threadIdx.x >> 2) & 1u) : ((threadIdx.x >> 1) & 3u);
   const int base = nres > 0 ? (nchunks - nres) % NB : 0;
@@ -359,16 +360,15 @@ __device__ void quantize_prologue(const FusedX& fx, int M, int K, uint8_t* ring,
         for (int k = 0; k < NV; ++k) mb = max(mb, max_mag8(v[u][k]));
         float mul, sval;
         uint32_t sbyte;
-        block_scale_rule<MODE>(mb, gs, mul, sbyte, sval);
+        block_scale_rule<MODE>(mb, gs, dv, mul, sbyte, sval);
         uint32_t w[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
           const uint32_t wv[4] = {v[u][k].x, v[u][k].y, v[u][k].z, v[u][k].w};
-          uint32_t word = 0;
+          float f[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            word |= e2m1x2_rn(__fmul_rn(bf16_lo(wv[q]), mul), __fmul_rn(bf16_hi(wv[q]), mul)) << (8 * q);
-          w[k] = word;
+          for (int q = 0; q < 4; ++q) fmul2_rn(bf16_lo(wv[q]), bf16_hi(wv[q]), mul, f[2 * q], f[2 * q + 1]);
+          w[k] = e2m1x8_rn(f);
         }
         // piece i's codes are w[(i - rot) mod NV]
         uint32_t* dst = fx.xq + (int64_t)rr[u] * (K / 8) + (int64_t)cc[u] * NV;

@@ -163,12 +163,10 @@ __device__ __forceinline__ void quantize_group(const uint4 (&v)[MODE == 2 ? 2 : 
         word |= (e2m1_sr(__fmul_rn(bf16_lo(wv[j]), mul), u[2 * j]) |
                  (e2m1_sr(__fmul_rn(bf16_hi(wv[j]), mul), u[2 * j + 1]) << 4)) << (8 * j);
     } else {
+      float f[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float lo, hi;
-        fmul2_rn(bf16_lo(wv[j]), bf16_hi(wv[j]), mul, lo, hi);
-        word |= e2m1x2_rn(lo, hi) << (8 * j);
-      }
+      for (int j = 0; j < 4; ++j) fmul2_rn(bf16_lo(wv[j]), bf16_hi(wv[j]), mul, f[2 * j], f[2 * j + 1]);
+      word = e2m1x8_rn(f);
     }
     out[i] = word;
   }
