@@ -37,11 +37,13 @@
 //     swizzled shared-memory stage and TMA tensor stores.
 // Every mbarrier wait is bounded (an expired wait records FP4_ERR_TIMEOUT).
 #include <algorithm>
+#include <mutex>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "pair.cuh"
 
 namespace fp4 {
 
@@ -126,12 +128,13 @@ __device__ __forceinline__ uint32_t load_item_scale(const void* scales, const ui
   return (uint32_t)__ldg(static_cast<const uint16_t*>(scales) + gi) | ((uint32_t)__ldg(biases + gi) << 16);
 }
 
-// Dequantize one item (32 codes) into its 4 swizzled 16-byte chunks of each term.
-template <int MODE>
+// Dequantize one item (NW words: 8 NW codes of row n, item g of the stage row)
+// into its NW swizzled 16-byte chunks of each term.
+template <int MODE, int NW = 4>
 __device__ __forceinline__ void dequant_item(uint4 q, uint32_t sc, uint8_t* b_hi, uint8_t* b_lo, int n, int g) {
   const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < NW; ++j) {
     uint32_t hi[4], lo[4];
     if (MODE == 0) {
       const float s = bf16_lo(sc), b = bf16_hi(sc);
@@ -155,8 +158,8 @@ __device__ __forceinline__ void dequant_item(uint4 q, uint32_t sc, uint8_t* b_hi
         hi[bb] = pack_bf16x2_rn(__fmul_rn(f16_lo_to_f32(h2), scale), __fmul_rn(f16_hi_to_f32(h2), scale));
       }
     }
-    *reinterpret_cast<uint4*>(b_hi + sw128(n, g * 4 + j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    if (MODE == 0) *reinterpret_cast<uint4*>(b_lo + sw128(n, g * 4 + j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(b_hi + sw128(n, g * NW + j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    if (MODE == 0) *reinterpret_cast<uint4*>(b_lo + sw128(n, g * NW + j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -494,6 +497,237 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// qmm on CTA pairs (tcgen05 cta_group::2).  A cluster of two CTAs owns 512
+// rows x 256 columns of the output.  CTA r holds rows 128 r .. 128 r + 127 and
+// 256 + 128 r .. 256 + 128 r + 127 of the tile's activations (two TMA boxes per
+// stage) and dequantizes W rows n0 + 128 r .. n0 + 128 r + 127 (16 codes per
+// producer thread).  One thread of CTA 0 issues, per 16-element k-step and
+// weight term, two kind::f16 MMAs of M 256 (rows 0-255 and 256-511 of the
+// tile), each reading both CTAs' activation rows and both CTAs' halves of the
+// weight slice.  Each CTA accumulates its 2 x 128 rows x 256 columns in its own
+// tensor memory.  An SM so dequantizes half the weights the one-SM tile does
+// for the same MMA work.  Both CTAs' activation boxes complete on CTA 0's
+// stage barrier.  Producer warps arrive on their own CTA's barrier (a CTA-scope
+// release, which does not wait for their weight loads in flight); CTA 1's idle
+// MMA warp forwards each completed stage to CTA 0's barrier with one
+// cluster-scope arrival (a cluster-scope release by every producer warp stalled
+// on those loads: half the speed).  CTA 0's commits free a stage (and publish
+// the accumulators) in both CTAs.
+template <int MODE>
+struct PairQ {
+  static constexpr int kTerms = MODE == 0 ? 2 : 1;
+  static constexpr uint32_t kA = 2 * A_HALF;           // two 128-row blocks of x: 32 KB
+  static constexpr uint32_t kB = (BN / 2) * BK * 2;    // 128 W rows x 64 bf16: 16 KB per term
+  static constexpr uint32_t kStageBytes = kA + kTerms * kB;
+  static constexpr int kStages = MODE == 0 ? 3 : 4;    // 192 KB of stages: below the 196 KB carve-out
+  static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                    ((uint32_t)(256 >> 4) << 24);
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
+};
+constexpr int kPairRows = 512;  // output rows per CTA pair
+constexpr int kPairPD = 2;      // weight prefetch distance (stages) of the pair kernel's producers (4: no faster)
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) qmm_pair_kernel(
+    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO, int M,
+    const uint32_t* __restrict__ w, const void* __restrict__ scales, const uint16_t* __restrict__ biases,
+    const float* __restrict__ gs_w, int N, int K, int group, uint16_t* __restrict__ out,
+    unsigned* __restrict__ err, int inject_timeout) {
+  using P = PairQ<MODE>;
+  constexpr int STAGES = P::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * P::kStageBytes);
+  uint64_t* full = bars;                     // CTA 0's are used
+  uint64_t* empty = bars + STAGES;
+  uint64_t* accum_full = bars + 2 * STAGES;
+  uint64_t* never = bars + 2 * STAGES + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int n0 = (int)(blockIdx.x >> 1) * BN;
+  const int prow0 = (int)blockIdx.y * kPairRows;
+  const int num_kb = K / BK;
+  bool failed = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      // CTA 0: its producer warps, the byte count and CTA 1's forwarded stage; CTA 1: its producer warps
+      mbar_init(&full[s], rank == 0 ? kProducerWarps + 2 : kProducerWarps);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum_full, 1);
+    mbar_init(never, 1);
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarps) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  cluster_sync_all();  // both CTAs' barriers initialised and tensor memory allocated
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < kProducerWarps) {
+    // ---------------------------------------------------------- producers --
+    const int t = threadIdx.x;
+    const int n = t >> 2, g = t & 3;  // this thread's item: W row n of the CTA's 128, codes 16 g .. 16 g + 15
+    const int64_t wr = (int64_t)n0 + 128 * (int64_t)rank + n;
+    const bool nrow_ok = wr < N;
+    const uint32_t* wrow = w + wr * (K / 8);
+    const uint32_t full0 = mapa_u32(smem_u32(full), 0);  // CTA 0's stage barriers (8 bytes apart)
+    uint2 qr[kPairPD + 1];
+    uint32_t sr[kPairPD + 1];
+    auto load_w = [&](int kb, uint2& q, uint32_t& sc) {
+      if (nrow_ok) {
+        const int64_t k0 = (int64_t)kb * BK + g * 16;
+        q = __ldg(reinterpret_cast<const uint2*>(wrow + k0 / 8));
+        sc = (MODE == 2) ? (uint32_t)__ldg(static_cast<const uint8_t*>(scales) + wr * (K / 16) + k0 / 16)
+                         : load_item_scale<MODE>(scales, biases, wr, K, group, k0);
+      } else {
+        q = make_uint2(0u, 0u);
+        sc = 0;
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < kPairPD; ++u)
+      if (u < num_kb) load_w(u, qr[u], sr[u]);
+    for (int kb0 = 0; kb0 < num_kb; kb0 += kPairPD + 1) {
+#pragma unroll
+      for (int u = 0; u <= kPairPD; ++u) {
+        const int kb = kb0 + u;
+        if (kb < num_kb) {
+          if (kb + kPairPD < num_kb) load_w(kb + kPairPD, qr[(u + kPairPD) % (kPairPD + 1)], sr[(u + kPairPD) % (kPairPD + 1)]);
+          const int s = kb % STAGES, round = kb / STAGES;
+          if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, err, failed);
+          const uint32_t a_s = base + s * P::kStageBytes;
+          uint8_t* b_s = smem + s * P::kStageBytes + P::kA;
+          if (t == 0) {
+            // this CTA's two 128-row blocks of x (rows past M read as zeros), counted on CTA 0's barrier
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * P::kA);
+            tma2_load_2d(a_s, &tmX, full0 + 8 * s, kb * BK, prow0 + 128 * (int)rank);
+            tma2_load_2d(a_s + A_HALF, &tmX, full0 + 8 * s, kb * BK, prow0 + 256 + 128 * (int)rank);
+          }
+          dequant_item<MODE, 2>(make_uint4(qr[u].x, qr[u].y, 0u, 0u), sr[u], b_s, b_s + P::kB, n, g);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);  // this CTA's barrier
+        }
+      }
+    }
+  } else if (rank == 0) {
+    // ------------------------------------------------- MMA issuer (CTA 0) --
+    if (elect_one_sync()) {
+      if (inject_timeout) {
+        bool injected = false;  // separate flag: the injected expiry must not stop later waits
+        mbar_wait(never, 0, err, injected, 2000000LL);
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        mbar_wait_cluster(&full[s], (kb / STAGES) & 1, err, failed);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint64_t adesc = desc_sw128(base + s * P::kStageBytes);
+        const uint64_t bdesc = desc_sw128(base + s * P::kStageBytes + P::kA);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+#pragma unroll
+          for (int tt = 0; tt < P::kTerms; ++tt) {
+            const uint32_t acc = (kb > 0 || k > 0 || tt > 0) ? 1u : 0u;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)  // rows 256 hh .. 256 hh + 255 of the tile, accumulator hh
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                  :: "r"(tmem + (uint32_t)(BN * hh)), "l"(adesc + (uint64_t)(2 * k + (A_HALF >> 4) * hh)),
+                     "l"(bdesc + (uint64_t)(2 * k + (P::kB >> 4) * tt)), "r"(P::IDESC), "r"(acc)
+                  : "memory");
+          }
+        }
+        tc2_commit_both(&empty[s]);
+      }
+      tc2_commit_both(accum_full);
+    }
+  } else {
+    // ------------------------------------- CTA 1: forward completed stages --
+    if (elect_one_sync()) {
+      const uint32_t full0 = mapa_u32(smem_u32(full), 0);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        mbar_wait(&full[s], (kb / STAGES) & 1, err, failed);
+        mbar_arrive_cluster(full0 + 8 * s);
+      }
+    }
+  }
+
+  // -------------------------------------------------------------- epilogue --
+  // Warp (q, hh) of either CTA owns rows row_base + 32 q .. + 31, row_base =
+  // prow0 + 256 hh + 128 rank, of accumulator hh: as the one-SM kernel's
+  // epilogue (full 32-row bands by TMA stores through a swizzled 4 KB stage,
+  // the last partial band row by row).  The operand ring is idle in both CTAs
+  // once the final commit has arrived.
+  if (warp < 8) {
+    mbar_wait(accum_full, 0, err, failed);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const float gsw = (MODE == 2 && gs_w) ? __ldg(gs_w) : 1.0f;
+    const int q = warp & 3, hh = warp >> 2;
+    const int row_base = prow0 + 256 * hh + 128 * (int)rank;
+    const int rows = max(0, min(128, M - row_base));
+    const int rb = 32 * q;
+    const int r = rb + lane;
+    const bool full_band = rb + 32 <= rows;
+    uint8_t* stage_o = smem + warp * 8192;
+    uint16_t* orow = out + (int64_t)(row_base + r) * N;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 64) {
+      uint32_t v[64];
+      tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * hh + c), v);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      uint32_t o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        o[e] = pack_bf16x2_rn(__fmul_rn(__uint_as_float(v[2 * e]), gsw), __fmul_rn(__uint_as_float(v[2 * e + 1]), gsw));
+      const int col = n0 + c;
+      if (full_band) {
+        uint8_t* box = stage_o + ((c >> 6) & 1) * 4096;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+              make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          if (col < N)
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                         :: "l"(&tmO), "r"(col), "r"(row_base + rb), "r"(smem_u32(box)) : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");  // one group per box, even past N
+        }
+      } else if (r < rows) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (col + 8 * k < N)
+            *reinterpret_cast<uint4*>(orow + col + 8 * k) = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+      }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  cluster_sync_all();  // neither CTA frees its tensor memory or retires while the pair still uses them
+  if (warp == kProducerWarps) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 template <int MODE, bool DENSE>
 cudaError_t launch_w4a16(const DevInfo& d, const uint16_t* x, const int32_t* lhs, const int32_t* rhs, int64_t R,
                          const uint32_t* w, const void* scales, const uint16_t* biases, const float* gs_w, int64_t E,
@@ -530,6 +764,78 @@ cudaError_t launch_w4a16(const DevInfo& d, const uint16_t* x, const int32_t* lhs
                                                                    biases, gs_w, (int)E, (int)N, (int)K, group, out,
                                                                    d.err, inject);
   return cudaGetLastError();
+}
+
+// Clusters of two qmm_pair_kernel<MODE> CTAs that can be resident at once (0:
+// the pair kernel cannot run here and qmm takes the one-SM kernel).
+template <int MODE>
+int qmm_pair_clusters(const DevInfo& d) {
+  static std::mutex mu;
+  static int cache[64];
+  static bool have[64];
+  if (d.device < 0 || d.device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (have[d.device]) return cache[d.device];
+  int n = 0;
+  const int smem = (int)PairQ<MODE>::kSmemBytes;
+  if (smem <= d.smem_optin &&
+      cudaFuncSetAttribute(qmm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * std::max(1, d.sm_count / 2)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, qmm_pair_kernel<MODE>, &cfg) != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();
+    }
+  } else {
+    cudaGetLastError();
+  }
+  cache[d.device] = n;
+  have[d.device] = true;
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_qmm_pair(const DevInfo& d, const uint16_t* x, int64_t M, const uint32_t* w, const void* scales,
+                            const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int group,
+                            uint16_t* out, int inject, cudaStream_t s) {
+  using P = PairQ<MODE>;
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  auto map2d = [&](CUtensorMap* m, const void* p, int64_t inner, int64_t outer, uint32_t bi, uint32_t bo) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {bi, bo};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  CUtensorMap tmX, tmO;
+  // activations [M, K]: boxes of 128 rows x 64 elements; output [M, N]: stores of 32 rows x 64 columns
+  if (!map2d(&tmX, x, K, M, BK, BM) || !map2d(&tmO, out, N, M, 64, 32)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * ((N + BN - 1) / BN)), (unsigned)((M + kPairRows - 1) / kPairRows));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, qmm_pair_kernel<MODE>, tmX, tmO, (int)M, w, scales, biases, gs_w, (int)N, (int)K,
+                            group, out, d.err, inject);
 }
 
 // out[i, :] = x[idx[i], :]: one warp per row at a time, 16-byte pieces; an index
@@ -594,6 +900,14 @@ cudaError_t launch_gather_qmm(const DevInfo& d, const uint16_t* x, const int32_t
 cudaError_t launch_qmm(const DevInfo& d, const uint16_t* x, int64_t M, const uint32_t* w, const void* scales,
                        const uint16_t* biases, const float* gs_w, int64_t N, int64_t K, int mode, int group,
                        uint16_t* out, int inject_timeout, cudaStream_t s) {
+  // CTA pairs wherever a pair can be resident (512 x 256 tiles, each SM
+  // dequantizing 128 weight rows); the one-SM kernel otherwise
+  if (mode == 1 && qmm_pair_clusters<1>(d) > 0)
+    return launch_qmm_pair<1>(d, x, M, w, scales, biases, gs_w, N, K, group, out, inject_timeout, s);
+  if (mode == 2 && qmm_pair_clusters<2>(d) > 0)
+    return launch_qmm_pair<2>(d, x, M, w, scales, biases, gs_w, N, K, group, out, inject_timeout, s);
+  if (mode == 0 && qmm_pair_clusters<0>(d) > 0)
+    return launch_qmm_pair<0>(d, x, M, w, scales, biases, gs_w, N, K, group, out, inject_timeout, s);
   if (mode == 1)
     return launch_w4a16<1, true>(d, x, nullptr, nullptr, M, w, scales, biases, gs_w, 1, N, K, group, out,
                                  inject_timeout, s);

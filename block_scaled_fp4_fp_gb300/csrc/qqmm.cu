@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "pair.cuh"
 
 namespace fp4 {
 
@@ -622,46 +623,6 @@ struct PairCfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(caddr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-               "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(bar_addr), "r"(parity) : "memory");
-  return ok != 0;
-}
-// Bounded wait (as mbar_wait) on a barrier that other CTAs of the cluster arrive at.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, unsigned* err, bool& failed) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  if (failed) return false;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait_cluster(a, parity)) return true;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      record_error(err, kErrTimeout);
-      failed = true;
-      return false;
-    }
-  }
-}
 // TMA loads into this CTA's shared memory that complete on a barrier of either
 // CTA of the pair (`bar`: shared::cluster address).
 __device__ __forceinline__ void tma2_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z) {
@@ -676,11 +637,6 @@ __device__ __forceinline__ void tma2_load_4d(uint32_t dst, const void* tmap, uin
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%3, %4, %5, %6}], [%2];"
       :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
-__device__ __forceinline__ void tc2_commit_both(uint64_t* bar) {
-  const uint16_t mask = 0x3;
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(smem_u32(bar)), "h"(mask) : "memory");
 }
 __device__ __forceinline__ void tc2_cp_sf(uint32_t tmem, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(tmem), "l"(sdesc) : "memory");

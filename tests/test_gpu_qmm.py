@@ -38,8 +38,12 @@ def weights(mode, N, K, seed, group=None, use_gs=True):
 
 
 @pytest.mark.parametrize("mode,group", [(2, 16), (1, 32), (0, 64), (0, 32), (0, 128)])
-@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (100, 272, 512), (256, 256, 256), (300, 48, 1024), (129, 512, 64)])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (100, 272, 512), (256, 256, 256), (300, 48, 1024), (129, 512, 64),
+                                   (1000, 272, 512)])
 def test_qmm_small(B, mode, group, M, N, K):
+    """Ragged shapes: one row, rows ending inside the first or second 256-row
+    half of a 512-row tile (and a second tile ending inside its last quarter),
+    columns ending inside a 256-column slice, K of one 64-code stage."""
     if K % group:
         pytest.skip("K not a multiple of the group")
     (q, s, b, gs, g), (qd, sd, bd, gsd) = weights(mode, N, K, seed=M + N + K, group=group)
@@ -56,17 +60,18 @@ def test_qmm_nvfp4_without_global_scale(B):
     assert_close_to_oracle(out, oracle.qmm(synth.to_u16(x), q, s, None, 2, 16, None), "qmm nvfp4 no gs")
 
 
-@pytest.mark.parametrize("mode", [2, 0])
+@pytest.mark.parametrize("mode", [2, 1, 0])
 @pytest.mark.parametrize("M", [1024, 2048, 8192])
 def test_qmm_prefill_full_size_sampled(B, mode, M):
     """The prefill shapes M x 17408 x 5120 in the bench's launch configuration;
-    sampled rows (first and last of the matrix, tile boundaries, random), every
-    column."""
+    sampled rows (first and last of the matrix, the 128-row blocks of both CTAs
+    of a pair and both 256-row halves of a 512-row tile, random), every column."""
     N, K = 17408, 5120
     (q, s, b, gs, g), (qd, sd, bd, gsd) = weights(mode, N, K, seed=1)
     x = synth.bf16_normal((M, K), 1.0, seed=2)
     out = B.qmm(x.cuda(), qd, sd, bd, gsd, mode=mode)
-    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], np.random.default_rng(M).integers(0, M, 18)]))
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, 383, 384, 511, 512, M - 1],
+                                     np.random.default_rng(M).integers(0, M, 18)]))
     ref = oracle.qmm(synth.to_u16(x), q, s, b, mode, g, gs, rows=rows)
     assert_close_to_oracle(out[torch.from_numpy(rows).cuda()], ref, f"qmm mode {mode} M={M}")
 
@@ -90,3 +95,24 @@ def test_gather_qmm_nvfp4_and_affine_experts(B, mode):
                        torch.from_numpy(q3.view(np.int32)).cuda(), sd, bd, mode=mode, group_size=g)
     ref = oracle.gather_qmm(synth.to_u16(x), lhs, rhs, q3, s3, b3, mode, g)
     assert_close_to_oracle(out, ref, f"gather mode {mode}")
+
+
+def test_qmm_timeout_injection_reports_and_recovers(B):
+    """The MMA thread waits 1 ms on a barrier nothing arrives at: the call still
+    gives the right product and reports FP4_ERR_TIMEOUT; the next call reports
+    nothing."""
+    (q, s, b, gs, g), (qd, sd, bd, gsd) = weights(2, 272, 512, seed=5)
+    x = synth.bf16_normal((600, 512), 1.0, seed=6)
+    ref = oracle.qmm(synth.to_u16(x), q, s, b, 2, g, gs)
+    B.fp4_debug_inject_wait_timeout(True)
+    try:
+        out = B.qmm(x.cuda(), qd, sd, bd, gsd, mode=2)
+        torch.cuda.synchronize()
+        assert B.fp4_check_device_error() == B.FP4_ERR_TIMEOUT
+    finally:
+        B.fp4_debug_inject_wait_timeout(False)
+    assert_close_to_oracle(out, ref, "qmm after injected timeout")
+    out = B.qmm(x.cuda(), qd, sd, bd, gsd, mode=2)
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    assert_close_to_oracle(out, ref, "qmm after recovery")
