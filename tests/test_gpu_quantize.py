@@ -205,3 +205,18 @@ def test_quantize_tiled_scales_unaligned_buffer(B, mode, rows, cols):
     assert np.array_equal(u8(s), oracle.tile_scales(os_))
     assert np.array_equal(u8(s_odd), oracle.tile_scales(os_))
     assert raw[0].item() == 0xAB  # nothing written before the buffer
+
+
+@pytest.mark.parametrize("mode,rows,cols", [(2, 300_000, 32), (1, 2_200_000, 32), (2, 300_001, 16)])
+def test_quantize_tiled_scales_past_the_grid_height(B, mode, rows, cols):
+    """Tiled scales for more 128-row tiles than one grid column of blocks covers
+    (NVFP4 past 2047 tiles, MXFP4 past 16383): the kernel strides over tile rows.
+    Every code and scale (and the padding) bit-exact against the oracle."""
+    x = synth.bf16_normal((rows, cols), 1.0, seed=rows)
+    xb = synth.to_u16(x)
+    gsd = B.fp4_amax_global_scale(x.cuda()) if mode == 2 else None
+    gs = oracle.global_scale(xb) if mode == 2 else None
+    q, s = B.fp4_quantize(x.cuda(), mode, global_scale=gsd, layout=1)
+    oq, os_ = oracle.quantize(xb, mode, gs)
+    assert np.array_equal(u32(q), oq)
+    assert np.array_equal(u8(s), oracle.tile_scales(os_))
