@@ -311,8 +311,10 @@ def capture(fn, stream):
 
 
 # ------------------------------------------------------------------ components
-def bench_quantize(B, device, reps=50):
-    """Activation quantize 4096x5120 (0.1 % outliers x50), tiled scales; 4 rotating inputs."""
+def bench_quantize(B, device, reps=200, windows=3):
+    """Activation quantize 4096x5120 (0.1 % outliers x50), tiled scales; 4 rotating
+    inputs.  A launch takes ~10 us, so one short window is noisy (+-5 % between
+    windows): the median of `windows` windows of `reps` back-to-back launches."""
     xs = [synth.activations_with_outliers(4096, 5120, seed=i, outlier_seed=100 + i, device=device) for i in range(4)]
     res = {}
     for mode, name, sr in ((B.MODE_NVFP4, "nvfp4", False), (B.MODE_MXFP4, "mxfp4", False),
@@ -333,14 +335,17 @@ def bench_quantize(B, device, reps=50):
             call(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for r in range(reps):  # back-to-back launches over 4 rotating inputs (4 x 84 MB > L2)
-            call(r)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps if reps else float("nan")
+        per = []
+        for wdw in range(max(1, windows)):
+            e0.record()
+            for r in range(reps):  # back-to-back launches over 4 rotating inputs (4 x 84 MB > L2)
+                call(wdw * reps + r)
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) / reps if reps else float("nan"))
+        ms = statistics.median(per)
         nbytes = 4096 * 5120 * 2 + 4096 * 5120 // 2 + outs[0][1].numel()
-        res[name] = {"ms": ms, "GB/s": nbytes / ms / 1e6, "bytes": nbytes}
+        res[name] = {"ms": ms, "GB/s": nbytes / ms / 1e6, "bytes": nbytes, "windows_ms": per}
     return res
 
 
