@@ -85,11 +85,13 @@ __global__ void __launch_bounds__(kThreads) amax_final_kernel(const uint32_t* __
 
 // -------------------------------------------------------------- quantize --
 // One thread per block-scale group (16 or 32 bf16 = 2 or 4 16-byte loads), so
-// the scale arithmetic (one correctly rounded division and reciprocal for
-// NVFP4) runs once per group.  2-D grid: blockIdx.x/threadIdx.x pick the group
-// within a row, blockIdx.y strides over rows (two rows per thread in flight);
-// no index needs a division.  Codes leave as 8/16 contiguous bytes per thread.
-// Blocks with blockIdx.x >= main_bx zero the padding of a tiled scale buffer.
+// the scale arithmetic (NVFP4: the division by a per-launch reciprocal and one
+// correctly rounded reciprocal) runs once per group, for a batch of rows per
+// thread (128 bytes of loads in flight).  Linear scales: blockIdx.x and
+// threadIdx.x pick the group within a row, blockIdx.y strides over rows.
+// 128x4-tiled scales: the mappings of quantize_nvfp4_tiled_kernel and
+// quantize_tiled_kernel (below), which also write the tiles' zero padding.
+// Codes leave as 8 or 16 contiguous bytes per thread.
 // ------------------------------------------------- stochastic rounding --
 // Random words: element e (row-major index) takes word e % 4 of Philox4x32-10
 // (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3") at the 128-bit
