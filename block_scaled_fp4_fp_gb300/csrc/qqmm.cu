@@ -9,7 +9,7 @@
 // Design (GB300-native, not the pages' cuBLASLt call).  Two persistent,
 // warp-specialised kernels of 320 threads (warp 0 TMA producer, warp 1 tensor
 // memory and MMA issue, warps 2-9 epilogue):
-//   * qqmm_pair_kernel (every plain and batched call): a cluster of two CTAs
+//   * qqmm_pair_kernel (every plain, batched and fused call): a cluster of two CTAs
 //     on two SMs owns 256 x 256 output tiles and one thread issues
 //     tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale (M 256, N 256, K 64;
 //     4X with E4M3 scales for NVFP4, 2X with E8M0 for MXFP4), each CTA holding
@@ -21,10 +21,12 @@
 //     by alpha, rounds to bf16, releases the accumulator to the next tile's
 //     MMAs and writes through a swizzled shared-memory stage with TMA tensor
 //     stores.
-//   * qqmm_kernel (the fused quantized-activation call, which needs a
-//     cooperative grid, and the fallback when no CTA pair can be resident):
-//     one CTA per SM, 128 x 256 tiles, tcgen05 cta_group::1, a 4-stage ring,
-//     scale tiles by 1-D bulk copies, per-thread row stores.
+//   * the fused quantized-activation call (qqmm_quantize_x) launches the pair
+//     kernel cooperatively with clusters of two: a quantize prologue (below)
+//     writes x's codes and tiled scales before the mainloop reads them;
+//   * qqmm_kernel (the fallback when no CTA pair can be resident): one CTA per
+//     SM, 128 x 256 tiles, tcgen05 cta_group::1, a 4-stage ring, scale tiles
+//     by 1-D bulk copies, per-thread row stores.
 //   * every mbarrier wait is bounded; an expired wait records an error word
 //     and the protocol continues, so the kernels always terminate.
 #include <algorithm>
