@@ -30,10 +30,11 @@ def separate(B, mode, x, wq, sw, gw, gx=None):
 
 @pytest.mark.parametrize("mode,static_gs", [(2, False), (2, True), (1, False)])
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (200, 264, 768), (1024, 17408, 5120), (300, 4096, 2048),
-                                   (4096, 512, 5120)])
+                                   (4096, 512, 5120), (2048, 17408, 5120), (8192, 17408, 5120)])
 def test_fused_equals_separate_launches(B, mode, static_gs, M, N, K):
     """(4096, 512, 5120): each CTA's share of x is larger than the shared-memory
-    ring, so the quantize pass streams part of it a second time."""
+    ring, so the quantize pass streams part of it a second time.  M = 1024, 2048
+    and 8192 x 17408 x 5120 are the shapes the bench times."""
     x = synth.activations_with_outliers(M, K, seed=M + K, outlier_seed=5).cuda()
     w = synth.bf16_normal((N, K), 0.02, seed=N, device="cuda")
     gw = B.fp4_amax_global_scale(w) if mode == 2 else None
