@@ -67,21 +67,23 @@ def test_qqmv_is_qmv_of_the_dequantized_activation(B, mode, use_gs_x):
 
 
 @pytest.mark.parametrize("mode", [2, 1])
-@pytest.mark.parametrize("N", [3 * synth.HIDDEN, 2 * synth.MLP])
+@pytest.mark.parametrize("N", [3 * synth.HIDDEN, synth.HIDDEN, 2 * synth.MLP])
 def test_qqmv_fused_decode_shapes_sampled(B, mode, N):
-    """The fused decode projections (q|k|v [15360, 5120], gate|up [34816, 5120])
-    with an activation global scale for NVFP4; sampled rows."""
+    """The fused decode projections (q|k|v [15360, 5120], o [5120, 5120] with
+    K split over clusters, gate|up [34816, 5120]) with an activation global
+    scale for NVFP4; sampled rows."""
     rows = np.unique(np.concatenate([np.arange(8), N - 1 - np.arange(8),
                                      np.random.default_rng(N).integers(0, N, 240)]))
     y, ref, _ = run(B, mode, N, synth.HIDDEN, seed=N + mode, use_gs_x=(mode == 2), rows=rows)
     assert_close_to_oracle(y, ref, f"qqmv fused {N} mode {mode}")
 
 
-def test_qqmv_down_projection_split_k(B):
+@pytest.mark.parametrize("mode", [2, 1])
+def test_qqmv_down_projection_split_k(B, mode):
     """K = 17408 (the down projection): the x blocks are quantized per CTA slice
     of a split-K cluster."""
     N, K = synth.HIDDEN, synth.MLP
     rows = np.unique(np.concatenate([np.arange(8), N - 1 - np.arange(8),
                                      np.random.default_rng(5).integers(0, N, 240)]))
-    y, ref, _ = run(B, 2, N, K, seed=17, use_gs_x=True, rows=rows)
-    assert_close_to_oracle(y, ref, "qqmv down")
+    y, ref, _ = run(B, mode, N, K, seed=17, use_gs_x=(mode == 2), rows=rows)
+    assert_close_to_oracle(y, ref, f"qqmv down mode {mode}")
