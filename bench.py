@@ -402,6 +402,33 @@ def bench_qqmm(B, device, Ms=(1024, 2048, 8192), reps=20):
     return res
 
 
+def bench_qqmm_mxfp4(B, device, Ms=(1024, 2048, 8192), reps=20):
+    """The same GEMM with MXFP4 operands (E8M0 scales per 32, no global scale)."""
+    N, K = 17408, 5120
+    w = synth.bf16_normal((N, K), 0.02, seed=1, device=device)
+    wq, ws_w = B.fp4_quantize(w, B.MODE_MXFP4, layout=B.SCALES_TILED)
+    del w
+    res = {}
+    for M in Ms:
+        x = synth.bf16_normal((M, K), 1.0, seed=2, device=device)
+        xq, xs = B.fp4_quantize(x, B.MODE_MXFP4, layout=B.SCALES_TILED)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        for _ in range(3):  # warm-up
+            B.qqmm(xq, xs, wq, ws_w, None, None, mode=B.MODE_MXFP4, out=out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            B.qqmm(xq, xs, wq, ws_w, None, None, mode=B.MODE_MXFP4, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps if reps else float("nan")
+        flops = 2.0 * M * N * K
+        res[f"M{M}"] = {"ms": ms, "TFLOP/s": flops / ms / 1e9, "flops": flops}
+        del x, xq, xs, out
+    return res
+
+
 def bench_qmm(B, device, Ms=(1024, 2048, 8192), reps=20):
     """Dense W4A16 prefill GEMM M x 17408 x 5120: bf16 activations against NVFP4
     (group 16, global scale) and affine-4 group-64 weights."""
@@ -727,6 +754,7 @@ def run_ours(args):
     if not args.quick and rank == 0:
         comps["quantize_4096x5120"] = bench_quantize(B, device)
         comps["qqmm_nvfp4_Mx17408x5120"] = bench_qqmm(B, device)
+        comps["qqmm_mxfp4_Mx17408x5120"] = bench_qqmm_mxfp4(B, device)
         comps["gather_qmm_mxfp4_moe"] = bench_gather(B, device)
         comps["qmm_w4a16_Mx17408x5120"] = bench_qmm(B, device)
         for fmt in comps["qmm_w4a16_Mx17408x5120"].values():
@@ -736,6 +764,8 @@ def run_ours(args):
         for k, v in comps["qqmm_nvfp4_Mx17408x5120"].items():
             v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
             v["frac_of_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+        for k, v in comps["qqmm_mxfp4_Mx17408x5120"].items():
+            v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
         for k, v in comps["gather_qmm_mxfp4_moe"].items():
             v["frac_of_bf16_peak"] = v["TFLOP/s"] / peaks["bf16_tflops"]
             if "TFLOP/s_routed_order" in v:
