@@ -821,7 +821,8 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_pair_kernel(
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty0);
+      // (the loads have completed: the signal publishes no memory, so no release)
+      if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty0);
       uint32_t o[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e)
