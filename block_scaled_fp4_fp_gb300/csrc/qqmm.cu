@@ -177,20 +177,33 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// All CTAs of the grid meet: bar[0] counts arrivals, the last one resets it and
-// bumps the generation bar[1]; the others wait (bounded) for the bump.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.add.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// All CTAs of the grid meet on one word, bar[0]: the arrival count in bits 0-30
+// and a generation in bit 31.  Thread 0 of each CTA arrives with one
+// acquire-release add (its CTA's writes, ordered before it by the CTA barrier,
+// are released; the last arrival acquires everyone's).  The last arrival clears
+// the count and flips the generation with a single release add (count n -> 0
+// and bit 31 toggled, modulo 2^32); the others wait (bounded) for the flip.  A
+// zero-filled word is a valid start and every barrier leaves the count at 0.
 __device__ void grid_barrier(unsigned* bar, unsigned* err, bool& failed) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_gpu(bar + 1);
-    __threadfence();
-    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
+    const unsigned n = gridDim.x;
+    const unsigned old = atom_add_acq_rel_gpu(bar, 1u);
+    const unsigned gen = old & 0x80000000u;
+    if ((old & 0x7fffffffu) == n - 1) {
+      red_add_release_gpu(bar, 0x80000000u - n);
     } else if (!failed) {
       const long long t0 = clock64();
-      while (ld_acquire_gpu(bar + 1) == gen) {
+      while ((ld_acquire_gpu(bar) & 0x80000000u) == gen) {
         if (clock64() - t0 > kWaitLimitCycles) {
           record_error(err, kErrTimeout);
           failed = true;
@@ -198,7 +211,6 @@ __device__ void grid_barrier(unsigned* bar, unsigned* err, bool& failed) {
         }
       }
     }
-    __threadfence();
   }
   __syncthreads();
 }
