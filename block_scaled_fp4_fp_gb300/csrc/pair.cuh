@@ -22,26 +22,23 @@ __device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(caddr) : "memory");
-}
-// The same arrive without release semantics, for a signal that publishes no
-// memory: "this thread's tensor-memory reads are complete" (after
-// tcgen05.wait::ld and tcgen05.fence::before_thread_sync), which frees the
-// accumulator for the next tile's MMAs.  A release at cluster scope waits
-// for memory traffic still in flight on the SM; measured on the qqmm pair
-// kernel, that held each epilogue warp ~0.7 us per tile while the next
-// tile's TMA loads landed, and the tensor pipe idled meanwhile.
+// Arrivals on an mbarrier of another CTA of the cluster (shared::cluster
+// address).  Neither carries a cluster-scope release: such a release waits for
+// the memory traffic still in flight on the arriving SM (measured: on the qqmm
+// pair kernel it held each epilogue warp ~0.7 us a tile while the next tile's
+// TMA loads landed; on the W4A16 pair kernel's stage forwarding it capped
+// NVFP4 at ~1370 TFLOP/s, ~1750 without it).
+//
+// Relaxed: for a signal that publishes no memory, "this thread's
+// tensor-memory reads are complete" (after tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync), which frees the accumulator for the next
+// tile's MMAs.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(caddr) : "memory");
 }
-// Arrive on a barrier of another CTA of the pair with release at CTA scope: it
-// orders this CTA's prior shared-memory writes (already made visible to the
-// async proxy by fence.proxy.async), the operands that the pair's MMAs read
-// from this CTA's shared memory.  The cluster-scope release above also waited
-// for the SM's in-flight global loads; on the W4A16 pair kernel's stage
-// forwarding that capped NVFP4 at ~1370 TFLOP/s (~1750 with this form).
+// Release at CTA scope: orders this CTA's prior shared-memory writes (already
+// made visible to the async proxy by fence.proxy.async), the operands that the
+// pair's MMAs read from this CTA's own shared memory.
 __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" :: "r"(caddr) : "memory");
 }
