@@ -395,7 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_kernel(
         }
       }
     }
-    // no copy may still be in flight when the block retires (the MMA thread may have given up)
+    // no copy may still be in flight when the block retires (the MMA thread may
+    // have given up): thread 0's TMA boxes land on the last stages' barriers,
+    // waited for (bounded) even after an earlier wait expired
+    if (t == 0) {
+      bool drain_failed = false;
+      for (int kb = max(0, num_kb - STAGES); kb < num_kb; ++kb)
+        mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1, err, drain_failed);
+    }
     if (!DENSE) asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ------------------------------------------------------------ MMA warp --
@@ -623,6 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_pair_kernel(
           if (lane == 0) mbar_arrive(&full[s]);  // this CTA's barrier
         }
       }
+    }
+    // no TMA box of either CTA may still be landing when the pair retires: CTA 0's
+    // stage barriers count both CTAs' bytes; waited for (bounded) even after an
+    // earlier wait expired
+    if (t == 0 && rank == 0) {
+      bool drain_failed = false;
+      for (int kb = max(0, num_kb - STAGES); kb < num_kb; ++kb)
+        mbar_wait_cluster(&full[kb % STAGES], (kb / STAGES) & 1, err, drain_failed);
     }
   } else if (rank == 0) {
     // ------------------------------------------------- MMA issuer (CTA 0) --

@@ -246,9 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_affine_kernel(
         tma_load_2d(ss + geo.RG * 16 * geo.sbytes, tmB, &full[s], kb * (KS / GROUP), r0);
         if (++s == geo.nslots) { s = 0; ++round; }
       }
-      // no copy may still be writing shared memory when the CTA exits
+      // no copy may still be writing shared memory when the CTA exits (the waits
+      // run, bounded, even after an earlier one expired)
+      bool drain_failed = false;
       for (int i = max(0, nst - geo.nslots); i < nst; ++i)
-        mbar_wait(&full[i % geo.nslots], (i / geo.nslots) & 1, err, failed);
+        mbar_wait(&full[i % geo.nslots], (i / geo.nslots) & 1, err, drain_failed);
       // every weight byte of this CTA has landed: warm L2 for the next launch (AffNext)
       if (next.count > 0) {
         const int ncta = next.blk0[next.count] * next.split;

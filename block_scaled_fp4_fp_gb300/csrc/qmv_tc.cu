@@ -303,9 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmv_tc_kernel(const __grid_consta
         tma_load_2d(smem + offS + s * sslot, tmS, &wfull[s], (kb0 + i) * G::kSB, r0);
         if (++s == nslots) { s = 0; ++round; }
       }
-      // no copy may still be writing shared memory when the CTA exits
+      // no copy may still be writing shared memory when the CTA exits (the waits
+      // run, bounded, even after an earlier one expired)
+      bool drain_failed = false;
       for (int i = max(0, nst - nslots); i < nst; ++i)
-        mbar_wait(&wfull[i % nslots], (i / nslots) & 1, err, failed);
+        mbar_wait(&wfull[i % nslots], (i / nslots) & 1, err, drain_failed);
       // every weight byte of this CTA has landed: warm L2 for the next launch (see
       // QmvNext).  Issued any earlier, the prefetches compete with the last CTAs'
       // own loads and lengthen this launch (measured on the fused decode stack).

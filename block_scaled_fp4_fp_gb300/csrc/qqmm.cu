@@ -504,9 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_kernel(
                       &full[s]);
         }
       }
-      // drain: every stage's last fill has landed before the CTA may exit
+      // drain: every stage's last fill has landed before the CTA may exit (the
+      // waits run, bounded, even after an earlier one expired)
+      bool drain_failed = false;
       for (int k = (g > STAGES ? g - STAGES : 0); k < g; ++k)
-        mbar_wait(&full[k % STAGES], (k / STAGES) & 1, err, failed);
+        mbar_wait(&full[k % STAGES], (k / STAGES) & 1, err, drain_failed);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer --
@@ -759,10 +761,13 @@ __global__ void __launch_bounds__(kThreads, 1) qqmm_pair_kernel(
           tma2_load_4d(st + P::AB_BYTES + 2 * P::SF_BYTES, &tmSB, fb, 0, ty, n_blk * 2 + 1, b * bt.wz);
         }
       }
-      // drain (CTA 0 sees both CTAs' fills): nothing may land after the pair retires
-      if (rank == 0)
+      // drain (CTA 0 sees both CTAs' fills): nothing may land after the pair
+      // retires, so these waits run (bounded) even after an earlier one expired
+      if (rank == 0) {
+        bool drain_failed = false;
         for (int k = (g > kPairStages ? g - kPairStages : 0); k < g; ++k)
-          mbar_wait_cluster(&full[k % kPairStages], (k / kPairStages) & 1, err, failed);
+          mbar_wait_cluster(&full[k % kPairStages], (k / kPairStages) & 1, err, drain_failed);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer (CTA 0) --

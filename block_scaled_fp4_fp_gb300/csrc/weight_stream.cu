@@ -58,8 +58,11 @@ __global__ void __launch_bounds__(kThreadsS, 1) weight_stream_kernel(const __gri
       tma_load_2d(smem + offS + s * sslot, &tmS, &full[s], (kb0 + i) * 16, r0);
       if (++s == nslots) { s = 0; ++round; }
     }
-    // no copy may still be writing shared memory when the CTA exits
-    for (int i = max(0, nkb - nslots); i < nkb; ++i) mbar_wait(&full[i % nslots], (i / nslots) & 1, err, failed);
+    // no copy may still be writing shared memory when the CTA exits (bounded
+    // waits, even after an earlier one expired)
+    bool drain_failed = false;
+    for (int i = max(0, nkb - nslots); i < nkb; ++i)
+      mbar_wait(&full[i % nslots], (i / nslots) & 1, err, drain_failed);
   } else if (threadIdx.x == 32) {
     asm volatile("griddepcontrol.wait;" ::: "memory");  // as the GEMV, which consumes after the previous kernel
     int s = 0, round = 0;
