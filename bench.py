@@ -429,6 +429,64 @@ def bench_qqmm_mxfp4(B, device, Ms=(1024, 2048, 8192), reps=20):
     return res
 
 
+def bench_qqmm_cublaslt(B, device, Ms=(1024, 2048, 8192), reps=20):
+    """Side comparison only: the same FP4 GEMMs through cuBLASLt's block-scaled
+    kernels (torch._scaled_mm on float4_e2m1fn_x2 operands), fed the very bytes
+    this library's quantizer wrote: packed codes as [rows, K/2] bytes and the
+    128x4-tiled scales as E4M3 (NVFP4) or E8M0 (MXFP4) bytes.  The output, times
+    alpha, is compared with qqmm's, which also checks that the nibble order and
+    the tile layout read the same way in both.  Never on the product path."""
+    N, K = 17408, 5120
+    f4 = getattr(torch, "float4_e2m1fn_x2", None)
+    e8 = getattr(torch, "float8_e8m0fnu", None)
+    if f4 is None:
+        return {"unavailable": "this PyTorch has no float4_e2m1fn_x2"}
+    res = {}
+    for name, mode, sdt in (("nvfp4", B.MODE_NVFP4, torch.float8_e4m3fn), ("mxfp4", B.MODE_MXFP4, e8)):
+        if sdt is None:
+            res[name] = {"unavailable": "this PyTorch has no float8_e8m0fnu"}
+            continue
+        w = synth.bf16_normal((N, K), 0.02, seed=1, device=device)
+        gw = B.fp4_amax_global_scale(w) if mode == B.MODE_NVFP4 else None
+        wq, ws_w = B.fp4_quantize(w, mode, global_scale=gw, layout=B.SCALES_TILED)
+        del w
+        bt = wq.view(torch.uint8).view(f4).t()  # [K/2, N], column-major
+        sb = ws_w.view(torch.uint8).view(sdt).reshape(-1)
+        for M in Ms:
+            x = synth.bf16_normal((M, K), 1.0, seed=2, device=device)
+            gx = B.fp4_amax_global_scale(x) if mode == B.MODE_NVFP4 else None
+            xq, xs = B.fp4_quantize(x, mode, global_scale=gx, layout=B.SCALES_TILED)
+            a = xq.view(torch.uint8).view(f4)
+            sa = xs.view(torch.uint8).view(sdt).reshape(-1)
+            rec = {}
+            try:
+                ref = torch._scaled_mm(a, bt, sa, sb, out_dtype=torch.bfloat16)
+                ours = B.qqmm(xq, xs, wq, ws_w, gx, gw, mode=mode)
+                alpha = (gx * gw).item() if gx is not None else 1.0
+                d = ref.float() * alpha - ours.float()
+                rec["rel_l2_vs_qqmm"] = (d.norm() / ours.float().norm()).item()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                for _ in range(3):
+                    torch._scaled_mm(a, bt, sa, sb, out_dtype=torch.bfloat16, out=ref)
+                ts = []
+                for _ in range(3):
+                    e0.record()
+                    for _ in range(reps):
+                        torch._scaled_mm(a, bt, sa, sb, out_dtype=torch.bfloat16, out=ref)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) / max(reps, 1))
+                ms = statistics.median(ts)
+                rec["ms"] = ms
+                rec["TFLOP/s"] = 2.0 * M * N * K / ms / 1e9
+            except Exception as e:  # cuBLASLt or this PyTorch may not take the shape or format
+                rec = {"unavailable": f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"}
+            res.setdefault(name, {})[f"M{M}"] = rec
+            del x, xq, xs, a, sa
+        del wq, ws_w, bt, sb
+    return res
+
+
 def bench_qmm(B, device, Ms=(1024, 2048, 8192), reps=20):
     """Dense W4A16 prefill GEMM M x 17408 x 5120: bf16 activations against NVFP4
     (group 16, global scale) and affine-4 group-64 weights."""
@@ -613,6 +671,8 @@ def run_case(args):
             stack.step()
     elif c.startswith("qqmm_m"):
         bench_qqmm(B, dev, Ms=(int(c[len("qqmm_m"):]),), reps=1)
+    elif c.startswith("cublaslt_m"):
+        print(json.dumps(bench_qqmm_cublaslt(B, dev, Ms=(int(c[len("cublaslt_m"):]),), reps=5)))
     elif c == "quantize":
         bench_quantize(B, dev, reps=2)
     elif c.startswith("qqmm_fused_m"):
@@ -755,6 +815,7 @@ def run_ours(args):
         comps["quantize_4096x5120"] = bench_quantize(B, device)
         comps["qqmm_nvfp4_Mx17408x5120"] = bench_qqmm(B, device)
         comps["qqmm_mxfp4_Mx17408x5120"] = bench_qqmm_mxfp4(B, device)
+        comps["qqmm_cublaslt_side_comparison"] = bench_qqmm_cublaslt(B, device)
         comps["gather_qmm_mxfp4_moe"] = bench_gather(B, device)
         comps["qmm_w4a16_Mx17408x5120"] = bench_qmm(B, device)
         for fmt in comps["qmm_w4a16_Mx17408x5120"].values():
@@ -766,6 +827,11 @@ def run_ours(args):
             v["frac_of_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
         for k, v in comps["qqmm_mxfp4_Mx17408x5120"].items():
             v["frac_of_fp4_peak"] = v["TFLOP/s"] / fp4_peak
+        for fmt, d in comps["qqmm_cublaslt_side_comparison"].items():
+            ours = comps["qqmm_nvfp4_Mx17408x5120" if fmt == "nvfp4" else "qqmm_mxfp4_Mx17408x5120"]
+            for M, v in (d.items() if isinstance(d, dict) else ()):
+                if isinstance(v, dict) and "TFLOP/s" in v and M in ours:
+                    v["qqmm_over_cublaslt"] = ours[M]["TFLOP/s"] / v["TFLOP/s"]
         for k, v in comps["gather_qmm_mxfp4_moe"].items():
             v["frac_of_bf16_peak"] = v["TFLOP/s"] / peaks["bf16_tflops"]
             if "TFLOP/s_routed_order" in v:
@@ -831,7 +897,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", default=None,
                     help="profiling case: qmv_nvfp4[_fused]|qmv_mxfp4[_fused]|qmv_affine[_fused]|qqmv_nvfp4_fused|"
-                         "qqmm_m<M>|qqmm_fused_m<M>|qmm_m<M>|quantize|gather")
+                         "qqmm_m<M>|qqmm_fused_m<M>|qmm_m<M>|cublaslt_m<M>|quantize|gather")
     args = ap.parse_args()
     if args.case:
         run_case(args)
