@@ -156,9 +156,9 @@ struct Batch {
 // quantized by every CTA of the (co-resident, cooperative) grid into the
 // caller's workspace -- codes xq and the 128x4-tiled scales sx the GEMM then
 // reads -- after, when no activation global scale is given (NVFP4), the tensor
-// amax reduced across the grid.  Grid barriers count arrivals in bar[0] and
-// release through the generation word bar[1] (both zero before the first call,
-// and left so); their waits are bounded.
+// amax reduced across the grid.  Grid barriers use one word, bar[0] (arrival
+// count and generation bit; zero before the first call, and each barrier
+// leaves the count at zero); their waits are bounded.
 struct FusedX {
   const uint16_t* x = nullptr;
   const float* gs_in = nullptr;  // NVFP4 activation global scale, or nullptr: amax / 2688 from x
