@@ -71,3 +71,30 @@ def test_fused_matches_oracle(B):
                             torch.from_numpy(oracle.tile_scales(os_)).cuda(), ws, None,
                             torch.tensor(gw, dtype=torch.float32, device="cuda"), mode=2)
     assert_close_to_oracle(out, ref, "fused qqmm")
+
+
+def test_fused_timeout_injection_reports_and_recovers(B):
+    """A bounded wait made to expire inside the fused launch (the MMA thread's
+    first wait, after the quantize prologue and both grid barriers): the call
+    reports FP4_ERR_TIMEOUT, still writes the right product (the expiry is on a
+    separate flag, so the protocol continues), and the same workspace serves the
+    next call -- its grid-barrier word was left at a zero count."""
+    M, N, K = 256, 512, 1024
+    x = synth.bf16_normal((M, K), 1.0, seed=21, device="cuda")
+    w = synth.bf16_normal((N, K), 0.02, seed=22, device="cuda")
+    gw = B.fp4_amax_global_scale(w)
+    wq, sw = B.fp4_quantize(w, 2, global_scale=gw, layout=B.SCALES_TILED)
+    ref, _, _, _ = separate(B, 2, x, wq, sw, gw)
+    ws = B.qqmm_quantize_x_workspace(M, K, 2)
+    B.fp4_debug_inject_wait_timeout(True)
+    try:
+        out = B.qqmm_quantize_x(x, wq, sw, ws, None, gw, mode=2)
+        torch.cuda.synchronize()
+        assert B.fp4_check_device_error() == B.FP4_ERR_TIMEOUT
+    finally:
+        B.fp4_debug_inject_wait_timeout(False)
+    assert np.array_equal(bf16_u16(out), bf16_u16(ref))
+    out = B.qqmm_quantize_x(x, wq, sw, ws, None, gw, mode=2)
+    torch.cuda.synchronize()
+    assert B.fp4_check_device_error() == B.FP4_OK
+    assert np.array_equal(bf16_u16(out), bf16_u16(ref))
